@@ -22,6 +22,7 @@
 //   * the quantiser is group-wise asymmetric min-max along D with a float
 //     zero equal to the group minimum, scale = (max-min)/(2^b-1), both
 //     stored as IEEE binary16;
+//   * a group minimum of -0 is taken as +0 (signed zeros compare equal);
 //   * codes are computed with the STORED fp16 scale and zero, in fp32:
 //     u = (x - z) / s (separate round-to-nearest subtraction and IEEE
 //     division), code = clamp(rint_half_even(u), 0, 2^b-1); a group whose
@@ -158,6 +159,10 @@ int oracle_quantize_row(const uint16_t* x, int D, int G, int bits, uint8_t* code
       if (v < mn) mn = v;
       if (v > mx) mx = v;
     }
+    // Signed zeros compare equal, so "the minimum" of a group holding both
+    // -0 and +0 has no defined sign; adding +0 maps -0 to +0 and leaves every
+    // other value unchanged, so the stored zero never depends on scan order.
+    mn = mn + 0.0f;
     const float range = mx - mn;                              // fp32, round to nearest
     const float s32 = range / static_cast<float>(qmax);       // fp32 IEEE division
     const uint16_t sh = oracle_f32_to_f16(s32);

@@ -126,7 +126,7 @@ def pin_quantiser_scale_zero(plant: int = 0):
         for g in range(len(s)):
             grp = xv[g * G:(g + 1) * G]
             mn, mx = float(grp.min()), float(grp.max())
-            assert z[g] == np.float16(np.float32(mn)).view(np.uint16), "zero != fp16(min)"
+            assert z[g] == np.float16(np.float32(mn) + np.float32(0.0)).view(np.uint16), "zero != fp16(min)"
             sv = float(_f16_value(s[g]))
             rng_ = mx - mn
             # |s - range/qmax| <= half an fp16 ulp of s (+ subnormal spacing) + fp32 rounding
@@ -162,6 +162,17 @@ def pin_quantiser_constant_group(plant: int = 0):
             deq = oracle.dequant_row(codes, s, z, 32, plant)
             assert np.array_equal(deq, _bf16_value(x).astype(np.float64)
                                   if val != 1e-3 else _f16_value(z).repeat(32))
+
+
+def pin_signed_zero_minimum(plant: int = 0):
+    """A group whose minimum is a signed zero stores the zero as +0 whatever
+    the order of -0 and +0 in the row (signed zeros compare equal)."""
+    for order in ((-0.0, 0.0), (0.0, -0.0)):
+        vals = np.full(32, 0.5)
+        vals[3], vals[17] = order
+        codes, s, z = oracle.quantize_row(_bf16_bits_from_float(vals), 32, 4, plant)
+        assert int(z[0]) == 0, hex(int(z[0]))
+        assert codes[3] == 0 and codes[17] == 0 and codes[0] == 15
 
 
 def pin_round_trip_bound(plant: int = 0):
@@ -336,6 +347,7 @@ ALL_PINS = [
     pin_quantiser_scale_zero,
     pin_quantiser_exact_grid,
     pin_quantiser_constant_group,
+    pin_signed_zero_minimum,
     pin_round_trip_bound,
     pin_pack_worked_examples,
     pin_pack_roundtrip,
