@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the compressed-KV attention path on one GB300.
+
+Workload (default): the LLaVA-OneVision-7B-shaped decode step -- 28 layers,
+B = 1, 28 query / 4 KV heads, D = 128, a history of 14 text + 6273 visual
+positions (K INT4, V INT2, group 64, KV head 0 protected in bf16).  One step
+= for every layer: kvq_quantize_append of the step's own K/V row (a text
+position, kept bf16) and kvq_decode_attention over the history plus that
+row.  The history is quantised once before timing (prefill).
+
+value  = algorithmic bytes per step / device time per step (GB/s), where the
+         bytes are the compressed cache rows actually attended, q, out and
+         the appended row (read + write); ms_per_step is the same time.
+e2e    = the same step through the public API with pinned HOST buffers: the
+         H2D copy of every layer's q and step K/V and the D2H copy of every
+         layer's output are inside the timed region.
+L2 is flushed (a write of 2x the L2 size) before every timed step, outside
+the timed interval.
+
+--impl reference times the CPU oracle (test infrastructure) on the host
+cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("decode-attention µs/step and achieved HBM GB/s (compressed bytes) vs 8 TB/s peak")
+UNIT = "GB/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llava_ov_7b")
+    ap.add_argument("--T", type=int, default=None, help="history length for the longctx workload")
+    ap.add_argument("--layers", type=int, default=None, help="limit layers (parity/debug only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: one independent copy of the workload per rank)
+# ---------------------------------------------------------------------------
+
+def dist_setup(use_cuda: bool):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if use_cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if use_cuda else "gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier(world: int, use_cuda: bool):
+    if use_cuda:
+        torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if use_cuda:
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, world: int, use_cuda: bool) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, use_cuda: bool) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks (sampled with nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def decode_bytes(L, T: int) -> int:
+    """Compressed cache bytes a decode over positions [0, T) must read, plus q
+    and out.  A packed visual row costs its codes plus its fp16 scale/zero."""
+    d = L.d
+    vsa, vea = min(d.vis_start, T), min(d.vis_end, T)
+    n_vis = vea - vsa
+    n_txt = T - n_vis
+    bf16_row = 2 * d.D
+    packed = sum(int(L.row_bytes[s]) for s in range(4))  # K codes, K s/z, V codes, V s/z
+    per_b = (d.H_kv * n_txt * 2 * bf16_row + L.n_prot * n_vis * 2 * bf16_row
+             + L.n_packed * n_vis * packed)
+    qo = 2 * d.B * d.H_q * d.D * 2
+    return d.B * per_b + qo
+
+
+def append_bytes(L, n_tok: int) -> int:
+    """Read of the step's bf16 K/V rows plus the write of their cache rows
+    (text positions: bf16)."""
+    d = L.d
+    return 2 * (d.B * d.H_kv * n_tok * 2 * 2 * d.D)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Model:
+    """Per-layer caches (history quantised once), per-step inputs, outputs."""
+
+    def __init__(self, w: synth.Workload, dev, n_layers: int):
+        import bit_mixed_precision_kvq_gb300 as kvq
+        self.kvq = kvq
+        self.w = w
+        self.T_hist = w.T
+        self.T = w.T + 1
+        self.layers = []
+        ws_bytes = 0
+        for l in range(n_layers):
+            ls = w.layers[l]
+            L = kvq.cache_layout(w.B, w.H_q, w.H_kv, w.D, self.T, w.vis_start, w.vis_end,
+                                 ls.k_bits, ls.v_bits, w.group_size, ls.protected)
+            cache = torch.empty(int(L.total_bytes), dtype=torch.uint8, device=dev)
+            k = synth.make_kv(w, l, "k", dev)
+            v = synth.make_kv(w, l, "v", dev)
+            kvq.quantize_append(L, cache, k, v, 0)
+            del k, v
+            self.layers.append(dict(L=L, cache=cache))
+            ws_bytes = max(ws_bytes, int(L.workspace_bytes))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        nL = n_layers
+        # per-step device inputs/outputs, packed per layer so that the e2e leg
+        # moves them with one copy each way
+        self.q = torch.stack([synth.make_q(w, l, 0, dev) for l in range(nL)])
+        self.ks = torch.stack([synth.make_step_kv(w, l, "k", 0, dev) for l in range(nL)])
+        self.vs = torch.stack([synth.make_step_kv(w, l, "v", 0, dev) for l in range(nL)])
+        self.out = torch.empty((nL, w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        self.scale = 1.0 / math.sqrt(w.D)
+        torch.cuda.synchronize()
+
+    def step(self):
+        kvq = self.kvq
+        for l, ly in enumerate(self.layers):
+            L = ly["L"]
+            kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
+            kvq.decode_attention(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
+                                 self.ws)
+
+    def decode_layer(self, l: int):
+        ly = self.layers[l]
+        self.kvq.decode_attention(ly["L"], ly["cache"], self.q[l], self.T, self.out[l],
+                                  self.scale, None, self.ws)
+
+    def step_bytes(self) -> int:
+        return sum(decode_bytes(ly["L"], self.T) + append_bytes(ly["L"], 1) for ly in self.layers)
+
+
+def run_ours(args, rank, world, local):
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    w = synth.workload(args.workload, args.T)
+    n_layers = args.layers or w.n_layers
+    model = Model(w, dev, n_layers)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # eager warm-up (first calls cache the SM count), then capture one step
+    model.step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        model.step()
+    torch.cuda.synchronize()
+    launches_per_step = 3 * n_layers  # append + split + combine per layer
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        graph.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world, True)
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    barrier(world, True)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    dev_ms = max_over_ranks(dev_ms, world, True)
+    step_bytes = model.step_bytes()
+    total_bytes = sum_over_ranks(float(step_bytes) * args.steps, world, True)
+    ms_per_step = dev_ms / args.steps
+    value = total_bytes / (dev_ms * 1e-3) / 1e9
+
+    # roofline: the decode call of one layer (split kernel + combine), timed
+    # per launch with events on the launching stream, L2 flushed before each
+    reps = 20
+    rl_ev = []
+    for r in range(reps):
+        for l in range(n_layers):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            model.decode_layer(l)
+            b.record()
+            rl_ev.append((a, b))
+    torch.cuda.synchronize()
+    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in rl_ev]))
+    layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) for ly in model.layers]))
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = layer_bytes / (launch_ms * 1e-3) / 1e9
+
+    # e2e: pinned host buffers in, outputs back, all inside the timed region
+    h_q = torch.empty(model.q.shape, dtype=model.q.dtype, pin_memory=True)
+    h_ks = torch.empty(model.ks.shape, dtype=model.ks.dtype, pin_memory=True)
+    h_vs = torch.empty(model.vs.shape, dtype=model.vs.dtype, pin_memory=True)
+    h_out = torch.empty(model.out.shape, dtype=model.out.dtype, pin_memory=True)
+    h_q.copy_(model.q)
+    h_ks.copy_(model.ks)
+    h_vs.copy_(model.vs)
+    e2e_ev = []
+    for i in range(args.steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        model.q.copy_(h_q, non_blocking=True)
+        model.ks.copy_(h_ks, non_blocking=True)
+        model.vs.copy_(h_vs, non_blocking=True)
+        graph.replay()
+        h_out.copy_(model.out, non_blocking=True)
+        b.record()
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), world, True)
+    h2d = (h_q.numel() + h_ks.numel() + h_vs.numel()) * 2
+    d2h = h_out.numel() * 2
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, n_layers=min(4, n_layers))
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8/u4/u2 codes + bf16; fp32 accumulate",
+        "data": "synthetic (seeded; shapes of the pages' LLaVA-OneVision-7B video workload)",
+        "config": {"workload": f"{w.name}: {n_layers} layers, B={w.B}, H_q={w.H_q}, "
+                               f"H_kv={w.H_kv}, D={w.D}, T={model.T} (history {w.T} + current), "
+                               f"K{w.layers[0].k_bits}/V{w.layers[0].v_bits} G{w.group_size}, "
+                               f"protected {w.layers[0].protected}",
+                   "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
+                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attention (split + combine launches)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "per_launch_bytes": int(layer_bytes), "per_launch_us": round(launch_ms * 1e3, 3),
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if peaks else
+                                    "fallback 6800 GB/s"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (test infrastructure) as the baseline / reference arm
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: the first
+    `n_layers` layers of one decode step (history + current token)."""
+
+    def __init__(self, w: synth.Workload, n_layers: int):
+        self.w = w
+        self.items = []
+        self.bytes = 0
+        for l in range(n_layers):
+            ls = w.layers[l]
+            k = torch.cat([synth.make_kv(w, l, "k"), synth.make_step_kv(w, l, "k", 0)], 2)
+            v = torch.cat([synth.make_kv(w, l, "v"), synth.make_step_kv(w, l, "v", 0)], 2)
+            q = synth.make_q(w, l, 0)
+            self.items.append((synth.bf16_bits(q), synth.bf16_bits(k), synth.bf16_bits(v), ls))
+            self.bytes += self._bytes(ls, w.T + 1) + 2 * (w.B * w.H_kv * 2 * 2 * w.D)
+
+    def _bytes(self, ls, T):
+        w = self.w
+        D, G = w.D, w.group_size
+        n_vis = min(w.vis_end, T) - min(w.vis_start, T)
+        row = lambda b: D * b // 8 + (4 * D // G if b < 16 else 0)  # noqa: E731
+        n_prot = len(ls.protected)
+        per_b = (w.H_kv * (T - n_vis) * 4 * D + n_prot * n_vis * 4 * D
+                 + (w.H_kv - n_prot) * n_vis * (row(ls.k_bits) + row(ls.v_bits)))
+        return w.B * per_b + 4 * w.B * w.H_q * D
+
+    def run(self, threads: int):
+        import oracle
+        w = self.w
+        for q, k, v, ls in self.items:
+            mask = [1 if h in ls.protected else 0 for h in range(w.H_kv)]
+            oracle.decode_reference(q, k, v, w.vis_start, w.vis_end, mask, ls.k_bits, ls.v_bits,
+                                    w.group_size, 1.0 / math.sqrt(w.D), threads=threads)
+
+
+def cpu_baseline(w: synth.Workload, n_layers: int) -> dict:
+    import oracle
+    oracle.build_oracle()
+    cores = oracle.online_cores()
+    s = OracleSample(w, n_layers)
+    s.run(cores)  # warm
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        s.run(cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > 10.0 or reps >= 20:
+            break
+    per = el / reps
+    return {"value": round(s.bytes / per / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_layers} of {w.n_layers} layers of one {w.name} decode step "
+                      f"(history {w.T} + current), {reps} reps",
+            "us_per_step_extrapolated": round(per * 1e6 * w.n_layers / n_layers, 1)}
+
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return  # the oracle arm runs on rank 0 only; other ranks exit without work
+    import oracle
+    oracle.build_oracle()
+    w = synth.workload(args.workload, args.T)
+    cores = oracle.online_cores()
+    s = OracleSample(w, n_layers=min(2, args.layers or w.n_layers))
+    for _ in range(args.warmup):
+        s.run(cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.run(cores)
+    el = time.perf_counter() - t0
+    value = s.bytes * args.steps / el / 1e9
+    ms = el / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{w.name}: 2 of {w.n_layers} layers per step (bounded sample), "
+                               f"B={w.B}, H_q={w.H_q}, H_kv={w.H_kv}, T={w.T + 1}"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "2 layers of one decode step per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank, world, local = dist_setup(use_cuda=False)
+        run_reference(args, rank, world, local)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (ours) needs a CUDA GPU")
+    rank, world, local = dist_setup(use_cuda=True)
+    run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+"""Thin Python binding of the kvq C ABI (``include/kvq.h``).
+
+Argument marshalling only: every step of the path runs in the CUDA library
+``_lib/libkvq.so`` (built by ``build_native.build()``).  There is no Python
+or CPU fallback -- if the library is missing, ``load()`` raises.
+
+Functions take either torch tensors (device memory, the current torch stream
+by default) or raw integer addresses.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+__all__ = [
+    "KvqError", "load", "lib_path", "cache_layout", "quantize_append", "decode_attention",
+    "kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention", "KVQ_MAX_HEADS",
+    "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
+    "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
+]
+
+KVQ_MAX_HEADS = 128
+KVQ_NSEG = 8
+(SEG_K_CODES, SEG_K_SZ, SEG_V_CODES, SEG_V_SZ, SEG_PROT_K, SEG_PROT_V, SEG_TEXT_K,
+ SEG_TEXT_V) = range(8)
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
+          3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
+EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
+                    "kvq_status_string"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_lib", "libkvq.so")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class LayoutDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("T_cap", ctypes.c_int32), ("vis_start", ctypes.c_int32),
+                ("vis_end", ctypes.c_int32), ("k_bits", ctypes.c_int32),
+                ("v_bits", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("protected_heads", ctypes.c_uint8 * KVQ_MAX_HEADS)]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("d", LayoutDesc), ("g", ctypes.c_int32), ("n_prot", ctypes.c_int32),
+                ("n_packed", ctypes.c_int32), ("Tv", ctypes.c_int32), ("T_text", ctypes.c_int32),
+                ("units", ctypes.c_int32),
+                ("slot", ctypes.c_int32 * KVQ_MAX_HEADS),
+                ("prot_head", ctypes.c_uint8 * KVQ_MAX_HEADS),
+                ("packed_head", ctypes.c_uint8 * KVQ_MAX_HEADS),
+                ("row_bytes", ctypes.c_int64 * KVQ_NSEG), ("off", ctypes.c_int64 * KVQ_NSEG),
+                ("bytes", ctypes.c_int64 * KVQ_NSEG), ("total_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64), ("eff_bits_k", ctypes.c_double),
+                ("eff_bits_v", ctypes.c_double)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"kvq native library missing at {path}; build it with "
+                           "bit_mixed_precision_kvq_gb300.build_native.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    lib.kvq_cache_layout.argtypes = [ctypes.POINTER(LayoutDesc), ctypes.POINTER(Layout)]
+    lib.kvq_cache_layout.restype = ctypes.c_int
+    lib.kvq_quantize_append.argtypes = [ctypes.POINTER(Layout), P, P, P, i64, i64, i64, i32, i32, P]
+    lib.kvq_quantize_append.restype = ctypes.c_int
+    lib.kvq_decode_attention.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P, sz, P]
+    lib.kvq_decode_attention.restype = ctypes.c_int
+    lib.kvq_status_string.argtypes = [ctypes.c_int]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def cache_layout(B: int, H_q: int, H_kv: int, D: int, T_cap: int, vis_start: int, vis_end: int,
+                 k_bits: int, v_bits: int, group_size: int,
+                 protected: Sequence[int] = ()) -> Layout:
+    """kvq_cache_layout: validate the per-layer description and derive the layout.
+    ``protected`` lists the protected KV heads."""
+    d = LayoutDesc(B, H_q, H_kv, D, T_cap, vis_start, vis_end, k_bits, v_bits, group_size)
+    for h in protected:
+        if not 0 <= int(h) < KVQ_MAX_HEADS:
+            raise KvqError(1, "kvq_cache_layout")
+        d.protected_heads[int(h)] = 1
+    out = Layout()
+    st = load().kvq_cache_layout(ctypes.byref(d), ctypes.byref(out))
+    if st != 0:
+        raise KvqError(st, "kvq_cache_layout")
+    return out
+
+
+def quantize_append(L: Layout, cache, k, v, t0: int, n_tok: Optional[int] = None,
+                    strides: Optional[Sequence[int]] = None, stream=None) -> None:
+    """kvq_quantize_append: write positions [t0, t0 + n_tok) of K and V
+    ([B, H_kv, n_tok, D] bf16 on the device) into the cache."""
+    if strides is None:
+        if k.stride() != v.stride():
+            raise ValueError("k and v must share strides")
+        if k.stride(-1) != 1:
+            raise ValueError("last dim must be contiguous")
+        strides = k.stride()[:3]
+        n_tok = k.shape[2] if n_tok is None else n_tok
+    st = load().kvq_quantize_append(ctypes.byref(L), _addr(cache), _addr(k), _addr(v),
+                                    int(strides[0]), int(strides[1]), int(strides[2]), int(t0),
+                                    int(n_tok), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_quantize_append")
+
+
+def decode_attention(L: Layout, cache, q, T: int, out, softmax_scale: Optional[float] = None,
+                     lse=None, workspace=None, ws_bytes: Optional[int] = None,
+                     stream=None) -> None:
+    """kvq_decode_attention: out[b, hq] = softmax(scale q . k) v over positions [0, T)."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kvq_decode_attention(ctypes.byref(L), _addr(cache), _addr(q), int(T),
+                                     float(softmax_scale), _addr(out), _addr(lse),
+                                     _addr(workspace), int(ws_bytes), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_attention")
+
+
+# Same names as the C entry points.
+kvq_cache_layout = cache_layout
+kvq_quantize_append = quantize_append
+kvq_decode_attention = decode_attention

@@ -1,0 +1,171 @@
+// kvq_internal.h -- shared by the library's host code and CUDA kernels.
+//
+// Work decomposition for split-KV decoding (flash-decoding pipeline of the
+// WSVD summary, section 2.라, restated for a mixed-precision cache):
+//   * a "unit" is one (sequence b, KV head h, chunk hc of up to 8 of the g
+//     query heads that read h).  Protected-head units come first, then the
+//     packed-head units; inside each kind the order is (b, slot, hc).
+//   * every unit is a stream of positions 0..T-1; a position costs 512 bytes
+//     (bf16 K + V rows) unless it is a visual position of a packed head,
+//     which costs the packed K and V rows plus their fp16 scale/zero.
+//   * the concatenated byte stream of all units is cut into C chunks of
+//     equal bytes; CTA c processes [cut(c), cut(c+1)).  Cuts inside a packed
+//     visual range are rounded down to a multiple of 16 rows so every staged
+//     tile starts on a 16-byte boundary in every segment.
+//   * CTA c writes one partial result (o, m, l) per unit it touches into
+//     workspace slot u + c.  The (u, c) pairs form a monotone staircase, so
+//     u + c is unique; there are at most units + C - 1 slots.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+#if defined(__CUDACC__)
+#define KVQ_HD __host__ __device__ __forceinline__
+#else
+#define KVQ_HD inline
+#endif
+
+namespace kvq {
+
+constexpr int kD = 128;          // head dimension supported by the kernels
+constexpr int kNH = KVQ_HEADS_PER_UNIT;  // query heads per unit (MMA N = 8)
+constexpr int kBf16PosBytes = 4 * kD;    // K + V bf16 rows of one position
+constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
+
+struct Plan {
+  int32_t U_p;        // protected units
+  int32_t U;          // all units
+  int32_t C;          // chunks (= CTAs of the split kernel)
+  int32_t NHC;        // query-head chunks per KV head
+  int32_t vsa, vea;   // attended visual positions [vsa, vea)
+  int32_t T;          // attended positions
+  int32_t w_vis;      // bytes of one packed visual position (K + V, codes + s/z)
+  int64_t ub_p, ub_u; // bytes of a protected / packed unit
+  int64_t P_bytes;    // U_p * ub_p
+  int64_t total;      // all bytes
+};
+
+struct Cut {
+  int32_t u;  // unit
+  int32_t p;  // position inside the unit
+};
+
+// Start of chunk c, 0 <= c <= C.  Monotone in c (lexicographic in (u, p)).
+KVQ_HD Cut plan_cut(const Plan& P, int32_t c) {
+  Cut r;
+  if (c >= P.C) {
+    r.u = P.U;
+    r.p = 0;
+    return r;
+  }
+  const int64_t X = (P.total * static_cast<int64_t>(c)) / P.C;
+  if (X < P.P_bytes) {
+    const int64_t u = X / P.ub_p;
+    const int64_t rem = X - u * P.ub_p;
+    r.u = static_cast<int32_t>(u);
+    r.p = static_cast<int32_t>(rem / kBf16PosBytes);
+    return r;
+  }
+  const int64_t Xu = X - P.P_bytes;
+  const int64_t u = Xu / P.ub_u;
+  const int64_t rem = Xu - u * P.ub_u;
+  r.u = P.U_p + static_cast<int32_t>(u);
+  const int64_t pre = static_cast<int64_t>(P.vsa) * kBf16PosBytes;
+  const int64_t vis = static_cast<int64_t>(P.vea - P.vsa) * P.w_vis;
+  if (rem < pre) {
+    r.p = static_cast<int32_t>(rem / kBf16PosBytes);
+  } else if (rem < pre + vis) {
+    int64_t row = (rem - pre) / P.w_vis;
+    row -= row % kVisAlign;
+    r.p = P.vsa + static_cast<int32_t>(row);
+  } else {
+    r.p = P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosBytes);
+  }
+  return r;
+}
+
+// Chunks that hold a piece of unit u: [c_first, c_last].
+//   c_last  = max c with cut(c).u <= u
+//   c_first = min c with (cut(c+1).u clamped to U-1) >= u
+KVQ_HD void plan_unit_chunks(const Plan& P, int32_t u, int32_t* c_first, int32_t* c_last) {
+  // c_last: number of c in [0, C) with cut(c).u <= u, minus one (cut(0).u == 0 <= u).
+  int32_t lo = 0, hi = P.C - 1;  // invariant: cut(lo).u <= u
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) / 2;
+    if (plan_cut(P, mid).u <= u) lo = mid; else hi = mid - 1;
+  }
+  *c_last = lo;
+  // c_first: smallest c in [0, C) with end unit >= u; end unit of c = min(cut(c+1).u, U-1).
+  lo = 0;
+  hi = P.C - 1;  // end unit of C-1 is U-1 >= u
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) / 2;
+    int32_t eu = plan_cut(P, mid + 1).u;
+    if (eu > P.U - 1) eu = P.U - 1;
+    if (eu >= u) hi = mid; else lo = mid + 1;
+  }
+  *c_first = lo;
+}
+
+// Everything a kernel needs about one layer and one call (passed by value).
+struct Params {
+  // geometry
+  int32_t B, Hq, Hkv, g, NHC;
+  int32_t T;           // attended positions (decode) / T_cap (append)
+  int32_t vs, ve;      // visual range of the layout
+  int32_t Tv, T_text;
+  int32_t kb, vb, G;
+  int32_t n_prot, n_packed;
+  int32_t krow, kszrow, vrow, vszrow;  // bytes per row of the packed segments
+  // cache segments
+  const uint8_t* seg[KVQ_NSEG];
+  // decode call
+  const uint16_t* q;   // bf16 [B][Hq][D]
+  uint16_t* out;       // bf16 [B][Hq][D]
+  float* lse;          // [B][Hq] or null
+  float* ws_o;         // [slots][kNH][kD]
+  float* ws_ml;        // [slots][kNH][2]
+  float scale_log2;    // softmax_scale * log2(e)
+  Plan plan;
+  uint8_t prot[KVQ_MAX_HEADS];        // head -> protected?
+  int32_t slot[KVQ_MAX_HEADS];        // head -> slot
+  uint8_t prot_head[KVQ_MAX_HEADS];   // protected slot -> head
+  uint8_t packed_head[KVQ_MAX_HEADS]; // packed slot -> head
+};
+
+// unit -> (b, head, hc, protected?)
+struct UnitInfo {
+  int32_t b, h, hc, slot;
+  bool prot;
+};
+
+KVQ_HD UnitInfo unit_info(const Params& p, int32_t u) {
+  UnitInfo r;
+  const bool prot = u < p.plan.U_p;
+  const int32_t v = prot ? u : u - p.plan.U_p;
+  const int32_t nslots = prot ? p.n_prot : p.n_packed;
+  r.b = v / (nslots * p.NHC);
+  const int32_t rem = v - r.b * nslots * p.NHC;
+  r.slot = rem / p.NHC;
+  r.hc = rem - r.slot * p.NHC;
+  r.h = prot ? p.prot_head[r.slot] : p.packed_head[r.slot];
+  r.prot = prot;
+  return r;
+}
+
+// (b, head, hc) -> unit
+KVQ_HD int32_t unit_of(const Params& p, int32_t b, int32_t h, int32_t hc) {
+  const int32_t s = p.slot[h];
+  if (p.prot[h]) return (b * p.n_prot + s) * p.NHC + hc;
+  return p.plan.U_p + (b * p.n_packed + s) * p.NHC + hc;
+}
+
+}  // namespace kvq
+
+// Host helpers implemented in kvq_layout.cpp.
+kvq_status kvq_check_layout(const kvq_layout* L);
+void kvq_fill_params(const kvq_layout* L, kvq::Params* p);
+kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target);
+int kvq_device_sm_count(int* n_sm);

@@ -1,0 +1,191 @@
+// kvq_layout.cpp -- host side of the cache layout, validation and the
+// split-KV work plan.
+//
+// The layout follows the pages' problem statement: a per-layer cache
+// [B, H_kv, T, D] ("VLM_KV_Quantization", section 2) whose visual block is
+// quantised group-wise with separate K and V bit-widths (sections 1 and 4),
+// while text positions and a per-layer set of protected KV heads (HeadGuard
+// brief, key ideas) stay bf16.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kvq_internal.h"
+
+namespace {
+
+constexpr int64_t kAlign = 256;   // segment alignment in the cache buffer
+constexpr int64_t kPad = 256;     // slack after each segment (rounded tile copies)
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool valid_bits(int b) { return b == 2 || b == 4 || b == 8 || b == 16; }
+
+kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
+  if (!desc || !out) return KVQ_ERR_INVALID_ARG;
+  const kvq_layout_desc& d = *desc;
+  if (d.B < 1 || d.H_kv < 1 || d.H_kv > KVQ_MAX_HEADS || d.H_q < 1 || d.H_q % d.H_kv != 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (d.D < 1 || d.D % 32 != 0) return KVQ_ERR_INVALID_ARG;
+  if (d.T_cap < 1) return KVQ_ERR_INVALID_ARG;
+  if (d.vis_start < 0 || d.vis_end < d.vis_start || d.vis_end > d.T_cap) return KVQ_ERR_INVALID_ARG;
+  if (!valid_bits(d.k_bits) || !valid_bits(d.v_bits)) return KVQ_ERR_INVALID_ARG;
+  if (!(d.group_size == 32 || d.group_size == 64 || d.group_size == 128)) return KVQ_ERR_INVALID_ARG;
+  if (d.D % d.group_size != 0) return KVQ_ERR_INVALID_ARG;
+  for (int h = 0; h < KVQ_MAX_HEADS; ++h)
+    if (d.protected_heads[h] > 1 || (h >= d.H_kv && d.protected_heads[h] != 0))
+      return KVQ_ERR_INVALID_ARG;
+  if (d.D != kvq::kD) return KVQ_ERR_UNSUPPORTED;
+
+  kvq_layout L;
+  std::memset(&L, 0, sizeof(L));
+  L.d = d;
+  L.g = d.H_q / d.H_kv;
+  L.Tv = d.vis_end - d.vis_start;
+  L.T_text = d.T_cap - L.Tv;
+  for (int h = 0; h < d.H_kv; ++h) {
+    if (d.protected_heads[h]) {
+      L.slot[h] = L.n_prot;
+      L.prot_head[L.n_prot++] = static_cast<uint8_t>(h);
+    } else {
+      L.slot[h] = L.n_packed;
+      L.packed_head[L.n_packed++] = static_cast<uint8_t>(h);
+    }
+  }
+  const int nhc = (L.g + kvq::kNH - 1) / kvq::kNH;
+  L.units = d.B * d.H_kv * nhc;
+
+  const int64_t D = d.D, G = d.group_size;
+  L.row_bytes[KVQ_SEG_K_CODES] = D * d.k_bits / 8;
+  L.row_bytes[KVQ_SEG_K_SZ] = d.k_bits < 16 ? 4 * D / G : 0;
+  L.row_bytes[KVQ_SEG_V_CODES] = D * d.v_bits / 8;
+  L.row_bytes[KVQ_SEG_V_SZ] = d.v_bits < 16 ? 4 * D / G : 0;
+  L.row_bytes[KVQ_SEG_PROT_K] = 2 * D;
+  L.row_bytes[KVQ_SEG_PROT_V] = 2 * D;
+  L.row_bytes[KVQ_SEG_TEXT_K] = 2 * D;
+  L.row_bytes[KVQ_SEG_TEXT_V] = 2 * D;
+  const int64_t packed_rows = static_cast<int64_t>(d.B) * L.n_packed * L.Tv;
+  const int64_t prot_rows = static_cast<int64_t>(d.B) * L.n_prot * L.Tv;
+  const int64_t text_rows = static_cast<int64_t>(d.B) * d.H_kv * L.T_text;
+  const int64_t rows[KVQ_NSEG] = {packed_rows, packed_rows, packed_rows, packed_rows,
+                                  prot_rows,   prot_rows,   text_rows,   text_rows};
+  int64_t off = 0;
+  for (int s = 0; s < KVQ_NSEG; ++s) {
+    L.off[s] = off;
+    L.bytes[s] = rows[s] * L.row_bytes[s];
+    off = align_up(off + L.bytes[s] + kPad, kAlign);
+  }
+  L.total_bytes = off;
+  // Workspace: one partial (o[8][D] fp32, (m, l)[8]) per slot, slots <= units + C - 1.
+  const int64_t slots = static_cast<int64_t>(L.units) + KVQ_MAX_CTAS - 1;
+  L.workspace_bytes = align_up(slots * kvq::kNH * D * 4, kAlign) + align_up(slots * kvq::kNH * 8, kAlign);
+  L.eff_bits_k = d.k_bits < 16 ? d.k_bits + 32.0 / d.group_size : 16.0;
+  L.eff_bits_v = d.v_bits < 16 ? d.v_bits + 32.0 / d.group_size : 16.0;
+  *out = L;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_cache_layout(const kvq_layout_desc* desc, kvq_layout* out) {
+  return build_layout(desc, out);
+}
+
+extern "C" const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_CAPACITY: return "KVQ_ERR_CAPACITY";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+  }
+  return "kvq_status(unknown)";
+}
+
+// A layout handed back by the caller must be exactly what kvq_cache_layout
+// derives from its own description (guards against corrupted structs).
+kvq_status kvq_check_layout(const kvq_layout* L) {
+  if (!L) return KVQ_ERR_INVALID_ARG;
+  kvq_layout ref;
+  const kvq_status st = build_layout(&L->d, &ref);
+  if (st != KVQ_OK) return st;
+  if (std::memcmp(&ref, L, sizeof(kvq_layout)) != 0) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+void kvq_fill_params(const kvq_layout* L, kvq::Params* p) {
+  std::memset(p, 0, sizeof(*p));
+  const kvq_layout_desc& d = L->d;
+  p->B = d.B;
+  p->Hq = d.H_q;
+  p->Hkv = d.H_kv;
+  p->g = L->g;
+  p->NHC = (L->g + kvq::kNH - 1) / kvq::kNH;
+  p->T = d.T_cap;
+  p->vs = d.vis_start;
+  p->ve = d.vis_end;
+  p->Tv = L->Tv;
+  p->T_text = L->T_text;
+  p->kb = d.k_bits;
+  p->vb = d.v_bits;
+  p->G = d.group_size;
+  p->n_prot = L->n_prot;
+  p->n_packed = L->n_packed;
+  p->krow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES]);
+  p->kszrow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_SZ]);
+  p->vrow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_V_CODES]);
+  p->vszrow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_V_SZ]);
+  for (int h = 0; h < KVQ_MAX_HEADS; ++h) {
+    p->prot[h] = d.protected_heads[h];
+    p->slot[h] = L->slot[h];
+    p->prot_head[h] = L->prot_head[h];
+    p->packed_head[h] = L->packed_head[h];
+  }
+}
+
+kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target) {
+  kvq::Plan P;
+  std::memset(&P, 0, sizeof(P));
+  const kvq_layout_desc& d = L->d;
+  P.T = T;
+  P.NHC = (L->g + kvq::kNH - 1) / kvq::kNH;
+  P.vsa = d.vis_start < T ? d.vis_start : T;
+  P.vea = d.vis_end < T ? d.vis_end : T;
+  P.w_vis = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES] + L->row_bytes[KVQ_SEG_K_SZ] +
+                                 L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ]);
+  P.U_p = d.B * L->n_prot * P.NHC;
+  P.U = d.B * d.H_kv * P.NHC;
+  P.ub_p = static_cast<int64_t>(T) * kvq::kBf16PosBytes;
+  const int64_t n_vis = P.vea - P.vsa;
+  P.ub_u = (static_cast<int64_t>(T) - n_vis) * kvq::kBf16PosBytes + n_vis * P.w_vis;
+  P.P_bytes = static_cast<int64_t>(P.U_p) * P.ub_p;
+  P.total = P.P_bytes + static_cast<int64_t>(P.U - P.U_p) * P.ub_u;
+  // Chunks: the target (a whole number of CTAs per SM), but no chunk below
+  // 8 KiB of cache bytes and never more than KVQ_MAX_CTAS.
+  int64_t C = n_chunks_target;
+  const int64_t by_size = (P.total + 8191) / 8192;
+  if (C > by_size) C = by_size;
+  if (C > KVQ_MAX_CTAS) C = KVQ_MAX_CTAS;
+  if (C < 1) C = 1;
+  P.C = static_cast<int32_t>(C);
+  return P;
+}
+
+int kvq_device_sm_count(int* n_sm) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *n_sm = cache[dev];
+    return 0;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev] = v;
+  *n_sm = v;
+  return 0;
+}

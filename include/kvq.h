@@ -1,0 +1,167 @@
+/*
+ * kvq.h -- decode-time attention over a compressed (mixed-precision) VLM KV
+ * cache, for one NVIDIA GB300 (sm_103a).  C ABI; no CUDA or torch types.
+ *
+ * What the library computes (sources, by page and section):
+ *   - "VLM_KV_Quantization" (nuiw.github.io), section 2: each layer stores a
+ *     K/V cache of shape [B, H_kv, T, D] (e.g. [1, 4, T, 128] for
+ *     LLaVA-OneVision-7B, GQA with 28 query heads over 4 KV heads); K is
+ *     stored after RoPE.  Intro checklist and section 1: only the historical
+ *     cache is compressed, the current/question tokens never are, INT8/INT4/
+ *     INT2 must really cost that many bits per value.  Section 4: K and V get
+ *     their own bit-widths at the same tokens and group size.
+ *   - HeadGuard news brief (jiinsi.com), key ideas: about 1/8 of the physical
+ *     KV heads keep their image K (and V) in bf16; composable with any
+ *     low-bit quantiser.
+ *   - WSVD summary (gist.science 2604.02570), section 2.라: reconstruct K/V on
+ *     chip inside a flash-decoding pipeline (QK, softmax, PV fused) and never
+ *     write the reconstructed tensors back to device memory.
+ *
+ * Readings where the pages are silent (all listed in the design doc):
+ *   quantiser = group-wise asymmetric min-max along D, groups of G consecutive
+ *   elements, scale s = fp16((max - min) / (2^b - 1)), zero z = fp16(min + 0),
+ *   code = clamp(rint_half_even((x - z) / s), 0, 2^b - 1) in fp32 with the
+ *   stored fp16 s and z (code 0 if s == 0); dequantised value = code * s + z.
+ *   Codes are packed little-endian into uint32 words: element d goes to word
+ *   d / (32/b) at bit b * (d mod (32/b)).  bits == 16 keeps bf16.  Query head
+ *   hq reads KV head hq / (H_q / H_kv).
+ *
+ * Conventions for every entry point:
+ *   - All device buffers are allocated and owned by the caller.  The library
+ *     allocates no device memory and keeps no state between calls except a
+ *     per-device cache of the SM count.
+ *   - Every argument is checked on the host before any launch; a failed
+ *     check returns a status and launches nothing.  A launch failure returns
+ *     KVQ_ERR_CUDA.  Faults of already-launched kernels surface at the
+ *     caller's next synchronisation.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and never synchronised by the library.
+ *   - The current CUDA device must be the one that owns the buffers.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_MAX_HEADS 128   /* H_kv limit (mask and slot tables are this long) */
+#define KVQ_NSEG 8          /* number of cache segments */
+#define KVQ_MAX_CTAS 1024   /* upper bound on split-KV work chunks per call */
+#define KVQ_HEADS_PER_UNIT 8 /* query heads handled together per KV head */
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, corrupt layout */
+  KVQ_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D != 128) */
+  KVQ_ERR_CAPACITY = 3,    /* positions beyond T_cap, or workspace too small */
+  KVQ_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} kvq_status;
+
+/* Segments of one layer's cache buffer (see kvq_layout.off / .bytes). */
+enum kvq_segment {
+  KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv][D*k_bits/32]; bf16 rows if k_bits == 16 */
+  KVQ_SEG_K_SZ = 1,    /* half2 (s, z) [B][n_packed][Tv][D/G]; empty if k_bits == 16 */
+  KVQ_SEG_V_CODES = 2, /* as K_CODES with v_bits */
+  KVQ_SEG_V_SZ = 3,    /* as K_SZ with v_bits */
+  KVQ_SEG_PROT_K = 4,  /* bf16 [B][n_prot][Tv][D]: visual K of protected heads */
+  KVQ_SEG_PROT_V = 5,  /* bf16 [B][n_prot][Tv][D] */
+  KVQ_SEG_TEXT_K = 6,  /* bf16 [B][H_kv][T_cap - Tv][D]: every non-visual position */
+  KVQ_SEG_TEXT_V = 7   /* bf16 [B][H_kv][T_cap - Tv][D] */
+};
+
+/* Per-layer description of the cache (the pages' problem statement). */
+typedef struct kvq_layout_desc {
+  int32_t B;          /* sequences in the batch, >= 1 */
+  int32_t H_q;        /* query heads, multiple of H_kv */
+  int32_t H_kv;       /* KV heads, 1..KVQ_MAX_HEADS */
+  int32_t D;          /* head dim; this build supports D == 128 */
+  int32_t T_cap;      /* positions the cache can hold per sequence, >= 1 */
+  int32_t vis_start;  /* visual range [vis_start, vis_end), 0 <= start <= end <= T_cap */
+  int32_t vis_end;
+  int32_t k_bits;     /* 2, 4, 8, or 16 (= bf16, unquantised) */
+  int32_t v_bits;     /* 2, 4, 8, or 16 */
+  int32_t group_size; /* G in {32, 64, 128}, groups of G consecutive elements along D */
+  uint8_t protected_heads[KVQ_MAX_HEADS]; /* 1 = visual K and V of that KV head stay bf16 */
+} kvq_layout_desc;
+
+/* Derived layout (plain value; filled by kvq_cache_layout, read-only after). */
+typedef struct kvq_layout {
+  kvq_layout_desc d;
+  int32_t g;          /* H_q / H_kv */
+  int32_t n_prot;     /* protected KV heads */
+  int32_t n_packed;   /* unprotected KV heads */
+  int32_t Tv;         /* vis_end - vis_start: visual rows per (b, head) */
+  int32_t T_text;     /* T_cap - Tv: text rows per (b, head) */
+  int32_t units;      /* B * H_kv * ceil(g / KVQ_HEADS_PER_UNIT) */
+  int32_t slot[KVQ_MAX_HEADS];        /* head -> index among its kind (protected / packed) */
+  uint8_t prot_head[KVQ_MAX_HEADS];   /* protected slot -> head */
+  uint8_t packed_head[KVQ_MAX_HEADS]; /* packed slot -> head */
+  int64_t row_bytes[KVQ_NSEG];        /* bytes of one row of each segment */
+  int64_t off[KVQ_NSEG];              /* byte offset of each segment (256-byte aligned) */
+  int64_t bytes[KVQ_NSEG];            /* payload bytes of each segment */
+  int64_t total_bytes;                /* size of the cache buffer (segments + padding) */
+  int64_t workspace_bytes;            /* decode workspace needed for any T <= T_cap */
+  double eff_bits_k;                  /* stored bits per visual K value, scale/zero included */
+  double eff_bits_v;
+} kvq_layout;
+
+/*
+ * kvq_cache_layout -- host only, pure.  Validates `desc` and fills `out`:
+ * which head goes to which segment slot, segment offsets and sizes, the
+ * effective bits per value (b + 32/G for quantised tensors, 16 otherwise)
+ * and the decode workspace size.  Returns KVQ_ERR_INVALID_ARG for a null
+ * pointer or an inconsistent description, KVQ_ERR_UNSUPPORTED for D != 128.
+ */
+kvq_status kvq_cache_layout(const kvq_layout_desc* desc, kvq_layout* out);
+
+/*
+ * kvq_quantize_append -- write positions [t0, t0 + n_tok) of every sequence
+ * into the cache ("VLM_KV_Quantization" section 1: historical visual K/V at
+ * INT8/INT4/INT2 with a group size; HeadGuard: protected heads stay bf16).
+ *   L        layout from kvq_cache_layout (host pointer, copied by value)
+ *   cache    device buffer of L->total_bytes, 256-byte aligned
+ *   k_bf16, v_bf16   device bf16 tensors [B][H_kv][n_tok][D]; element
+ *            (b, h, i, d) at index b*stride_b + h*stride_h + i*stride_t + d
+ *            (strides in elements; d contiguous; 8-byte aligned rows)
+ *   t0, n_tok  first position and count; n_tok == 0 is a no-op
+ * A position in [vis_start, vis_end) of an unprotected head is quantised
+ * (bits < 16) and packed; every other position is copied bf16 verbatim.
+ * Returns KVQ_ERR_CAPACITY if t0 + n_tok > T_cap.
+ */
+kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, const void* k_bf16,
+                               const void* v_bf16, int64_t stride_b, int64_t stride_h,
+                               int64_t stride_t, int32_t t0, int32_t n_tok, void* stream);
+
+/*
+ * kvq_decode_attention -- one decode query per sequence attends to positions
+ * [0, T) of the cache (split-KV flash decoding; dequantisation happens in
+ * registers and no dequantised K/V is ever written to device memory).
+ *   q_bf16    device bf16 [B][H_q][D], 16-byte aligned
+ *   T         attended positions, 1 <= T <= T_cap (all appended before)
+ *   softmax_scale  multiplies q.k (e.g. 1/sqrt(D))
+ *   out_bf16  device bf16 [B][H_q][D], 16-byte aligned
+ *   lse       device fp32 [B][H_q] (natural-log sum of exp of the scaled
+ *             scores) or NULL
+ *   workspace device scratch of at least L->workspace_bytes, 256-byte
+ *             aligned; contents on entry are ignored; overlapping calls
+ *             must not share one workspace
+ * out[b, hq, :] = sum_p softmax_p(scale * q[b,hq] . khat[b,h,p]) * vhat[b,h,p],
+ * h = hq / g, where khat/vhat are the dequantised (or bf16) cache rows.
+ * Returns KVQ_ERR_CAPACITY if ws_bytes < L->workspace_bytes.
+ */
+kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                int32_t T, float softmax_scale, void* out_bf16, float* lse,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_string(kvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

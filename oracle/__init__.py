@@ -66,6 +66,8 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.oracle_quantize_row.restype = i32
     lib.oracle_pack_row.argtypes = [P, i32, i32, P]
     lib.oracle_pack_row.restype = i32
+    lib.oracle_quantize_pack_rows.argtypes = [P, i64, i32, i32, i32, P, P, P]
+    lib.oracle_quantize_pack_rows.restype = i32
     lib.oracle_dequant_row.argtypes = [P, P, P, i32, i32, P]
     lib.oracle_dequant_row.restype = None
     lib.oracle_is_packed.argtypes = [i32, i32, i32, i32, i32]
@@ -118,6 +120,20 @@ def pack_row(codes: np.ndarray, bits: int, plant: int = 0) -> np.ndarray:
     if load(plant).oracle_pack_row(_ptr(c), c.shape[0], bits, _ptr(words)) != 0:
         raise ValueError("oracle_pack_row rejected its arguments")
     return words
+
+
+def quantize_pack_rows(x_bf16: np.ndarray, G: int, bits: int, plant: int = 0):
+    """x_bf16 uint16 [..., D] -> (words uint32 [n, D*bits/32], s uint16 [n, D/G], z uint16 [n, D/G])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    D = x.shape[-1]
+    n = x.size // D
+    words = np.zeros((n, D * bits // 32), np.uint32)
+    s = np.zeros((n, D // G), np.uint16)
+    z = np.zeros((n, D // G), np.uint16)
+    rc = load(plant).oracle_quantize_pack_rows(_ptr(x), n, D, G, bits, _ptr(words), _ptr(s), _ptr(z))
+    if rc != 0:
+        raise ValueError("oracle_quantize_pack_rows rejected its arguments")
+    return words, s, z
 
 
 def dequant_row(codes, s, z, G: int, plant: int = 0) -> np.ndarray:

@@ -210,6 +210,21 @@ int oracle_pack_row(const uint8_t* codes, int D, int bits, uint32_t* words) {
   return 0;
 }
 
+// Many rows at once: quantise + pack n_rows rows of D values.
+// words[n_rows][D*bits/32], s_bits/z_bits[n_rows][D/G].
+int oracle_quantize_pack_rows(const uint16_t* x, int64_t n_rows, int D, int G, int bits,
+                              uint32_t* words, uint16_t* s_bits, uint16_t* z_bits) {
+  std::vector<uint8_t> codes(D);
+  const int W = D * bits / 32;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    if (oracle_quantize_row(x + r * D, D, G, bits, codes.data(), s_bits + r * (D / G),
+                            z_bits + r * (D / G)) != 0)
+      return -1;
+    if (oracle_pack_row(codes.data(), D, bits, words + r * W) != 0) return -1;
+  }
+  return 0;
+}
+
 // Dequantise in fp64: x_hat = code * s + z.
 void oracle_dequant_row(const uint8_t* codes, const uint16_t* s_bits, const uint16_t* z_bits,
                         int D, int G, double* out) {

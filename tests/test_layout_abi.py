@@ -1,0 +1,178 @@
+"""Host-side tests of the C ABI: layout arithmetic, exported symbols and the
+argument checks that return before any launch (no GPU needed)."""
+import ctypes
+import re
+import subprocess
+
+import pytest
+
+import bit_mixed_precision_kvq_gb300 as kvq
+from bit_mixed_precision_kvq_gb300 import build_native
+
+HEADER = __import__("os").path.join(build_native.ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_native.build()
+    return kvq.load()
+
+
+def test_header_declares_what_library_exports(lib):
+    text = open(HEADER).read()
+    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*)\s+(kvq_\w+)\s*\(", text, re.M))
+    assert declared == set(kvq.EXPORTED_SYMBOLS)
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(kvq_\w+)$", out, re.M))
+    assert declared <= exported, declared - exported
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def _align(x, a):
+    return (x + a - 1) // a * a
+
+
+def _expected(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot):
+    """Independent restatement of the documented segment shapes."""
+    Tv = ve - vs
+    npr = len(prot)
+    npk = Hkv - npr
+    rb = [D * kb // 8, 4 * D // G if kb < 16 else 0, D * vb // 8, 4 * D // G if vb < 16 else 0,
+          2 * D, 2 * D, 2 * D, 2 * D]
+    rows = [B * npk * Tv] * 4 + [B * npr * Tv] * 2 + [B * Hkv * (Tcap - Tv)] * 2
+    off, offs = 0, []
+    for r, n in zip(rb, rows):
+        offs.append(off)
+        off = _align(off + r * n + 256, 256)
+    return rb, rows, offs, off
+
+
+CASES = [
+    (1, 4, 1, 128, 257, 14, 256, 4, 4, 32, []),
+    (1, 28, 4, 128, 6288, 14, 6287, 4, 2, 64, [0]),
+    (16, 32, 32, 128, 617, 40, 616, 8, 4, 32, [1, 5, 9, 30]),
+    (8, 32, 8, 128, 32769, 32, 32768, 2, 2, 32, [3]),
+    (32, 40, 40, 128, 2941, 60, 2940, 8, 8, 64, [0, 1, 2, 3, 39]),
+    (3, 12, 4, 128, 100, 0, 100, 16, 2, 128, [0, 1, 2, 3]),
+    (2, 2, 2, 128, 50, 10, 10, 4, 16, 32, []),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_layout_matches_formula(lib, case):
+    B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot = case
+    L = kvq.cache_layout(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot)
+    rb, rows, offs, total = _expected(*case)
+    assert list(L.row_bytes) == rb
+    assert list(L.bytes) == [r * n for r, n in zip(rb, rows)]
+    assert list(L.off) == offs and L.total_bytes == total
+    assert all(o % 256 == 0 for o in L.off)
+    assert L.g == Hq // Hkv and L.n_prot == len(prot) and L.n_packed == Hkv - len(prot)
+    assert L.Tv == ve - vs and L.T_text == Tcap - (ve - vs)
+    nhc = -(-(Hq // Hkv) // 8)
+    assert L.units == B * Hkv * nhc
+    # head -> slot -> head round trip
+    ps = pk = 0
+    for h in range(Hkv):
+        if h in prot:
+            assert L.slot[h] == ps and L.prot_head[ps] == h
+            ps += 1
+        else:
+            assert L.slot[h] == pk and L.packed_head[pk] == h
+            pk += 1
+    # "is INT2 really 2 bit/value": codes cost b bits, plus 32 bits of fp16
+    # scale and zero per group of G ("VLM_KV_Quantization", intro checklist)
+    assert L.eff_bits_k == (kb + 32.0 / G if kb < 16 else 16.0)
+    assert L.eff_bits_v == (vb + 32.0 / G if vb < 16 else 16.0)
+    if kb < 16:
+        assert L.row_bytes[kvq.SEG_K_CODES] * 8 == kb * D
+    slots = L.units + 1024 - 1
+    assert L.workspace_bytes == _align(slots * 8 * D * 4, 256) + _align(slots * 8 * 8, 256)
+
+
+BAD_DESCS = [
+    dict(B=0), dict(H_kv=0), dict(H_q=6), dict(H_kv=129, H_q=129), dict(D=100), dict(T_cap=0),
+    dict(vis_start=-1), dict(vis_end=300), dict(vis_start=20, vis_end=10), dict(k_bits=3),
+    dict(v_bits=1), dict(k_bits=32), dict(group_size=16), dict(group_size=48),
+]
+
+
+@pytest.mark.parametrize("bad", BAD_DESCS, ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_layout_rejects_bad_desc(lib, bad):
+    args = dict(B=1, H_q=8, H_kv=4, D=128, T_cap=256, vis_start=10, vis_end=200, k_bits=4,
+                v_bits=4, group_size=32)
+    args.update(bad)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.cache_layout(protected=[], **args)
+    assert e.value.status == 1
+
+
+def test_layout_unsupported_head_dim(lib):
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.cache_layout(1, 8, 4, 64, 256, 10, 200, 4, 4, 32, [])
+    assert e.value.status == 2
+
+
+def test_layout_rejects_mask_beyond_heads(lib):
+    with pytest.raises(kvq.KvqError):
+        kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [5])
+
+
+# Fake, never-dereferenced device addresses: every case below must be rejected
+# on the host before any CUDA call.
+FAKE = 1 << 40
+
+
+def test_append_argument_checks(lib):
+    L = kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ok = dict(cache=FAKE, k=FAKE, v=FAKE, t0=0, n_tok=4, strides=(4 * 256 * 128, 256 * 128, 128))
+    for bad, code in ((dict(cache=0), 1), (dict(k=0), 1), (dict(cache=FAKE + 16), 1),
+                      (dict(k=FAKE + 2), 1), (dict(strides=(1, 128, 128)), 1),
+                      (dict(t0=-1), 1), (dict(n_tok=-2), 1), (dict(t0=250, n_tok=7), 3)):
+        a = dict(ok)
+        a.update(bad)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.quantize_append(L, a["cache"], a["k"], a["v"], a["t0"], a["n_tok"], a["strides"],
+                                stream=0)
+        assert e.value.status == code, bad
+    # n_tok == 0 is a no-op and touches nothing
+    kvq.quantize_append(L, FAKE, FAKE, FAKE, 256, 0, ok["strides"], stream=0)
+
+
+def test_decode_argument_checks(lib):
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ws = L.workspace_bytes
+    ok = dict(cache=FAKE, q=FAKE, T=100, out=FAKE, lse=0, ws=FAKE, ws_bytes=ws)
+    for bad, code in ((dict(cache=0), 1), (dict(q=0), 1), (dict(out=0), 1), (dict(ws=0), 1),
+                      (dict(T=0), 1), (dict(T=257), 1), (dict(q=FAKE + 8), 1),
+                      (dict(ws=FAKE + 64), 1), (dict(lse=FAKE + 2), 1),
+                      (dict(ws_bytes=ws - 1), 3)):
+        a = dict(ok)
+        a.update(bad)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_attention(L, a["cache"], a["q"], a["T"], a["out"], 0.1, a["lse"], a["ws"],
+                                 a["ws_bytes"], stream=0)
+        assert e.value.status == code, bad
+    with pytest.raises(kvq.KvqError):
+        kvq.decode_attention(L, FAKE, FAKE, 10, FAKE, float("nan"), 0, FAKE, ws, stream=0)
+
+
+def test_corrupted_layout_rejected(lib):
+    L = kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    for field, val in (("total_bytes", 1), ("n_prot", 2), ("Tv", 5)):
+        bad = kvq.Layout.from_buffer_copy(L)
+        setattr(bad, field, val)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_attention(bad, FAKE, FAKE, 10, FAKE, 0.1, 0, FAKE, 1 << 40, stream=0)
+        assert e.value.status == 1
+    bad = kvq.Layout.from_buffer_copy(L)
+    bad.off[3] += 256
+    with pytest.raises(kvq.KvqError):
+        kvq.quantize_append(bad, FAKE, FAKE, FAKE, 0, 1, (128, 128, 128), stream=0)
+
+
+def test_status_strings(lib):
+    for code, name in kvq.STATUS.items():
+        assert lib.kvq_status_string(code).decode() == name
