@@ -53,7 +53,8 @@ class LayoutDesc(ctypes.Structure):
 
 class Layout(ctypes.Structure):
     _fields_ = [("d", LayoutDesc), ("g", ctypes.c_int32), ("n_prot", ctypes.c_int32),
-                ("n_packed", ctypes.c_int32), ("Tv", ctypes.c_int32), ("T_text", ctypes.c_int32),
+                ("n_packed", ctypes.c_int32), ("Tv", ctypes.c_int32), ("Tv_pad", ctypes.c_int32),
+                ("T_text", ctypes.c_int32),
                 ("units", ctypes.c_int32),
                 ("slot", ctypes.c_int32 * KVQ_MAX_HEADS),
                 ("prot_head", ctypes.c_uint8 * KVQ_MAX_HEADS),

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) append_kernel(Params p, const uint16_t* _
       dst = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_PROT_V : KVQ_SEG_PROT_K]) + row * (2 * kD);
     } else {
       const int bits = which ? p.vb : p.kb;
-      const int64_t row = (static_cast<int64_t>(b) * p.n_packed + p.slot[h]) * p.Tv + (t - p.vs);
+      const int64_t row = (static_cast<int64_t>(b) * p.n_packed + p.slot[h]) * p.Tv_pad + (t - p.vs);
       uint8_t* codes = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_V_CODES : KVQ_SEG_K_CODES]) +
                        row * (which ? p.vrow : p.krow);
       if (bits < 16) {

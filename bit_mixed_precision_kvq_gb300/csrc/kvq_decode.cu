@@ -1,5 +1,5 @@
-// kvq_decode.cu -- kvq_decode_attention: split-KV flash decoding over the
-// mixed-precision cache, plus the cross-split log-sum-exp combine.
+// kvq_decode.cu -- kvq_decode_attention: host launcher for the split-KV
+// partial kernel (kvq_split.cuh) and the cross-split log-sum-exp combine.
 //
 // Method sources: WSVD summary (gist.science 2604.02570), section 2.라 --
 // K/V are rebuilt on chip inside a flash-decoding pipeline and used at once
@@ -7,22 +7,40 @@
 // device memory; "VLM_KV_Quantization", section 2 -- GQA cache
 // [B, H_kv, T, D] read by H_q / H_kv query heads per KV head.
 //
-// Softmax runs in base 2: q is pre-multiplied by softmax_scale * log2(e), so
-// a partial holds m = max score (log2 units), l = sum 2^(s - m) and
+// Softmax runs in base 2: scores are scaled by softmax_scale * log2(e), so a
+// partial holds m = max score (log2 units), l = sum 2^(s - m) and
 // o = sum 2^(s - m) v.  The combine merges partials with the usual rescaling
 // and reports lse = ln(2) * (M + log2 L).
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "kvq_device.cuh"
+#include "kvq_ptx.cuh"
+#include "kvq_split.cuh"
 
 namespace kvq {
 
+const void* split_kernel_k2(int vb);
+const void* split_kernel_k4(int vb);
+const void* split_kernel_k8(int vb);
+const void* split_kernel_k16(int vb);
+
+constexpr int kCombineWarps = 8;
+
 // ---------------------------------------------------------------------------
-// Combine: one CTA per (b, hq), one thread per d.
+// Combine: one CTA per (b, hq).  Warp w folds slots w, w + 8, ... with an
+// online rescaling; the 8 warp states are merged in shared memory.  Lane l
+// owns d = 4l .. 4l+3.  A NaN partial max (a failed wait in the split kernel)
+// turns the output into NaN.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) combine_kernel(Params p) {
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ Params p) {
+  __shared__ float sm_ml[kCombineWarps][2];
+  __shared__ float4 sm_o[kCombineWarps][32];
+  __shared__ int sm_bad;
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bq = blockIdx.x;
   const int b = bq / p.Hq;
   const int hq = bq - b * p.Hq;
@@ -33,145 +51,109 @@ __global__ void __launch_bounds__(128) combine_kernel(Params p) {
   const int u = unit_of(p, b, h, hc);
   int cf, cl;
   plan_unit_chunks(p.plan, u, &cf, &cl);
-  const int d = threadIdx.x;
-  float M = -INFINITY;
-  for (int c = cf; c <= cl; ++c) M = fmaxf(M, p.ws_ml[(static_cast<int64_t>(u + c) * kNH + j) * 2]);
-  float L = 0.0f, O = 0.0f;
-  for (int c = cf; c <= cl; ++c) {
+  if (threadIdx.x == 0) sm_bad = 0;
+  __syncthreads();
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool bad = false;
+  for (int c = cf + warp; c <= cl; c += kCombineWarps) {
     const int64_t s = static_cast<int64_t>(u + c) * kNH + j;
     const float m = p.ws_ml[s * 2];
-    if (m == -INFINITY) continue;
-    const float w = exp2f(m - M);
-    L = fmaf(w, p.ws_ml[s * 2 + 1], L);
-    O = fmaf(w, p.ws_o[s * kD + d], O);
+    const float l = p.ws_ml[s * 2 + 1];
+    const float4 o = reinterpret_cast<const float4*>(p.ws_o + s * kD)[lane];
+    if (m != m) bad = true;
+    if (m == -INFINITY || m != m) continue;
+    const float Mn = fmaxf(M, m);
+    const float a = exp2f(M - Mn), w = exp2f(m - Mn);
+    L = L * a + l * w;
+    O.x = O.x * a + o.x * w;
+    O.y = O.y * a + o.y * w;
+    O.z = O.z * a + o.z * w;
+    O.w = O.w * a + o.w * w;
+    M = Mn;
   }
-  p.out[static_cast<int64_t>(bq) * kD + d] = f32_to_bf16_bits(O / L);
-  if (d == 0 && p.lse) p.lse[bq] = 0.69314718055994531f * (M + log2f(L));
+  if (bad) sm_bad = 1;
+  if (lane == 0) {
+    sm_ml[warp][0] = M;
+    sm_ml[warp][1] = L;
+  }
+  sm_o[warp][lane] = O;
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, sm_ml[w][0]);
+  float Lt = 0.f;
+  float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    if (sm_ml[w][0] == -INFINITY) continue;
+    const float sc = exp2f(sm_ml[w][0] - Mt);
+    Lt = fmaf(sm_ml[w][1], sc, Lt);
+    const float4 o = sm_o[w][lane];
+    Ot.x = fmaf(o.x, sc, Ot.x);
+    Ot.y = fmaf(o.y, sc, Ot.y);
+    Ot.z = fmaf(o.z, sc, Ot.z);
+    Ot.w = fmaf(o.w, sc, Ot.w);
+  }
+  float inv = 1.0f / Lt;
+  if (sm_bad) inv = __int_as_float(0x7fffffff);
+  uint2 packed;
+  packed.x = static_cast<uint32_t>(f32_to_bf16_bits(Ot.x * inv)) |
+             (static_cast<uint32_t>(f32_to_bf16_bits(Ot.y * inv)) << 16);
+  packed.y = static_cast<uint32_t>(f32_to_bf16_bits(Ot.z * inv)) |
+             (static_cast<uint32_t>(f32_to_bf16_bits(Ot.w * inv)) << 16);
+  reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(bq) * kD)[lane] = packed;
+  if (lane == 0 && p.lse) p.lse[bq] = sm_bad ? inv : 0.69314718055994531f * (Mt + log2f(Lt));
 }
+
+}  // namespace kvq
 
 namespace {
 
-// ---------------------------------------------------------------------------
-// Simple split kernel: 8 warps, one position per warp per step, lanes over D.
-// ---------------------------------------------------------------------------
-
-// Lane's 4 elements (d = 4*lane .. 4*lane+3) of one K or V row, as fp32.
-__device__ __forceinline__ void load4(const uint8_t* row, const uint8_t* sz, int bits, int G, int lane,
-                                      float out[4]) {
-  if (bits == 16) {
-    const uint2 w = *reinterpret_cast<const uint2*>(row + 8 * lane);
-    out[0] = bf16_lo(w.x);
-    out[1] = bf16_hi(w.x);
-    out[2] = bf16_lo(w.y);
-    out[3] = bf16_hi(w.y);
-    return;
-  }
-  const int d0 = 4 * lane;
-  const uint32_t word = reinterpret_cast<const uint32_t*>(row)[(d0 * bits) >> 5];
-  const int shift = (d0 * bits) & 31;
-  const __half2 szv = reinterpret_cast<const __half2*>(sz)[d0 / G];
-  const float s = __low2float(szv), z = __high2float(szv);
-  const uint32_t mask = (1u << bits) - 1u;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t c = (word >> (shift + i * bits)) & mask;
-    out[i] = fmaf(static_cast<float>(c), s, z);
-  }
+// Positions per packed tile and its sub-buffer offsets inside one stage.
+void packed_tile_geometry(kvq::Params* p) {
+  const int w = p->krow + p->kszrow + p->vrow + p->vszrow;
+  int tt = ((kvq::kStageBytes - 4 * 128) / w) / 16 * 16;
+  if (tt > 512) tt = 512;
+  auto r128 = [](int x) { return (x + 127) / 128 * 128; };
+  p->tt_pk = tt;
+  p->pk_off_vc = r128(tt * p->krow);
+  p->pk_off_ksz = p->pk_off_vc + r128(tt * p->vrow);
+  p->pk_off_vsz = p->pk_off_ksz + r128(tt * p->kszrow);
 }
 
-constexpr int kWarpsSimple = 8;
-
-__global__ void __launch_bounds__(256) split_simple_kernel(Params p) {
-  __shared__ float sm_ml[kWarpsSimple][kNH][2];
-  __shared__ float sm_o[kWarpsSimple][kNH][kD];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int c = blockIdx.x;
-  const Cut a = plan_cut(p.plan, c);
-  const Cut e = plan_cut(p.plan, c + 1);
-  const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
-  for (int u = a.u; u <= u_last; ++u) {
-    const int ps = (u == a.u) ? a.p : 0;
-    const int pe = (u == e.u) ? e.p : p.plan.T;
-    const UnitInfo ui = unit_info(p, u);
-    const int hq0 = ui.h * p.g + ui.hc * kNH;
-    const int nh = min(kNH, p.g - ui.hc * kNH);
-    float q[kNH][4];
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-      if (j < nh) {
-        const uint2 w = *reinterpret_cast<const uint2*>(
-            p.q + (static_cast<int64_t>(ui.b) * p.Hq + hq0 + j) * kD + 4 * lane);
-        q[j][0] = bf16_lo(w.x) * p.scale_log2;
-        q[j][1] = bf16_hi(w.x) * p.scale_log2;
-        q[j][2] = bf16_lo(w.y) * p.scale_log2;
-        q[j][3] = bf16_hi(w.y) * p.scale_log2;
-      } else {
-        q[j][0] = q[j][1] = q[j][2] = q[j][3] = 0.0f;
-      }
-    }
-    float m[kNH], l[kNH], o[kNH][4];
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-      m[j] = -INFINITY;
-      l[j] = 0.0f;
-      o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-    }
-    for (int pos = ps + warp; pos < pe; pos += kWarpsSimple) {
-      const RowRef rr = row_ref(p, ui, pos);
-      float k[4], v[4];
-      load4(rr.k, rr.ksz, rr.kbits, p.G, lane, k);
-      load4(rr.v, rr.vsz, rr.vbits, p.G, lane, v);
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        if (j >= nh) break;
-        float s = q[j][0] * k[0] + q[j][1] * k[1] + q[j][2] * k[2] + q[j][3] * k[3];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        const float mn = fmaxf(m[j], s);
-        const float corr = exp2f(m[j] - mn);
-        const float pj = exp2f(s - mn);
-        l[j] = fmaf(l[j], corr, pj);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[j][i] = fmaf(o[j][i], corr, pj * v[i]);
-        m[j] = mn;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-      if (lane == 0) {
-        sm_ml[warp][j][0] = m[j];
-        sm_ml[warp][j][1] = l[j];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sm_o[warp][j][4 * lane + i] = o[j][i];
-    }
-    __syncthreads();
-    const int64_t slot = static_cast<int64_t>(u) + c;
-    for (int idx = threadIdx.x; idx < nh * kD; idx += blockDim.x) {
-      const int j = idx / kD, d = idx - j * kD;
-      float M = -INFINITY;
-      for (int w = 0; w < kWarpsSimple; ++w) M = fmaxf(M, sm_ml[w][j][0]);
-      float L = 0.0f, O = 0.0f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < kWarpsSimple; ++w) {
-          const float sc = exp2f(sm_ml[w][j][0] - M);
-          L = fmaf(sm_ml[w][j][1], sc, L);
-          O = fmaf(sm_o[w][j][d], sc, O);
-        }
-      }
-      p.ws_o[(slot * kNH + j) * kD + d] = O;
-      if (d == 0) {
-        p.ws_ml[(slot * kNH + j) * 2] = M;
-        p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
-      }
-    }
-    __syncthreads();
+const void* split_kernel_for(int kb, int vb) {
+  switch (kb) {
+    case 2: return kvq::split_kernel_k2(vb);
+    case 4: return kvq::split_kernel_k4(vb);
+    case 8: return kvq::split_kernel_k8(vb);
+    case 16: return kvq::split_kernel_k16(vb);
   }
+  return nullptr;
+}
+
+// Two CTAs per SM: 2 x (115,584 + 1,024 reserved) bytes fit the SM's 228 KiB.
+constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
+static_assert(kSplitSmemBytes <= (233472 - 2 * 1024) / 2, "split kernel must fit twice per SM");
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       kvq::Params* p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[1] = {p};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace
-}  // namespace kvq
 
 extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
                                            int32_t T, float softmax_scale, void* out_bf16, float* lse,
@@ -186,6 +168,8 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   if (T < 1 || T > L->d.T_cap) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (ws_bytes < static_cast<size_t>(L->workspace_bytes)) return KVQ_ERR_CAPACITY;
+  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits);
+  if (!split) return KVQ_ERR_UNSUPPORTED;
   int n_sm = 0;
   if (kvq_device_sm_count(&n_sm) != 0) return KVQ_ERR_CUDA;
 
@@ -202,12 +186,27 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   const int64_t o_bytes = (slots * kvq::kNH * kvq::kD * 4 + 255) / 256 * 256;
   p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  packed_tile_geometry(&p);
   p.plan = kvq_make_plan(L, T, 2 * n_sm);
 
+  // Opt each split kernel into >48 KB of dynamic shared memory, once.
+  static std::mutex mu;
+  static bool smem_set[17][17] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    bool& done = smem_set[L->d.k_bits][L->d.v_bits];
+    if (!done) {
+      if (cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSplitSmemBytes)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+      done = true;
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kvq::split_simple_kernel<<<p.plan.C, 256, 0, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  kvq::combine_kernel<<<L->d.B * L->d.H_q, kvq::kD, 0, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_pdl(split, dim3(p.plan.C), dim3(kvq::kSplitThreads), kSplitSmemBytes, s, &p) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), dim3(L->d.B * L->d.H_q),
+                 dim3(kvq::kCombineWarps * 32), 0, s, &p) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

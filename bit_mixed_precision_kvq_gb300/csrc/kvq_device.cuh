@@ -42,7 +42,7 @@ __device__ __forceinline__ RowRef row_ref(const Params& p, const UnitInfo& ui, i
     r.ksz = r.vsz = nullptr;
     r.kbits = r.vbits = 16;
   } else {
-    const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv + (pos - p.vs);
+    const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (pos - p.vs);
     r.k = p.seg[KVQ_SEG_K_CODES] + row * p.krow;
     r.v = p.seg[KVQ_SEG_V_CODES] + row * p.vrow;
     r.ksz = p.kb < 16 ? p.seg[KVQ_SEG_K_SZ] + row * p.kszrow : nullptr;

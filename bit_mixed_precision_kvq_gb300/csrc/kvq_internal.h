@@ -115,10 +115,12 @@ struct Params {
   int32_t B, Hq, Hkv, g, NHC;
   int32_t T;           // attended positions (decode) / T_cap (append)
   int32_t vs, ve;      // visual range of the layout
-  int32_t Tv, T_text;
+  int32_t Tv, Tv_pad, T_text;
   int32_t kb, vb, G;
   int32_t n_prot, n_packed;
   int32_t krow, kszrow, vrow, vszrow;  // bytes per row of the packed segments
+  int32_t tt_pk;                       // positions per packed tile (multiple of 16)
+  int32_t pk_off_vc, pk_off_ksz, pk_off_vsz;  // packed-tile offsets in a stage
   // cache segments
   const uint8_t* seg[KVQ_NSEG];
   // decode call

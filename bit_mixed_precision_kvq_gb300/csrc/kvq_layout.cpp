@@ -44,6 +44,10 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   L.d = d;
   L.g = d.H_q / d.H_kv;
   L.Tv = d.vis_end - d.vis_start;
+  // Packed segments keep every (b, head) block of visual rows on a 16-row
+  // boundary so that a tile of scale/zero rows (4-16 bytes each) starting at
+  // a 16-aligned visual row is 16-byte aligned for bulk copies.
+  L.Tv_pad = (L.Tv + 15) / 16 * 16;
   L.T_text = d.T_cap - L.Tv;
   for (int h = 0; h < d.H_kv; ++h) {
     if (d.protected_heads[h]) {
@@ -66,7 +70,7 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   L.row_bytes[KVQ_SEG_PROT_V] = 2 * D;
   L.row_bytes[KVQ_SEG_TEXT_K] = 2 * D;
   L.row_bytes[KVQ_SEG_TEXT_V] = 2 * D;
-  const int64_t packed_rows = static_cast<int64_t>(d.B) * L.n_packed * L.Tv;
+  const int64_t packed_rows = static_cast<int64_t>(d.B) * L.n_packed * L.Tv_pad;
   const int64_t prot_rows = static_cast<int64_t>(d.B) * L.n_prot * L.Tv;
   const int64_t text_rows = static_cast<int64_t>(d.B) * d.H_kv * L.T_text;
   const int64_t rows[KVQ_NSEG] = {packed_rows, packed_rows, packed_rows, packed_rows,
@@ -127,6 +131,7 @@ void kvq_fill_params(const kvq_layout* L, kvq::Params* p) {
   p->vs = d.vis_start;
   p->ve = d.vis_end;
   p->Tv = L->Tv;
+  p->Tv_pad = L->Tv_pad;
   p->T_text = L->T_text;
   p->kb = d.k_bits;
   p->vb = d.v_bits;

@@ -1,0 +1,514 @@
+// kvq_split.cuh -- split-KV partial attention over the mixed-precision cache.
+//
+// Flash-decoding with on-chip reconstruction (WSVD summary, section 2.라):
+// cache tiles are streamed into shared memory, unpacked and dequantised in
+// registers, and consumed at once by QK, an online softmax and PV; nothing
+// dequantised is ever written to device memory.
+//
+// CTA = 1 producer warp + 4 consumer warps.
+//   producer : one lane walks the CTA's tiles and issues 1-D bulk async
+//              copies (TMA) of the tile's K/V rows (+ scale/zero rows) into a
+//              3-stage ring of 32 KB stages, signalled by mbarriers.
+//   consumers: each 16-position block of a tile goes to one warp.  QK and PV
+//              run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
+//              accumulate) with the unit's <= 8 query heads as N = 8:
+//                QK: S^T[t][j] = K[t][:] . q[j][:]    (M = 16 positions)
+//                PV: O^T[d][j] += V^T[d][t] P^T[t][j] (M = 16 of the D rows)
+//              Codes become fp16 with the 0x6400 exponent trick
+//              (1024 + c, then subtract 1024: exact), so QK accumulates
+//              sum_d c*q exactly per quantisation group and applies the
+//              group's scale and zero afterwards:
+//                q.k_hat = sum_g ( s_g * sum_{d in g} q_d c_d + z_g * sum_{d in g} q_d ).
+//              V is dequantised per element in f16x2 (c*s + z, one rounding)
+//              because the reduction runs over positions.
+// Per unit piece the 4 warps' (m, l, o) are merged in shared memory and
+// written to the workspace slot (unit + chunk).
+#pragma once
+
+#include "kvq_device.cuh"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 32 * 1024;
+constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
+constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
+constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
+constexpr uint32_t kF16Magic = 0x64006400u;    // two fp16 1024.0
+
+struct SplitSmem {
+  alignas(128) uint8_t stage[kStages][kStageBytes];
+  float merge_o[kConsumerWarps][kNH][kD];
+  float merge_ml[kConsumerWarps][kNH][2];
+  float qsum[kConsumerWarps][kNH][4];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort;
+};
+
+enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2 };
+
+// Walk the tiles of one piece [ps, pe) of a unit: text prefix, visual block,
+// text suffix, each cut into tiles.  f(kind, t0, n).
+template <typename F>
+__device__ __forceinline__ void walk_piece(const Params& p, bool prot, int ps, int pe, F&& f) {
+  const int bounds[4] = {ps, max(ps, min(pe, p.vs)), max(ps, min(pe, p.ve)), pe};
+  for (int s = 0; s < 3; ++s) {
+    const int s0 = bounds[s], s1 = bounds[s + 1];
+    if (s0 >= s1) continue;
+    const int kind = s == 1 ? (prot ? kTileProt : kTilePacked) : kTileText;
+    const int tt = kind == kTilePacked ? p.tt_pk : kTileBf16;
+    for (int t0 = s0; t0 < s1; t0 += tt) f(kind, t0, min(tt, s1 - t0));
+  }
+}
+
+__device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// ---------------------------------------------------------------------------
+// Producer
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
+  const Cut a = plan_cut(p.plan, c);
+  const Cut e = plan_cut(p.plan, c + 1);
+  const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
+  uint32_t it = 0;
+  for (int u = a.u; u <= u_last; ++u) {
+    const int ps = (u == a.u) ? a.p : 0;
+    const int pe = (u == e.u) ? e.p : p.plan.T;
+    const UnitInfo ui = unit_info(p, u);
+    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) {
+      const int st = it % kStages;
+      const uint32_t round = it / kStages;
+      if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
+      uint8_t* dst = sm.stage[st];
+      if (kind != kTilePacked) {
+        int64_t row;
+        const uint8_t *ks, *vs;
+        if (kind == kTileText) {
+          const int tr = t0 < p.vs ? t0 : t0 - p.Tv;
+          row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
+          ks = p.seg[KVQ_SEG_TEXT_K];
+          vs = p.seg[KVQ_SEG_TEXT_V];
+        } else {
+          row = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
+          ks = p.seg[KVQ_SEG_PROT_K];
+          vs = p.seg[KVQ_SEG_PROT_V];
+        }
+        const uint32_t bytes = static_cast<uint32_t>(n) * (2 * kD);
+        mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
+        bulk_g2s(dst, ks + row * (2 * kD), bytes, &sm.full[st]);
+        bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), bytes, &sm.full[st]);
+      } else {
+        const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
+        const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
+        const uint32_t bks = round16(n * p.kszrow), bvs = round16(n * p.vszrow);
+        mbar_arrive_expect_tx(&sm.full[st], bk + bv + bks + bvs);
+        bulk_g2s(dst, p.seg[KVQ_SEG_K_CODES] + row * p.krow, bk, &sm.full[st]);
+        bulk_g2s(dst + p.pk_off_vc, p.seg[KVQ_SEG_V_CODES] + row * p.vrow, bv, &sm.full[st]);
+        if (bks) bulk_g2s(dst + p.pk_off_ksz, p.seg[KVQ_SEG_K_SZ] + row * p.kszrow, bks, &sm.full[st]);
+        if (bvs) bulk_g2s(dst + p.pk_off_vsz, p.seg[KVQ_SEG_V_SZ] + row * p.vszrow, bvs, &sm.full[st]);
+      }
+      ++it;
+    });
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fragment builders.  Lane = 4*gid + tig.
+//
+// QK A operand (rows = positions gid and gid+8 of a 16-position block,
+// K index = d).  The K index is permuted so that each lane reads 8
+// consecutive d of a row: k-step pair P (k-steps 2P, 2P+1) covers
+// d in [32P, 32P+32), lane tig owns d0 = 32P + 8*tig .. d0+7 and places
+//   k-step 2P  : slots (2tig, 2tig+1) <- (d0, d0+4), slots (2tig+8, 2tig+9) <- (d0+1, d0+5)
+//   k-step 2P+1: slots (2tig, 2tig+1) <- (d0+2, d0+6), slots (2tig+8, 2tig+9) <- (d0+3, d0+7)
+// The q operand (B) is loaded with the same permutation.  Each k-step pair
+// stays inside one quantisation group (G >= 32).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// Masked code-field pair -> exact fp16 codes (c_lo, c_hi).
+__device__ __forceinline__ uint32_t codes_f16(uint32_t x, uint32_t mask) {
+  return hsub2_u(and_or(x, mask, kF16Magic), kF16Magic);
+}
+
+// bf16 elements -> fp16 pair.
+__device__ __forceinline__ uint32_t bf16pair_f16(uint32_t lo_word, bool lo_hi, uint32_t hi_word, bool hi_hi) {
+  const float a = lo_hi ? bf16_hi(lo_word) : bf16_lo(lo_word);
+  const float b = hi_hi ? bf16_hi(hi_word) : bf16_lo(hi_word);
+  return pack_f16x2(a, b);
+}
+
+// Four fp16 pairs (d0,d0+4), (d0+1,d0+5), (d0+2,d0+6), (d0+3,d0+7) of one
+// row's 8 elements starting at d0.  KB = bits (16 = bf16 row).
+template <int KB>
+__device__ __forceinline__ void k_row_pairs(const uint8_t* row, int P, int tig, uint32_t (&f)[4]) {
+  if constexpr (KB == 4) {
+    const uint32_t w = lds32(row + 4 * (4 * P + tig));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f[k] = codes_f16(w >> (4 * k), 0x000F000Fu);
+  } else if constexpr (KB == 2) {
+    const uint32_t w = lds32(row + 4 * (2 * P + (tig >> 1)));
+    const uint32_t h = tig & 1;
+    const uint32_t r = prmt(w, 0u, (2 * h) | (4u << 4) | ((2 * h + 1) << 8) | (4u << 12));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f[k] = codes_f16(r >> (2 * k), 0x00030003u);
+  } else if constexpr (KB == 8) {
+    const uint2 w = lds64(row + 4 * (8 * P + 2 * tig));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t x = prmt(w.x, w.y, k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+      f[k] = codes_f16(x, 0x00FF00FFu);
+    }
+  } else {  // bf16 row
+    const uint4 r = lds128(row + 2 * (32 * P + 8 * tig));
+    f[0] = bf16pair_f16(r.x, false, r.z, false);
+    f[1] = bf16pair_f16(r.x, true, r.z, true);
+    f[2] = bf16pair_f16(r.y, false, r.w, false);
+    f[3] = bf16pair_f16(r.y, true, r.w, true);
+  }
+}
+
+// PV A operand (rows = d, K index = positions).  Lane gid owns
+// d in [16 gid, 16 gid + 16): m-tile mt row gid <-> d = 16 gid + mt,
+// row gid+8 <-> d = 16 gid + 8 + mt.  Positions: a0/a1 use (2tig, 2tig+1),
+// a2/a3 use (2tig+8, 2tig+9).
+//
+// VData holds one lane's 16 d of 4 positions in the storage format.
+template <int VB>
+struct VData {
+  static constexpr int kWords = VB == 16 ? 8 : VB / 2;  // 32-bit words per position
+  uint32_t w[4][kWords];
+};
+
+template <int VB>
+__device__ __forceinline__ void v_load(const uint8_t* vrows, int row_bytes, int gid, const int (&t)[4],
+                                       VData<VB>& v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t* r = vrows + t[i] * row_bytes;
+    if constexpr (VB == 2) {
+      v.w[i][0] = lds32(r + 4 * gid);
+    } else if constexpr (VB == 4) {
+      const uint2 x = lds64(r + 8 * gid);
+      v.w[i][0] = x.x;
+      v.w[i][1] = x.y;
+    } else if constexpr (VB == 8) {
+      const uint4 x = lds128(r + 16 * gid);
+      v.w[i][0] = x.x; v.w[i][1] = x.y; v.w[i][2] = x.z; v.w[i][3] = x.w;
+    } else {
+      const uint4 x = lds128(r + 32 * gid);
+      const uint4 y = lds128(r + 32 * gid + 16);
+      v.w[i][0] = x.x; v.w[i][1] = x.y; v.w[i][2] = x.z; v.w[i][3] = x.w;
+      v.w[i][4] = y.x; v.w[i][5] = y.y; v.w[i][6] = y.z; v.w[i][7] = y.w;
+    }
+  }
+}
+
+// Code pair (position i0, position i1) for local element e in [0, 16) of the
+// lane's d range, as exact fp16 (bf16 rows: the value itself).
+template <int VB>
+__device__ __forceinline__ uint32_t v_pair(const VData<VB>& v, int i0, int i1, int e) {
+  if constexpr (VB == 2) {
+    const uint32_t x = prmt(v.w[i0][0], v.w[i1][0], e < 8 ? 0x5410u : 0x7632u);
+    return codes_f16(x >> (2 * (e & 7)), 0x00030003u);
+  } else if constexpr (VB == 4) {
+    const int wi = e >> 3, ee = e & 7;
+    const uint32_t x = prmt(v.w[i0][wi], v.w[i1][wi], ee < 4 ? 0x5410u : 0x7632u);
+    return codes_f16(x >> (4 * (ee & 3)), 0x000F000Fu);
+  } else if constexpr (VB == 8) {
+    const int wi = e >> 2, b = e & 3;
+    const uint32_t x = prmt(v.w[i0][wi], v.w[i1][wi], b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12));
+    return codes_f16(x, 0x00FF00FFu);
+  } else {
+    const int wi = e >> 1;
+    const bool hi = e & 1;
+    return bf16pair_f16(v.w[i0][wi], hi, v.w[i1][wi], hi);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Consumers
+// ---------------------------------------------------------------------------
+
+// Online-softmax state of one warp for its unit: m, l for the lane's two
+// query-head columns (2tig, 2tig+1); o^T fragments for 8 m-tiles of d.
+struct Acc {
+  float m[2], l[2];
+  float o[8][4];
+};
+
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// One 16-position block [r0, r0 + 16) of a staged tile (n valid positions).
+// KB/VB: bit-widths of the K and V rows (16 = bf16 rows).
+template <int KB, int VB>
+__device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
+                                       const uint8_t* vsz, int r0, int n, int G, float sl2,
+                                       const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
+                                       int tig, Acc& acc) {
+  constexpr int KROW = KB * kD / 8;
+  constexpr int VROW = VB * kD / 8;
+  const int szrow = 4 * (kD / G);
+  const uint8_t* krow0 = kc + (r0 + gid) * KROW;
+  const uint8_t* krow1 = kc + (r0 + gid + 8) * KROW;
+
+  // ---- S^T = K q^T (scaled to log2 units) ----
+  float S[4] = {0.f, 0.f, 0.f, 0.f};
+  float C[4] = {0.f, 0.f, 0.f, 0.f};
+  const int ppg = G >> 5;  // k-step pairs per quantisation group: 1, 2 or 4
+#pragma unroll
+  for (int P = 0; P < 4; ++P) {
+    uint32_t f0[4], f1[4];
+    k_row_pairs<KB>(krow0, P, tig, f0);
+    k_row_pairs<KB>(krow1, P, tig, f1);
+    const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
+    const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
+    mma_f16(C, A0, qb[2 * P][0], qb[2 * P][1]);
+    mma_f16(C, A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
+    if constexpr (KB < 16) {
+      if (((P + 1) & (ppg - 1)) == 0) {  // end of a quantisation group
+        const int g = P / ppg;
+        const uint32_t sz0 = lds32(ksz + (r0 + gid) * szrow + 4 * g);
+        const uint32_t sz1 = lds32(ksz + (r0 + gid + 8) * szrow + 4 * g);
+        const float s0 = f16lo(sz0) * sl2, z0 = f16hi(sz0) * sl2;
+        const float s1 = f16lo(sz1) * sl2, z1 = f16hi(sz1) * sl2;
+        S[0] = fmaf(s0, C[0], fmaf(z0, qsP[P][0], S[0]));
+        S[1] = fmaf(s0, C[1], fmaf(z0, qsP[P][1], S[1]));
+        S[2] = fmaf(s1, C[2], fmaf(z1, qsP[P][0], S[2]));
+        S[3] = fmaf(s1, C[3], fmaf(z1, qsP[P][1], S[3]));
+        C[0] = C[1] = C[2] = C[3] = 0.f;
+      }
+    }
+  }
+  if constexpr (KB == 16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S[i] = C[i] * sl2;
+  }
+  const bool ok0 = r0 + gid < n, ok1 = r0 + gid + 8 < n;
+  if (!ok0) S[0] = S[1] = -INFINITY;
+  if (!ok1) S[2] = S[3] = -INFINITY;
+
+  // ---- online softmax (columns = query heads 2tig, 2tig+1) ----
+  float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
+  const float b0s = mn0 == -INFINITY ? 0.f : mn0, b1s = mn1 == -INFINITY ? 0.f : mn1;
+  const float c0 = exp2f(acc.m[0] - b0s), c1 = exp2f(acc.m[1] - b1s);
+  const float P0 = exp2f(S[0] - b0s), P1 = exp2f(S[1] - b1s);
+  const float P2 = exp2f(S[2] - b0s), P3 = exp2f(S[3] - b1s);
+  acc.m[0] = mn0;
+  acc.m[1] = mn1;
+  acc.l[0] = fmaf(acc.l[0], c0, P0 + P2);
+  acc.l[1] = fmaf(acc.l[1], c1, P1 + P3);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    acc.o[mt][0] *= c0;
+    acc.o[mt][1] *= c1;
+    acc.o[mt][2] *= c0;
+    acc.o[mt][3] *= c1;
+  }
+  // P^T as the B operand of PV: transpose the two 8x8 halves.
+  const uint32_t pb0 = movmatrix_trans(pack_f16x2(P0, P1));
+  const uint32_t pb1 = movmatrix_trans(pack_f16x2(P2, P3));
+
+  // ---- O^T += V^T P^T ----
+  const int t[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
+  VData<VB> v;
+  v_load<VB>(vc, VROW, gid, t, v);
+  uint32_t s2a = 0, z2a = 0, s2c = 0, z2c = 0;
+  if constexpr (VB < 16) {
+    const int g = (16 * gid) / G;
+    const uint32_t sa = lds32(vsz + t[0] * szrow + 4 * g), sb = lds32(vsz + t[1] * szrow + 4 * g);
+    const uint32_t sc = lds32(vsz + t[2] * szrow + 4 * g), sd = lds32(vsz + t[3] * szrow + 4 * g);
+    s2a = prmt(sa, sb, 0x5410u);
+    z2a = prmt(sa, sb, 0x7632u);
+    s2c = prmt(sc, sd, 0x5410u);
+    z2c = prmt(sc, sd, 0x7632u);
+  }
+  const uint32_t ma = (t[0] < n ? 0x0000ffffu : 0u) | (t[1] < n ? 0xffff0000u : 0u);
+  const uint32_t mc = (t[2] < n ? 0x0000ffffu : 0u) | (t[3] < n ? 0xffff0000u : 0u);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t A[4] = {v_pair<VB>(v, 0, 1, mt), v_pair<VB>(v, 0, 1, 8 + mt), v_pair<VB>(v, 2, 3, mt),
+                     v_pair<VB>(v, 2, 3, 8 + mt)};
+    if constexpr (VB < 16) {
+      A[0] = hfma2_u(A[0], s2a, z2a);
+      A[1] = hfma2_u(A[1], s2a, z2a);
+      A[2] = hfma2_u(A[2], s2c, z2c);
+      A[3] = hfma2_u(A[3], s2c, z2c);
+    }
+    A[0] &= ma;
+    A[1] &= ma;
+    A[2] &= mc;
+    A[3] &= mc;
+    mma_f16(acc.o[mt], A, pb0, pb1);
+  }
+}
+
+template <int KB, int VB>
+__device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int ctid = warp * 32 + lane;  // 0..127
+  const Cut a = plan_cut(p.plan, c);
+  const Cut e = plan_cut(p.plan, c + 1);
+  const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
+  const int ppg = p.G >> 5;
+  uint32_t it = 0;
+  for (int u = a.u; u <= u_last; ++u) {
+    const int ps = (u == a.u) ? a.p : 0;
+    const int pe = (u == e.u) ? e.p : p.plan.T;
+    const UnitInfo ui = unit_info(p, u);
+    const int hq0 = ui.h * p.g + ui.hc * kNH;
+    const int nh = min(kNH, p.g - ui.hc * kNH);
+
+    // q of head column gid as the B operand, in the permuted d order; group sums.
+    uint32_t qb[8][2];
+    float qpart[4];
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (gid < nh)
+        raw = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<int64_t>(ui.b) * p.Hq + hq0 + gid) * kD + 32 * P + 8 * tig));
+      const float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                          bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+      qb[2 * P][0] = pack_f16x2(x[0], x[4]);
+      qb[2 * P][1] = pack_f16x2(x[1], x[5]);
+      qb[2 * P + 1][0] = pack_f16x2(x[2], x[6]);
+      qb[2 * P + 1][1] = pack_f16x2(x[3], x[7]);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += __half2float(__float2half_rn(x[i]));
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      qpart[P] = sum;
+    }
+    if (tig == 0) {
+#pragma unroll
+      for (int P = 0; P < 4; ++P) sm.qsum[warp][gid][P] = qpart[P];
+    }
+    __syncwarp();
+    float qsP[4][2];  // sum of q over the quantisation group of k-step pair P
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int g0 = (P / ppg) * ppg;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float s = 0.f;
+        for (int i = 0; i < ppg; ++i) s += sm.qsum[warp][2 * tig + cc][g0 + i];
+        qsP[P][cc] = s;
+      }
+    }
+
+    Acc acc;
+    acc.m[0] = acc.m[1] = -INFINITY;
+    acc.l[0] = acc.l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) acc.o[mt][0] = acc.o[mt][1] = acc.o[mt][2] = acc.o[mt][3] = 0.f;
+
+    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) {
+      const int st = it % kStages;
+      const uint32_t round = it / kStages;
+      if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
+      const uint8_t* base = sm.stage[st];
+      for (int kb = warp; kb * 16 < n; kb += kConsumerWarps) {
+        if (kind == kTilePacked)
+          kblock<KB, VB>(base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16,
+                         n, p.G, p.scale_log2, qb, qsP, gid, tig, acc);
+        else
+          kblock<16, 16>(base, nullptr, base + kBf16VOff, nullptr, kb * 16, n, p.G, p.scale_log2, qb,
+                         qsP, gid, tig, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[st]);
+      ++it;
+    });
+
+    // ---- merge the 4 warps' states and write the partial of (u, c) ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], off);
+      acc.l[1] += __shfl_xor_sync(0xffffffffu, acc.l[1], off);
+    }
+    if (gid == 0) {
+      sm.merge_ml[warp][2 * tig][0] = acc.m[0];
+      sm.merge_ml[warp][2 * tig][1] = acc.l[0];
+      sm.merge_ml[warp][2 * tig + 1][0] = acc.m[1];
+      sm.merge_ml[warp][2 * tig + 1][1] = acc.l[1];
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = 16 * gid + mt, d1 = d0 + 8;
+      sm.merge_o[warp][2 * tig][d0] = acc.o[mt][0];
+      sm.merge_o[warp][2 * tig + 1][d0] = acc.o[mt][1];
+      sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
+      sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
+    }
+    named_bar(1, kConsumerWarps * 32);
+    const int64_t slot = static_cast<int64_t>(u) + c;
+    const int d = ctid;
+    for (int j = 0; j < nh; ++j) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float sc = exp2f(sm.merge_ml[w][j][0] - M);
+          L = fmaf(sm.merge_ml[w][j][1], sc, L);
+          O = fmaf(sm.merge_o[w][j][d], sc, O);
+        }
+      }
+      if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
+      p.ws_o[(slot * kNH + j) * kD + d] = O;
+      if (d == 0) {
+        p.ws_ml[(slot * kNH + j) * 2] = M;
+        p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
+      }
+    }
+    named_bar(1, kConsumerWarps * 32);
+  }
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kSplitThreads, 2) split_mma_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumerWarps);
+    }
+    sm.abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the previous kernel in the stream may have written q or the cache
+  pdl_launch_dependents();
+  if (warp == kConsumerWarps) {
+    if (lane == 0) producer_loop(p, sm, blockIdx.x);
+    return;
+  }
+  consumer_loop<KB, VB>(p, sm, blockIdx.x, warp, lane);
+}
+
+}  // namespace kvq

@@ -1,0 +1,15 @@
+// Instantiations of the split-KV kernel for K bit-width 4 (all V widths);
+// one translation unit per K width so that they compile in parallel.
+#include "kvq_split.cuh"
+
+namespace kvq {
+const void* split_kernel_k4(int vb) {
+  switch (vb) {
+    case 2: return reinterpret_cast<const void*>(&split_mma_kernel<4, 2>);
+    case 4: return reinterpret_cast<const void*>(&split_mma_kernel<4, 4>);
+    case 8: return reinterpret_cast<const void*>(&split_mma_kernel<4, 8>);
+    case 16: return reinterpret_cast<const void*>(&split_mma_kernel<4, 16>);
+  }
+  return nullptr;
+}
+}  // namespace kvq

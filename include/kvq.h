@@ -63,8 +63,8 @@ typedef enum kvq_status {
 
 /* Segments of one layer's cache buffer (see kvq_layout.off / .bytes). */
 enum kvq_segment {
-  KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv][D*k_bits/32]; bf16 rows if k_bits == 16 */
-  KVQ_SEG_K_SZ = 1,    /* half2 (s, z) [B][n_packed][Tv][D/G]; empty if k_bits == 16 */
+  KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv_pad][D*k_bits/32]; bf16 rows if k_bits == 16 */
+  KVQ_SEG_K_SZ = 1,    /* half2 (s, z) [B][n_packed][Tv_pad][D/G]; empty if k_bits == 16 */
   KVQ_SEG_V_CODES = 2, /* as K_CODES with v_bits */
   KVQ_SEG_V_SZ = 3,    /* as K_SZ with v_bits */
   KVQ_SEG_PROT_K = 4,  /* bf16 [B][n_prot][Tv][D]: visual K of protected heads */
@@ -95,6 +95,7 @@ typedef struct kvq_layout {
   int32_t n_prot;     /* protected KV heads */
   int32_t n_packed;   /* unprotected KV heads */
   int32_t Tv;         /* vis_end - vis_start: visual rows per (b, head) */
+  int32_t Tv_pad;     /* Tv rounded up to a multiple of 16: row stride of the packed segments */
   int32_t T_text;     /* T_cap - Tv: text rows per (b, head) */
   int32_t units;      /* B * H_kv * ceil(g / KVQ_HEADS_PER_UNIT) */
   int32_t slot[KVQ_MAX_HEADS];        /* head -> index among its kind (protected / packed) */

@@ -82,6 +82,7 @@ def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.nda
     Returns the number of packed rows compared."""
     cn = cache.cpu().numpy()
     B, H, D, Tv, Tt = c.B, c.H_kv, c.D, int(L.Tv), int(L.T_text)
+    Tvp = int(L.Tv_pad)
     b_sel = list(range(B)) if b_sel is None else list(b_sel)
     prot = [h for h in range(H) if h in c.prot]
     pack = [h for h in range(H) if h not in c.prot]
@@ -108,13 +109,13 @@ def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.nda
         if not pack:
             continue
         if nbits == 16:
-            raw = seg(L, cn, sc, np.uint16).reshape(B, len(pack), Tv, D)
+            raw = seg(L, cn, sc, np.uint16).reshape(B, len(pack), Tvp, D)
             for i, b in enumerate(b_sel):
                 assert np.array_equal(raw[b, :, :nvis], x_np[i][pack][:, c.vs:c.vs + nvis])
             continue
         W = D * nbits // 32
-        words = seg(L, cn, sc, np.uint32).reshape(B, len(pack), Tv, W)
-        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pack), Tv, D // c.G, 2)
+        words = seg(L, cn, sc, np.uint32).reshape(B, len(pack), Tvp, W)
+        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pack), Tvp, D // c.G, 2)
         for i, b in enumerate(b_sel):
             xin = np.ascontiguousarray(x_np[i][pack][:, c.vs:c.vs + nvis])
             w_ref, s_ref, z_ref = oracle.quantize_pack_rows(xin, c.G, nbits)

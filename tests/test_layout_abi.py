@@ -37,11 +37,12 @@ def _align(x, a):
 def _expected(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot):
     """Independent restatement of the documented segment shapes."""
     Tv = ve - vs
+    Tvp = -(-Tv // 16) * 16
     npr = len(prot)
     npk = Hkv - npr
     rb = [D * kb // 8, 4 * D // G if kb < 16 else 0, D * vb // 8, 4 * D // G if vb < 16 else 0,
           2 * D, 2 * D, 2 * D, 2 * D]
-    rows = [B * npk * Tv] * 4 + [B * npr * Tv] * 2 + [B * Hkv * (Tcap - Tv)] * 2
+    rows = [B * npk * Tvp] * 4 + [B * npr * Tv] * 2 + [B * Hkv * (Tcap - Tv)] * 2
     off, offs = 0, []
     for r, n in zip(rb, rows):
         offs.append(off)
@@ -70,7 +71,7 @@ def test_layout_matches_formula(lib, case):
     assert list(L.off) == offs and L.total_bytes == total
     assert all(o % 256 == 0 for o in L.off)
     assert L.g == Hq // Hkv and L.n_prot == len(prot) and L.n_packed == Hkv - len(prot)
-    assert L.Tv == ve - vs and L.T_text == Tcap - (ve - vs)
+    assert L.Tv == ve - vs and L.T_text == Tcap - (ve - vs) and L.Tv_pad == -(-(ve - vs) // 16) * 16
     nhc = -(-(Hq // Hkv) // 8)
     assert L.units == B * Hkv * nhc
     # head -> slot -> head round trip
