@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
+#include "kvq_ptx.cuh"
 
 namespace kvq {
 namespace {
@@ -68,10 +69,22 @@ __device__ __forceinline__ void quantize_store(const Params& p, uint8_t* codes_r
   }
 }
 
-__global__ void __launch_bounds__(256) append_kernel(Params p, const uint16_t* __restrict__ kin,
-                                                     const uint16_t* __restrict__ vin, int64_t sb,
-                                                     int64_t sh, int64_t st, int32_t t0,
-                                                     int32_t n_tok) {
+struct AppendArgs {
+  Params p;
+  const uint16_t* kin;
+  const uint16_t* vin;
+  int64_t sb, sh, st;
+  int32_t t0, n_tok;
+};
+
+__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
+  pdl_wait();  // the previous kernel in the stream may still read the cache
+  pdl_launch_dependents();
+  const Params& p = a.p;
+  const uint16_t* __restrict__ kin = a.kin;
+  const uint16_t* __restrict__ vin = a.vin;
+  const int64_t sb = a.sb, sh = a.sh, st = a.st;
+  const int32_t t0 = a.t0, n_tok = a.n_tok;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nrows = static_cast<int64_t>(p.B) * p.Hkv * n_tok;
@@ -140,8 +153,26 @@ extern "C" kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, cons
   const int64_t rows = static_cast<int64_t>(L->d.B) * L->d.H_kv * n_tok;
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
-  kvq::append_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      p, static_cast<const uint16_t*>(k_bf16), static_cast<const uint16_t*>(v_bf16), stride_b,
-      stride_h, stride_t, t0, n_tok);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  kvq::AppendArgs a;
+  a.p = p;
+  a.kin = static_cast<const uint16_t*>(k_bf16);
+  a.vin = static_cast<const uint16_t*>(v_bf16);
+  a.sb = stride_b;
+  a.sh = stride_h;
+  a.st = stride_t;
+  a.t0 = t0;
+  a.n_tok = n_tok;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* kargs[1] = {&a};
+  if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&kvq::append_kernel), kargs) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
 }

@@ -27,11 +27,11 @@ const void* split_kernel_k4(int vb);
 const void* split_kernel_k8(int vb);
 const void* split_kernel_k16(int vb);
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineWarps = 16;
 
 // ---------------------------------------------------------------------------
-// Combine: one CTA per (b, hq).  Warp w folds slots w, w + 8, ... with an
-// online rescaling; the 8 warp states are merged in shared memory.  Lane l
+// Combine: one CTA per (b, hq).  16 warps fold the unit's partial slots with
+// an online rescaling; the warp states are merged in shared memory.  Lane l
 // owns d = 4l .. 4l+3.  A NaN partial max (a failed wait in the split kernel)
 // turns the output into NaN.
 // ---------------------------------------------------------------------------
@@ -50,27 +50,43 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   const int j = r - hc * kNH;
   const int u = unit_of(p, b, h, hc);
   int cf, cl;
-  plan_unit_chunks(p.plan, u, &cf, &cl);
+  plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
   if (threadIdx.x == 0) sm_bad = 0;
   __syncthreads();
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   bool bad = false;
-  for (int c = cf + warp; c <= cl; c += kCombineWarps) {
-    const int64_t s = static_cast<int64_t>(u + c) * kNH + j;
-    const float m = p.ws_ml[s * 2];
-    const float l = p.ws_ml[s * 2 + 1];
-    const float4 o = reinterpret_cast<const float4*>(p.ws_o + s * kD)[lane];
-    if (m != m) bad = true;
-    if (m == -INFINITY || m != m) continue;
-    const float Mn = fmaxf(M, m);
-    const float a = exp2f(M - Mn), w = exp2f(m - Mn);
-    L = L * a + l * w;
-    O.x = O.x * a + o.x * w;
-    O.y = O.y * a + o.y * w;
-    O.z = O.z * a + o.z * w;
-    O.w = O.w * a + o.w * w;
-    M = Mn;
+  // Warp w folds slots cf + 8w + {0..7}, then the next 8 * kCombineWarps;
+  // the eight loads of a batch are issued before any of them is used.
+  for (int c0 = cf + 8 * warp; c0 <= cl; c0 += 8 * kCombineWarps) {
+    float mb[8], lb[8];
+    float4 ob[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      mb[k] = -INFINITY;
+      lb[k] = 0.f;
+      ob[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 + k <= cl) {
+        const int64_t s = static_cast<int64_t>(u + c0 + k) * kNH + j;
+        mb[k] = p.ws_ml[s * 2];
+        lb[k] = p.ws_ml[s * 2 + 1];
+        ob[k] = reinterpret_cast<const float4*>(p.ws_o + s * kD)[lane];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float m = mb[k];
+      if (m != m) bad = true;
+      if (m == -INFINITY || m != m) continue;
+      const float Mn = fmaxf(M, m);
+      const float a = exp2f(M - Mn), w = exp2f(m - Mn);
+      L = L * a + lb[k] * w;
+      O.x = O.x * a + ob[k].x * w;
+      O.y = O.y * a + ob[k].y * w;
+      O.z = O.z * a + ob[k].z * w;
+      O.w = O.w * a + ob[k].w * w;
+      M = Mn;
+    }
   }
   if (bad) sm_bad = 1;
   if (lane == 0) {
@@ -137,22 +153,6 @@ const void* split_kernel_for(int kb, int vb) {
 constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
 static_assert(kSplitSmemBytes <= (233472 - 2 * 1024) / 2, "split kernel must fit twice per SM");
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       kvq::Params* p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[1] = {p};
-  return cudaLaunchKernelExC(&cfg, fn, args);
-}
-
 }  // namespace
 
 extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
@@ -188,6 +188,7 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   packed_tile_geometry(&p);
   p.plan = kvq_make_plan(L, T, 2 * n_sm);
+  for (int c = 0; c <= p.plan.C; ++c) p.cuts[c] = kvq::plan_cut(p.plan, c);
 
   // Opt each split kernel into >48 KB of dynamic shared memory, once.
   static std::mutex mu;
@@ -202,11 +203,10 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
       done = true;
     }
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(split, dim3(p.plan.C), dim3(kvq::kSplitThreads), kSplitSmemBytes, s, &p) != cudaSuccess)
+  if (kvq_launch_pdl(split, p.plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, &p) != 0)
     return KVQ_ERR_CUDA;
-  if (launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), dim3(L->d.B * L->d.H_q),
-                 dim3(kvq::kCombineWarps * 32), 0, s, &p) != cudaSuccess)
+  if (kvq_launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), L->d.B * L->d.H_q,
+                     kvq::kCombineWarps * 32, 0, stream, &p) != 0)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

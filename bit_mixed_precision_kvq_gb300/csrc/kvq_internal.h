@@ -5,11 +5,12 @@
 //   * a "unit" is one (sequence b, KV head h, chunk hc of up to 8 of the g
 //     query heads that read h).  Protected-head units come first, then the
 //     packed-head units; inside each kind the order is (b, slot, hc).
-//   * every unit is a stream of positions 0..T-1; a position costs 512 bytes
-//     (bf16 K + V rows) unless it is a visual position of a packed head,
-//     which costs the packed K and V rows plus their fp16 scale/zero.
-//   * the concatenated byte stream of all units is cut into C chunks of
-//     equal bytes; CTA c processes [cut(c), cut(c+1)).  Cuts inside a packed
+//   * every unit is a stream of positions 0..T-1; a position costs its cache
+//     bytes -- 512 (bf16 K + V rows), or for a visual position of a packed
+//     head the packed K and V rows plus their fp16 scale/zero -- plus a
+//     fixed compute cost (kPosCost).
+//   * the concatenated cost stream of all units is cut into C chunks of
+//     equal cost; CTA c processes [cut(c), cut(c+1)).  Cuts inside a packed
 //     visual range are rounded down to a multiple of 16 rows so every staged
 //     tile starts on a 16-byte boundary in every segment.
 //   * CTA c writes one partial result (o, m, l) per unit it touches into
@@ -33,6 +34,11 @@ constexpr int kD = 128;          // head dimension supported by the kernels
 constexpr int kNH = KVQ_HEADS_PER_UNIT;  // query heads per unit (MMA N = 8)
 constexpr int kBf16PosBytes = 4 * kD;    // K + V bf16 rows of one position
 constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
+// Work balance: a position costs its cache bytes plus this many byte
+// equivalents of unpack / tensor-core / softmax work, so that chunks of
+// cheap packed rows do not get several times more positions to compute.
+constexpr int kPosCost = 256;
+constexpr int kBf16PosCost = kBf16PosBytes + kPosCost;
 
 struct Plan {
   int32_t U_p;        // protected units
@@ -41,10 +47,10 @@ struct Plan {
   int32_t NHC;        // query-head chunks per KV head
   int32_t vsa, vea;   // attended visual positions [vsa, vea)
   int32_t T;          // attended positions
-  int32_t w_vis;      // bytes of one packed visual position (K + V, codes + s/z)
-  int64_t ub_p, ub_u; // bytes of a protected / packed unit
+  int32_t w_vis;      // cost of one packed visual position (bytes + kPosCost)
+  int64_t ub_p, ub_u; // cost of a protected / packed unit
   int64_t P_bytes;    // U_p * ub_p
-  int64_t total;      // all bytes
+  int64_t total;      // cost of all units
 };
 
 struct Cut {
@@ -65,44 +71,44 @@ KVQ_HD Cut plan_cut(const Plan& P, int32_t c) {
     const int64_t u = X / P.ub_p;
     const int64_t rem = X - u * P.ub_p;
     r.u = static_cast<int32_t>(u);
-    r.p = static_cast<int32_t>(rem / kBf16PosBytes);
+    r.p = static_cast<int32_t>(rem / kBf16PosCost);
     return r;
   }
   const int64_t Xu = X - P.P_bytes;
   const int64_t u = Xu / P.ub_u;
   const int64_t rem = Xu - u * P.ub_u;
   r.u = P.U_p + static_cast<int32_t>(u);
-  const int64_t pre = static_cast<int64_t>(P.vsa) * kBf16PosBytes;
+  const int64_t pre = static_cast<int64_t>(P.vsa) * kBf16PosCost;
   const int64_t vis = static_cast<int64_t>(P.vea - P.vsa) * P.w_vis;
   if (rem < pre) {
-    r.p = static_cast<int32_t>(rem / kBf16PosBytes);
+    r.p = static_cast<int32_t>(rem / kBf16PosCost);
   } else if (rem < pre + vis) {
     int64_t row = (rem - pre) / P.w_vis;
     row -= row % kVisAlign;
     r.p = P.vsa + static_cast<int32_t>(row);
   } else {
-    r.p = P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosBytes);
+    r.p = P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosCost);
   }
   return r;
 }
 
-// Chunks that hold a piece of unit u: [c_first, c_last].
-//   c_last  = max c with cut(c).u <= u
-//   c_first = min c with (cut(c+1).u clamped to U-1) >= u
-KVQ_HD void plan_unit_chunks(const Plan& P, int32_t u, int32_t* c_first, int32_t* c_last) {
-  // c_last: number of c in [0, C) with cut(c).u <= u, minus one (cut(0).u == 0 <= u).
-  int32_t lo = 0, hi = P.C - 1;  // invariant: cut(lo).u <= u
+// Chunks that hold a piece of unit u: [c_first, c_last], by binary search
+// over a table of the cuts (cuts[c] = plan_cut(P, c), c = 0..C).
+//   c_last  = max c with cuts[c].u <= u
+//   c_first = min c with min(cuts[c+1].u, U-1) >= u
+KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t* c_first,
+                             int32_t* c_last) {
+  int32_t lo = 0, hi = P.C - 1;  // invariant: cuts[lo].u <= u
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) / 2;
-    if (plan_cut(P, mid).u <= u) lo = mid; else hi = mid - 1;
+    if (cuts[mid].u <= u) lo = mid; else hi = mid - 1;
   }
   *c_last = lo;
-  // c_first: smallest c in [0, C) with end unit >= u; end unit of c = min(cut(c+1).u, U-1).
   lo = 0;
   hi = P.C - 1;  // end unit of C-1 is U-1 >= u
   while (lo < hi) {
     const int32_t mid = (lo + hi) / 2;
-    int32_t eu = plan_cut(P, mid + 1).u;
+    int32_t eu = cuts[mid + 1].u;
     if (eu > P.U - 1) eu = P.U - 1;
     if (eu >= u) hi = mid; else lo = mid + 1;
   }
@@ -131,6 +137,7 @@ struct Params {
   float* ws_ml;        // [slots][kNH][2]
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
+  Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host
   uint8_t prot[KVQ_MAX_HEADS];        // head -> protected?
   int32_t slot[KVQ_MAX_HEADS];        // head -> slot
   uint8_t prot_head[KVQ_MAX_HEADS];   // protected slot -> head
@@ -171,3 +178,8 @@ kvq_status kvq_check_layout(const kvq_layout* L);
 void kvq_fill_params(const kvq_layout* L, kvq::Params* p);
 kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target);
 int kvq_device_sm_count(int* n_sm);
+// Launch `fn(*p)` with programmatic stream serialisation allowed, so that its
+// CTAs may be scheduled while the previous kernel in the stream drains (the
+// kernel itself waits with griddepcontrol.wait before touching memory).
+int kvq_launch_pdl(const void* fn, unsigned grid, unsigned block, size_t smem, void* stream,
+                   kvq::Params* p);

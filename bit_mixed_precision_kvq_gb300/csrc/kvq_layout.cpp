@@ -159,16 +159,17 @@ kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target)
   P.vsa = d.vis_start < T ? d.vis_start : T;
   P.vea = d.vis_end < T ? d.vis_end : T;
   P.w_vis = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES] + L->row_bytes[KVQ_SEG_K_SZ] +
-                                 L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ]);
+                                 L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ]) +
+            kvq::kPosCost;
   P.U_p = d.B * L->n_prot * P.NHC;
   P.U = d.B * d.H_kv * P.NHC;
-  P.ub_p = static_cast<int64_t>(T) * kvq::kBf16PosBytes;
+  P.ub_p = static_cast<int64_t>(T) * kvq::kBf16PosCost;
   const int64_t n_vis = P.vea - P.vsa;
-  P.ub_u = (static_cast<int64_t>(T) - n_vis) * kvq::kBf16PosBytes + n_vis * P.w_vis;
+  P.ub_u = (static_cast<int64_t>(T) - n_vis) * kvq::kBf16PosCost + n_vis * P.w_vis;
   P.P_bytes = static_cast<int64_t>(P.U_p) * P.ub_p;
   P.total = P.P_bytes + static_cast<int64_t>(P.U - P.U_p) * P.ub_u;
   // Chunks: the target (a whole number of CTAs per SM), but no chunk below
-  // 8 KiB of cache bytes and never more than KVQ_MAX_CTAS.
+  // 8 Ki cost units and never more than KVQ_MAX_CTAS.
   int64_t C = n_chunks_target;
   const int64_t by_size = (P.total + 8191) / 8192;
   if (C > by_size) C = by_size;
@@ -193,4 +194,20 @@ int kvq_device_sm_count(int* n_sm) {
   if (dev >= 0 && dev < 64) cache[dev] = v;
   *n_sm = v;
   return 0;
+}
+
+int kvq_launch_pdl(const void* fn, unsigned grid, unsigned block, size_t smem, void* stream,
+                   kvq::Params* p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[1] = {p};
+  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 0 : -1;
 }

@@ -71,8 +71,8 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // Producer
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
-  const Cut a = plan_cut(p.plan, c);
-  const Cut e = plan_cut(p.plan, c + 1);
+  const Cut a = p.cuts[c];
+  const Cut e = p.cuts[c + 1];
   const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
   uint32_t it = 0;
   for (int u = a.u; u <= u_last; ++u) {
@@ -265,36 +265,55 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   const uint8_t* krow1 = kc + (r0 + gid + 8) * KROW;
 
   // ---- S^T = K q^T (scaled to log2 units) ----
-  float S[4] = {0.f, 0.f, 0.f, 0.f};
-  float C[4] = {0.f, 0.f, 0.f, 0.f};
-  const int ppg = G >> 5;  // k-step pairs per quantisation group: 1, 2 or 4
+  // One accumulator per k-step pair keeps the MMA dependency chains short.
+  float C[4][4];
 #pragma unroll
   for (int P = 0; P < 4; ++P) {
+    C[P][0] = C[P][1] = C[P][2] = C[P][3] = 0.f;
     uint32_t f0[4], f1[4];
     k_row_pairs<KB>(krow0, P, tig, f0);
     k_row_pairs<KB>(krow1, P, tig, f1);
     const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
     const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
-    mma_f16(C, A0, qb[2 * P][0], qb[2 * P][1]);
-    mma_f16(C, A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
-    if constexpr (KB < 16) {
-      if (((P + 1) & (ppg - 1)) == 0) {  // end of a quantisation group
-        const int g = P / ppg;
-        const uint32_t sz0 = lds32(ksz + (r0 + gid) * szrow + 4 * g);
-        const uint32_t sz1 = lds32(ksz + (r0 + gid + 8) * szrow + 4 * g);
-        const float s0 = f16lo(sz0) * sl2, z0 = f16hi(sz0) * sl2;
-        const float s1 = f16lo(sz1) * sl2, z1 = f16hi(sz1) * sl2;
-        S[0] = fmaf(s0, C[0], fmaf(z0, qsP[P][0], S[0]));
-        S[1] = fmaf(s0, C[1], fmaf(z0, qsP[P][1], S[1]));
-        S[2] = fmaf(s1, C[2], fmaf(z1, qsP[P][0], S[2]));
-        S[3] = fmaf(s1, C[3], fmaf(z1, qsP[P][1], S[3]));
-        C[0] = C[1] = C[2] = C[3] = 0.f;
-      }
-    }
+    mma_f16(C[P], A0, qb[2 * P][0], qb[2 * P][1]);
+    mma_f16(C[P], A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
   }
+  float S[4];
   if constexpr (KB == 16) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[i] = C[i] * sl2;
+    for (int i = 0; i < 4; ++i) S[i] = ((C[0][i] + C[1][i]) + (C[2][i] + C[3][i])) * sl2;
+  } else {
+    // Sum the pairs of each quantisation group, then apply its scale/zero
+    // (qsP[P] already holds the q sum of the group that contains pair P).
+    S[0] = S[1] = S[2] = S[3] = 0.f;
+    auto apply = [&](const float (&Cg)[4], const float (&qg)[2], int g) {
+      const uint32_t sz0 = lds32(ksz + (r0 + gid) * szrow + 4 * g);
+      const uint32_t sz1 = lds32(ksz + (r0 + gid + 8) * szrow + 4 * g);
+      const float s0 = f16lo(sz0) * sl2, z0 = f16hi(sz0) * sl2;
+      const float s1 = f16lo(sz1) * sl2, z1 = f16hi(sz1) * sl2;
+      S[0] = fmaf(s0, Cg[0], fmaf(z0, qg[0], S[0]));
+      S[1] = fmaf(s0, Cg[1], fmaf(z0, qg[1], S[1]));
+      S[2] = fmaf(s1, Cg[2], fmaf(z1, qg[0], S[2]));
+      S[3] = fmaf(s1, Cg[3], fmaf(z1, qg[1], S[3]));
+    };
+    if (G == 32) {
+      apply(C[0], qsP[0], 0);
+      apply(C[1], qsP[1], 1);
+      apply(C[2], qsP[2], 2);
+      apply(C[3], qsP[3], 3);
+    } else if (G == 64) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        C[0][i] += C[1][i];
+        C[2][i] += C[3][i];
+      }
+      apply(C[0], qsP[0], 0);
+      apply(C[2], qsP[2], 1);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) C[0][i] = (C[0][i] + C[1][i]) + (C[2][i] + C[3][i]);
+      apply(C[0], qsP[0], 0);
+    }
   }
   const bool ok0 = r0 + gid < n, ok1 = r0 + gid + 8 < n;
   if (!ok0) S[0] = S[1] = -INFINITY;
@@ -316,12 +335,14 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   acc.m[1] = mn1;
   acc.l[0] = fmaf(acc.l[0], c0, P0 + P2);
   acc.l[1] = fmaf(acc.l[1], c1, P1 + P3);
+  if (!__all_sync(0xffffffffu, c0 == 1.f && c1 == 1.f)) {  // some running max moved
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    acc.o[mt][0] *= c0;
-    acc.o[mt][1] *= c1;
-    acc.o[mt][2] *= c0;
-    acc.o[mt][3] *= c1;
+    for (int mt = 0; mt < 8; ++mt) {
+      acc.o[mt][0] *= c0;
+      acc.o[mt][1] *= c1;
+      acc.o[mt][2] *= c0;
+      acc.o[mt][3] *= c1;
+    }
   }
   // P^T as the B operand of PV: transpose the two 8x8 halves.
   const uint32_t pb0 = movmatrix_trans(pack_f16x2(P0, P1));
@@ -341,6 +362,9 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
     s2c = prmt(sc, sd, 0x5410u);
     z2c = prmt(sc, sd, 0x7632u);
   }
+  // Rows past n hold stale shared memory (possibly NaN/Inf patterns): zero
+  // their V operands so that 0 * garbage cannot reach the accumulators.
+  const bool ragged = r0 + 16 > n;
   const uint32_t ma = (t[0] < n ? 0x0000ffffu : 0u) | (t[1] < n ? 0xffff0000u : 0u);
   const uint32_t mc = (t[2] < n ? 0x0000ffffu : 0u) | (t[3] < n ? 0xffff0000u : 0u);
 #pragma unroll
@@ -353,10 +377,12 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
       A[2] = hfma2_u(A[2], s2c, z2c);
       A[3] = hfma2_u(A[3], s2c, z2c);
     }
-    A[0] &= ma;
-    A[1] &= ma;
-    A[2] &= mc;
-    A[3] &= mc;
+    if (ragged) {
+      A[0] &= ma;
+      A[1] &= ma;
+      A[2] &= mc;
+      A[3] &= mc;
+    }
     mma_f16(acc.o[mt], A, pb0, pb1);
   }
 }
@@ -365,8 +391,8 @@ template <int KB, int VB>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0..127
-  const Cut a = plan_cut(p.plan, c);
-  const Cut e = plan_cut(p.plan, c + 1);
+  const Cut a = p.cuts[c];
+  const Cut e = p.cuts[c + 1];
   const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
   const int ppg = p.G >> 5;
   uint32_t it = 0;
