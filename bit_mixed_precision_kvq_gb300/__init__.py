@@ -17,6 +17,7 @@ from typing import Optional, Sequence
 __all__ = [
     "KvqError", "load", "lib_path", "cache_layout", "quantize_append", "decode_attention",
     "kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention", "KVQ_MAX_HEADS",
+    "decode_attention_static_ws", "kvq_decode_attention_static_ws", "STATIC_WS_BYTES",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
@@ -28,7 +29,8 @@ KVQ_NSEG = 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
 EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
-                    "kvq_status_string"]
+                    "kvq_decode_attention_static_ws", "kvq_status_string"]
+STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -86,6 +88,8 @@ def load() -> ctypes.CDLL:
     lib.kvq_quantize_append.restype = ctypes.c_int
     lib.kvq_decode_attention.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P, sz, P]
     lib.kvq_decode_attention.restype = ctypes.c_int
+    lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
+    lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -159,7 +163,24 @@ def decode_attention(L: Layout, cache, q, T: int, out, softmax_scale: Optional[f
         raise KvqError(st, "kvq_decode_attention")
 
 
+def decode_attention_static_ws(L: Layout, cache, q, T: int, out,
+                               softmax_scale: Optional[float] = None, lse=None,
+                               stream=None) -> None:
+    """kvq_decode_attention_static_ws: same result as decode_attention, for
+    callers that may not allocate device memory -- the scratch is a fixed
+    array inside the library (STATIC_WS_BYTES per GPU).  Calls on one device
+    share that array, so they must not overlap on the GPU."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    st = load().kvq_decode_attention_static_ws(ctypes.byref(L), _addr(cache), _addr(q), int(T),
+                                               float(softmax_scale), _addr(out), _addr(lse),
+                                               _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_attention_static_ws")
+
+
 # Same names as the C entry points.
 kvq_cache_layout = cache_layout
 kvq_quantize_append = quantize_append
 kvq_decode_attention = decode_attention
+kvq_decode_attention_static_ws = decode_attention_static_ws

@@ -158,6 +158,35 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
                                 int32_t T, float softmax_scale, void* out_bf16, float* lse,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/* Size in bytes of the device scratch array used by
+ * kvq_decode_attention_static_ws (16 MiB: enough for layouts with up to
+ * 3008 units, i.e. B * H_kv * ceil(g/8) <= 3008). */
+#define KVQ_STATIC_WS_BYTES (16u * 1024u * 1024u)
+
+/*
+ * kvq_decode_attention_static_ws -- the pages have no counterpart to this
+ * entry point; it exists for callers that are not allowed to allocate
+ * device memory (for example a plug-in whose host framework owns every
+ * device allocation, or a serving loop that must never allocate).
+ * It computes exactly what kvq_decode_attention computes, with the same
+ * arguments minus the workspace: the split-KV scratch lives in a fixed
+ * KVQ_STATIC_WS_BYTES array inside the library's device image, present on
+ * every GPU that loads the library until the process exits.  No device
+ * memory is allocated by this call.
+ *   - Returns KVQ_ERR_CAPACITY, before any CUDA call, when
+ *     L->workspace_bytes > KVQ_STATIC_WS_BYTES.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device); make that first call before
+ *     any stream capture on that device.
+ *   - All calls on a device share the one array.  Calls whose kernels may
+ *     run at the same time on the GPU (unordered streams) race on it; order
+ *     them on one stream or use kvq_decode_attention with separate
+ *     workspaces.  The array's contents on entry do not matter.
+ */
+kvq_status kvq_decode_attention_static_ws(const kvq_layout* L, const void* cache,
+                                          const void* q_bf16, int32_t T, float softmax_scale,
+                                          void* out_bf16, float* lse, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvq_status_string(kvq_status s);
 
