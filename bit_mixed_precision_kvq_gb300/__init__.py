@@ -29,7 +29,7 @@ KVQ_NSEG = 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
 EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
-                    "kvq_decode_attention_static_ws", "kvq_status_string"]
+                    "kvq_decode_attention_static_ws", "kvq_last_cuda_error", "kvq_status_string"]
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,12 @@ def lib_path() -> str:
 
 class KvqError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        msg = f"{what}: {STATUS.get(status, status)}"
+        self.cuda_error = 0
+        if status == 4 and _lib is not None:
+            self.cuda_error = int(_lib.kvq_last_cuda_error())
+            msg += f" (cudaError {self.cuda_error})"
+        super().__init__(msg)
         self.status = status
 
 
@@ -90,6 +95,8 @@ def load() -> ctypes.CDLL:
     lib.kvq_decode_attention.restype = ctypes.c_int
     lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
     lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
+    lib.kvq_last_cuda_error.argtypes = []
+    lib.kvq_last_cuda_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     _lib = lib

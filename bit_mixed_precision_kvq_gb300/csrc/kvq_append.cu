@@ -172,7 +172,7 @@ extern "C" kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* kargs[1] = {&a};
-  if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&kvq::append_kernel), kargs) != cudaSuccess)
-    return KVQ_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&kvq::append_kernel), kargs);
+  if (e != cudaSuccess) return kvq_cuda_fail(e);
   return KVQ_OK;
 }

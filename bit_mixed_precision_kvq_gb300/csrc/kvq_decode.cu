@@ -149,9 +149,10 @@ const void* split_kernel_for(int kb, int vb) {
   return nullptr;
 }
 
-// Two CTAs per SM: 2 x (115,584 + 1,024 reserved) bytes fit the SM's 228 KiB.
+// One CTA per SM: the stage ring, merge buffers and barriers must fit the
+// 227 KiB a CTA may use.
 constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
-static_assert(kSplitSmemBytes <= (233472 - 2 * 1024) / 2, "split kernel must fit twice per SM");
+static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
 
 }  // namespace
 
@@ -187,7 +188,7 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   packed_tile_geometry(&p);
-  p.plan = kvq_make_plan(L, T, 2 * n_sm);
+  p.plan = kvq_make_plan(L, T, n_sm);  // one CTA per SM
   for (int c = 0; c <= p.plan.C; ++c) p.cuts[c] = kvq::plan_cut(p.plan, c);
 
   // Opt each split kernel into >48 KB of dynamic shared memory, once.
@@ -197,9 +198,13 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
     std::lock_guard<std::mutex> lock(mu);
     bool& done = smem_set[L->d.k_bits][L->d.v_bits];
     if (!done) {
-      if (cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSplitSmemBytes)) != cudaSuccess)
-        return KVQ_ERR_CUDA;
+      const cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kSplitSmemBytes));
+      if (e != cudaSuccess) return kvq_cuda_fail(e);
+      cudaFuncAttributes fa;
+      const cudaError_t e2 = cudaFuncGetAttributes(&fa, split);
+      if (e2 != cudaSuccess) return kvq_cuda_fail(e2);
+      if (fa.maxThreadsPerBlock < kvq::kSplitThreads) return kvq_cuda_fail(cudaErrorLaunchOutOfResources);
       done = true;
     }
   }

@@ -37,13 +37,15 @@ void* scratch_ptr[kMaxDevices] = {};
 // device (the first call on a device does this set-up).
 kvq_status scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return kvq_cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(scratch_mu);
   if (!scratch_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, kvq_static_scratch) != cudaSuccess || p == nullptr)
-      return KVQ_ERR_CUDA;
+    const cudaError_t se = cudaGetSymbolAddress(&p, kvq_static_scratch);
+    if (se != cudaSuccess) return kvq_cuda_fail(se);
+    if (p == nullptr) return kvq_cuda_fail(cudaErrorInvalidSymbol);
     scratch_ptr[dev] = p;
   }
   *out = scratch_ptr[dev];

@@ -178,6 +178,8 @@ kvq_status kvq_check_layout(const kvq_layout* L);
 void kvq_fill_params(const kvq_layout* L, kvq::Params* p);
 kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target);
 int kvq_device_sm_count(int* n_sm);
+// Record a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.
+kvq_status kvq_cuda_fail(int err);
 // Launch `fn(*p)` with programmatic stream serialisation allowed, so that its
 // CTAs may be scheduled while the previous kernel in the stream drains (the
 // kernel itself waits with griddepcontrol.wait before touching memory).

@@ -179,18 +179,31 @@ kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target)
   return P;
 }
 
+namespace {
+thread_local int last_cuda_error = 0;
+}
+
+kvq_status kvq_cuda_fail(int err) {
+  last_cuda_error = err;
+  return KVQ_ERR_CUDA;
+}
+
+extern "C" int kvq_last_cuda_error(void) { return last_cuda_error; }
+
 int kvq_device_sm_count(int* n_sm) {
   static std::mutex mu;
   static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return kvq_cuda_fail(e), -1;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && cache[dev] > 0) {
     *n_sm = cache[dev];
     return 0;
   }
   int v = 0;
-  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return kvq_cuda_fail(e), -1;
   if (dev >= 0 && dev < 64) cache[dev] = v;
   *n_sm = v;
   return 0;
@@ -209,5 +222,10 @@ int kvq_launch_pdl(const void* fn, unsigned grid, unsigned block, size_t smem, v
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[1] = {p};
-  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 0 : -1;
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) {
+    kvq_cuda_fail(e);
+    return -1;
+  }
+  return 0;
 }

@@ -5,22 +5,25 @@
 // registers, and consumed at once by QK, an online softmax and PV; nothing
 // dequantised is ever written to device memory.
 //
-// CTA = 1 producer warp + 4 consumer warps.
+// CTA = 1 producer warp + 11 consumer warps, one CTA per SM.
 //   producer : one lane walks the CTA's tiles and issues 1-D bulk async
 //              copies (TMA) of the tile's K/V rows (+ scale/zero rows) into a
-//              3-stage ring of 32 KB stages, signalled by mbarriers.
-//   consumers: each 16-position block of a tile goes to one warp.  QK and PV
+//              5-stage ring of 32 KB stages, signalled by mbarriers.
+//   consumers: the CTA's 16-position blocks are dealt round-robin to the 11
+//              warps across tile boundaries (every warp still waits for and
+//              releases every tile, which keeps the mbarrier phases exact).  QK and PV
 //              run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 //              accumulate) with the unit's <= 8 query heads as N = 8:
 //                QK: S^T[t][j] = K[t][:] . q[j][:]    (M = 16 positions)
 //                PV: O^T[d][j] += V^T[d][t] P^T[t][j] (M = 16 of the D rows)
-//              Codes become fp16 with the 0x6400 exponent trick
-//              (1024 + c, then subtract 1024: exact), so QK accumulates
-//              sum_d c*q exactly per quantisation group and applies the
-//              group's scale and zero afterwards:
-//                q.k_hat = sum_g ( s_g * sum_{d in g} q_d c_d + z_g * sum_{d in g} q_d ).
-//              V is dequantised per element in f16x2 (c*s + z, one rounding)
-//              because the reduction runs over positions.
+//              K codes enter QK as the fp16 values v = 1 + c * 2^-m (code in
+//              the mantissa below the 1.0 exponent; m = b for 2/4 bits, 10 for
+//              8 bits), so per quantisation group
+//                sum_d q_d c_d = 2^m (sum_d q_d v_d - sum_d q_d)
+//                q.k_hat = sum_g ( 2^m s_g * sum_g q v + (z_g - 2^m s_g) * sum_g q ).
+//              V codes become exact fp16 integers (1024 + c, minus 1024) and are
+//              dequantised per element in f16x2 (c*s + z, one rounding)
+//              because the PV reduction runs over positions.
 // Per unit piece the 4 warps' (m, l, o) are merged in shared memory and
 // written to the workspace slot (unit + chunk).
 #pragma once
@@ -30,14 +33,18 @@
 
 namespace kvq {
 
-constexpr int kConsumerWarps = 4;
+// 11 consumers + 1 producer = 12 warps, 3 per SM sub-partition (latency
+// hiding for the unpack chains); each sub-partition's 16K registers then
+// allow 168 registers per thread.
+constexpr int kConsumerWarps = 11;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
 constexpr uint32_t kF16Magic = 0x64006400u;    // two fp16 1024.0
+constexpr uint32_t kF16One = 0x3C003C00u;      // two fp16 1.0
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
@@ -147,24 +154,39 @@ __device__ __forceinline__ uint32_t bf16pair_f16(uint32_t lo_word, bool lo_hi, u
 
 // Four fp16 pairs (d0,d0+4), (d0+1,d0+5), (d0+2,d0+6), (d0+3,d0+7) of one
 // row's 8 elements starting at d0.  KB = bits (16 = bf16 row).
+// K code pair -> fp16 (v_lo, v_hi) with v = 1 + c * 2^-m: mask the code
+// into the mantissa under the exponent of 1.0.
+__device__ __forceinline__ uint32_t kcode_pair(uint32_t x, uint32_t mask) { return and_or(x, mask, kF16One); }
+
+// Four fp16 pairs (d0,d0+4), (d0+1,d0+5), (d0+2,d0+6), (d0+3,d0+7) of one
+// row's 8 elements starting at d0.  KB = bits (16 = bf16 row).  For packed
+// rows the pairs hold 1 + c * 2^-m (m = kKShift<KB>).
 template <int KB>
 __device__ __forceinline__ void k_row_pairs(const uint8_t* row, int P, int tig, uint32_t (&f)[4]) {
   if constexpr (KB == 4) {
+    // nibble k at bits 4k (and 16 + 4k) -> mantissa bits 6..9
     const uint32_t w = lds32(row + 4 * (4 * P + tig));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) f[k] = codes_f16(w >> (4 * k), 0x000F000Fu);
+    f[0] = kcode_pair(w << 6, 0x03C003C0u);
+    f[1] = kcode_pair(w << 2, 0x03C003C0u);
+    f[2] = kcode_pair(w >> 2, 0x03C003C0u);
+    f[3] = kcode_pair(w >> 6, 0x03C003C0u);
   } else if constexpr (KB == 2) {
+    // bytes of the lane's half-word split into the two halves, then
+    // crumb k at bits 2k (and 16 + 2k) -> mantissa bits 8..9
     const uint32_t w = lds32(row + 4 * (2 * P + (tig >> 1)));
     const uint32_t h = tig & 1;
     const uint32_t r = prmt(w, 0u, (2 * h) | (4u << 4) | ((2 * h + 1) << 8) | (4u << 12));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) f[k] = codes_f16(r >> (2 * k), 0x00030003u);
+    f[0] = kcode_pair(r << 8, 0x03000300u);
+    f[1] = kcode_pair(r << 6, 0x03000300u);
+    f[2] = kcode_pair(r << 4, 0x03000300u);
+    f[3] = kcode_pair(r << 2, 0x03000300u);
   } else if constexpr (KB == 8) {
+    // byte k of the two words -> mantissa bits 0..7
     const uint2 w = lds64(row + 4 * (8 * P + 2 * tig));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t x = prmt(w.x, w.y, k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-      f[k] = codes_f16(x, 0x00FF00FFu);
+      f[k] = kcode_pair(x, 0x00FF00FFu);
     }
   } else {  // bf16 row
     const uint4 r = lds128(row + 2 * (32 * P + 8 * tig));
@@ -174,6 +196,10 @@ __device__ __forceinline__ void k_row_pairs(const uint8_t* row, int P, int tig, 
     f[3] = bf16pair_f16(r.y, true, r.w, true);
   }
 }
+
+// 2^m of the K code placement above.
+template <int KB>
+__host__ __device__ constexpr float kKScale() { return KB == 4 ? 16.f : (KB == 2 ? 4.f : 1024.f); }
 
 // PV A operand (rows = d, K index = positions).  Lane gid owns
 // d in [16 gid, 16 gid + 16): m-tile mt row gid <-> d = 16 gid + mt,
@@ -253,14 +279,24 @@ __device__ __forceinline__ float f16hi(uint32_t w) {
 
 // One 16-position block [r0, r0 + 16) of a staged tile (n valid positions).
 // KB/VB: bit-widths of the K and V rows (16 = bf16 rows).
+// Per-layer constants of kblock (no divisions inside the block loop).
+struct KbConst {
+  int G;          // group size
+  int szrow;      // bytes of one scale/zero row: 4 * D / G
+  int vgoff;      // byte offset of the lane's V group in a scale/zero row: 4 * (16 gid / G)
+  float sl2;      // softmax scale * log2(e)
+};
+
 template <int KB, int VB>
 __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
-                                       const uint8_t* vsz, int r0, int n, int G, float sl2,
+                                       const uint8_t* vsz, int r0, int n, const KbConst& kcst,
                                        const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
                                        int tig, Acc& acc) {
   constexpr int KROW = KB * kD / 8;
   constexpr int VROW = VB * kD / 8;
-  const int szrow = 4 * (kD / G);
+  const int G = kcst.G;
+  const int szrow = kcst.szrow;
+  const float sl2 = kcst.sl2;
   const uint8_t* krow0 = kc + (r0 + gid) * KROW;
   const uint8_t* krow1 = kc + (r0 + gid + 8) * KROW;
 
@@ -289,8 +325,10 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
     auto apply = [&](const float (&Cg)[4], const float (&qg)[2], int g) {
       const uint32_t sz0 = lds32(ksz + (r0 + gid) * szrow + 4 * g);
       const uint32_t sz1 = lds32(ksz + (r0 + gid + 8) * szrow + 4 * g);
-      const float s0 = f16lo(sz0) * sl2, z0 = f16hi(sz0) * sl2;
-      const float s1 = f16lo(sz1) * sl2, z1 = f16hi(sz1) * sl2;
+      // sum q c = 2^m (sum q v - sum q): scale 2^m s on C, zero (z - 2^m s) on sum q
+      const float sc = kKScale<KB>() * sl2;
+      const float s0 = f16lo(sz0) * sc, s1 = f16lo(sz1) * sc;
+      const float z0 = fmaf(f16hi(sz0), sl2, -s0), z1 = fmaf(f16hi(sz1), sl2, -s1);
       S[0] = fmaf(s0, Cg[0], fmaf(z0, qg[0], S[0]));
       S[1] = fmaf(s0, Cg[1], fmaf(z0, qg[1], S[1]));
       S[2] = fmaf(s1, Cg[2], fmaf(z1, qg[0], S[2]));
@@ -328,9 +366,9 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   }
   const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
   const float b0s = mn0 == -INFINITY ? 0.f : mn0, b1s = mn1 == -INFINITY ? 0.f : mn1;
-  const float c0 = exp2f(acc.m[0] - b0s), c1 = exp2f(acc.m[1] - b1s);
-  const float P0 = exp2f(S[0] - b0s), P1 = exp2f(S[1] - b1s);
-  const float P2 = exp2f(S[2] - b0s), P3 = exp2f(S[3] - b1s);
+  const float c0 = ex2(acc.m[0] - b0s), c1 = ex2(acc.m[1] - b1s);
+  const float P0 = ex2(S[0] - b0s), P1 = ex2(S[1] - b1s);
+  const float P2 = ex2(S[2] - b0s), P3 = ex2(S[3] - b1s);
   acc.m[0] = mn0;
   acc.m[1] = mn1;
   acc.l[0] = fmaf(acc.l[0], c0, P0 + P2);
@@ -354,9 +392,9 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   v_load<VB>(vc, VROW, gid, t, v);
   uint32_t s2a = 0, z2a = 0, s2c = 0, z2c = 0;
   if constexpr (VB < 16) {
-    const int g = (16 * gid) / G;
-    const uint32_t sa = lds32(vsz + t[0] * szrow + 4 * g), sb = lds32(vsz + t[1] * szrow + 4 * g);
-    const uint32_t sc = lds32(vsz + t[2] * szrow + 4 * g), sd = lds32(vsz + t[3] * szrow + 4 * g);
+    const uint8_t* vg = vsz + kcst.vgoff;
+    const uint32_t sa = lds32(vg + t[0] * szrow), sb = lds32(vg + t[1] * szrow);
+    const uint32_t sc = lds32(vg + t[2] * szrow), sd = lds32(vg + t[3] * szrow);
     s2a = prmt(sa, sb, 0x5410u);
     z2a = prmt(sa, sb, 0x7632u);
     s2c = prmt(sc, sd, 0x5410u);
@@ -390,12 +428,18 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
 template <int KB, int VB>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
-  const int ctid = warp * 32 + lane;  // 0..127
+  const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
   const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
   const int ppg = p.G >> 5;
-  uint32_t it = 0;
+  KbConst kcst;
+  kcst.G = p.G;
+  kcst.szrow = 4 * (kD / p.G);
+  kcst.vgoff = 4 * ((16 * gid) / p.G);
+  kcst.sl2 = p.scale_log2;
+  uint32_t it = 0;    // tiles seen (stage ring position)
+  uint32_t gblk = 0;  // 16-position blocks dealt so far (round-robin over warps)
   for (int u = a.u; u <= u_last; ++u) {
     const int ps = (u == a.u) ? a.p : 0;
     const int pe = (u == e.u) ? e.p : p.plan.T;
@@ -453,13 +497,16 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
       const uint8_t* base = sm.stage[st];
-      for (int kb = warp; kb * 16 < n; kb += kConsumerWarps) {
+      const int nb = (n + 15) >> 4;
+      const int first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
+      gblk += nb;
+      for (int kb = first; kb < nb; kb += kConsumerWarps) {
         if (kind == kTilePacked)
           kblock<KB, VB>(base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16,
-                         n, p.G, p.scale_log2, qb, qsP, gid, tig, acc);
+                         n, kcst, qb, qsP, gid, tig, acc);
         else
-          kblock<16, 16>(base, nullptr, base + kBf16VOff, nullptr, kb * 16, n, p.G, p.scale_log2, qb,
-                         qsP, gid, tig, acc);
+          kblock<16, 16>(base, nullptr, base + kBf16VOff, nullptr, kb * 16, n, kcst, qb, qsP, gid, tig,
+                         acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
@@ -488,8 +535,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     }
     named_bar(1, kConsumerWarps * 32);
     const int64_t slot = static_cast<int64_t>(u) + c;
-    const int d = ctid;
-    for (int j = 0; j < nh; ++j) {
+    for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
+      const int j = idx / kD, d = idx - j * kD;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
@@ -514,7 +561,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(kSplitThreads, 2) split_mma_kernel(const __grid_constant__ Params p) {
+__global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

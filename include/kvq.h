@@ -187,6 +187,10 @@ kvq_status kvq_decode_attention_static_ws(const kvq_layout* L, const void* cache
                                           const void* q_bf16, int32_t T, float softmax_scale,
                                           void* out_bf16, float* lse, void* stream);
 
+/* The cudaError_t value (as int) of the last CUDA call that made an entry
+ * point return KVQ_ERR_CUDA on the calling host thread; 0 if none. */
+int kvq_last_cuda_error(void);
+
 /* Human-readable name of a status code (static string). */
 const char* kvq_status_string(kvq_status s);
 

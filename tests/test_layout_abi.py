@@ -20,7 +20,7 @@ def lib():
 
 def test_header_declares_what_library_exports(lib):
     text = open(HEADER).read()
-    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*)\s+(kvq_\w+)\s*\(", text, re.M))
+    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*|int)\s+(kvq_\w+)\s*\(", text, re.M))
     assert declared == set(kvq.EXPORTED_SYMBOLS)
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.lib_path()], capture_output=True,
                          text=True, check=True).stdout
