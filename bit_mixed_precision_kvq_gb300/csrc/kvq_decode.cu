@@ -22,10 +22,10 @@
 
 namespace kvq {
 
-const void* split_kernel_k2(int vb);
-const void* split_kernel_k4(int vb);
-const void* split_kernel_k8(int vb);
-const void* split_kernel_k16(int vb);
+const void* split_kernel_k2(int vb, int G);
+const void* split_kernel_k4(int vb, int G);
+const void* split_kernel_k8(int vb, int G);
+const void* split_kernel_k16(int vb, int G);
 
 constexpr int kCombineWarps = 16;
 
@@ -130,7 +130,7 @@ namespace {
 // Positions per packed tile and its sub-buffer offsets inside one stage.
 void packed_tile_geometry(kvq::Params* p) {
   const int w = p->krow + p->kszrow + p->vrow + p->vszrow;
-  int tt = ((kvq::kStageBytes - 4 * 128) / w) / 16 * 16;
+  int tt = ((kvq::kStageBytes - 4 * 128) / w) / 32 * 32;  // whole 32-position blocks
   if (tt > 512) tt = 512;
   auto r128 = [](int x) { return (x + 127) / 128 * 128; };
   p->tt_pk = tt;
@@ -139,12 +139,12 @@ void packed_tile_geometry(kvq::Params* p) {
   p->pk_off_vsz = p->pk_off_ksz + r128(tt * p->kszrow);
 }
 
-const void* split_kernel_for(int kb, int vb) {
+const void* split_kernel_for(int kb, int vb, int G) {
   switch (kb) {
-    case 2: return kvq::split_kernel_k2(vb);
-    case 4: return kvq::split_kernel_k4(vb);
-    case 8: return kvq::split_kernel_k8(vb);
-    case 16: return kvq::split_kernel_k16(vb);
+    case 2: return kvq::split_kernel_k2(vb, G);
+    case 4: return kvq::split_kernel_k4(vb, G);
+    case 8: return kvq::split_kernel_k8(vb, G);
+    case 16: return kvq::split_kernel_k16(vb, G);
   }
   return nullptr;
 }
@@ -169,7 +169,7 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   if (T < 1 || T > L->d.T_cap) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (ws_bytes < static_cast<size_t>(L->workspace_bytes)) return KVQ_ERR_CAPACITY;
-  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits);
+  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size);
   if (!split) return KVQ_ERR_UNSUPPORTED;
   int n_sm = 0;
   if (kvq_device_sm_count(&n_sm) != 0) return KVQ_ERR_CUDA;
@@ -193,10 +193,10 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
 
   // Opt each split kernel into >48 KB of dynamic shared memory, once.
   static std::mutex mu;
-  static bool smem_set[17][17] = {};
+  static bool smem_set[17][17][3] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
-    bool& done = smem_set[L->d.k_bits][L->d.v_bits];
+    bool& done = smem_set[L->d.k_bits][L->d.v_bits][L->d.group_size == 32 ? 0 : (L->d.group_size == 64 ? 1 : 2)];
     if (!done) {
       const cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(kSplitSmemBytes));

@@ -9,11 +9,12 @@
 //   producer : one lane walks the CTA's tiles and issues 1-D bulk async
 //              copies (TMA) of the tile's K/V rows (+ scale/zero rows) into a
 //              5-stage ring of 32 KB stages, signalled by mbarriers.
-//   consumers: the CTA's 16-position blocks are dealt round-robin to the 11
+//   consumers: the CTA's 32-position blocks are dealt round-robin to the 11
 //              warps across tile boundaries (every warp still waits for and
 //              releases every tile, which keeps the mbarrier phases exact).  QK and PV
 //              run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
-//              accumulate) with the unit's <= 8 query heads as N = 8:
+//              accumulate) with the unit's <= 8 query heads as N = 8; a block
+//              is two 16-row MMA halves sharing one softmax update:
 //                QK: S^T[t][j] = K[t][:] . q[j][:]    (M = 16 positions)
 //                PV: O^T[d][j] += V^T[d][t] P^T[t][j] (M = 16 of the D rows)
 //              K codes enter QK as the fp16 values v = 1 + c * 2^-m (code in
@@ -62,11 +63,12 @@ enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2 };
 // text suffix, each cut into tiles.  f(kind, t0, n).
 template <typename F>
 __device__ __forceinline__ void walk_piece(const Params& p, bool prot, int ps, int pe, F&& f) {
-  const int bounds[4] = {ps, max(ps, min(pe, p.vs)), max(ps, min(pe, p.ve)), pe};
-  for (int s = 0; s < 3; ++s) {
-    const int s0 = bounds[s], s1 = bounds[s + 1];
-    if (s0 >= s1) continue;
-    const int kind = s == 1 ? (prot ? kTileProt : kTilePacked) : kTileText;
+  const int b1 = max(ps, min(pe, p.vs)), b2 = max(ps, min(pe, p.ve));
+#pragma unroll 1
+  for (int seg = 0; seg < 3; ++seg) {  // selects, not an array: no local memory
+    const int s0 = seg == 0 ? ps : (seg == 1 ? b1 : b2);
+    const int s1 = seg == 0 ? b1 : (seg == 1 ? b2 : pe);
+    const int kind = seg == 1 ? (prot ? kTileProt : kTilePacked) : kTileText;
     const int tt = kind == kTilePacked ? p.tt_pk : kTileBf16;
     for (int t0 = s0; t0 < s1; t0 += tt) f(kind, t0, min(tt, s1 - t0));
   }
@@ -270,37 +272,23 @@ struct Acc {
   float o[8][4];
 };
 
-__device__ __forceinline__ float f16lo(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
-}
-__device__ __forceinline__ float f16hi(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+// Both halves of a half2 register as floats (the split is a register view).
+__device__ __forceinline__ void h2_to_f2(uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
 }
 
-// One 16-position block [r0, r0 + 16) of a staged tile (n valid positions).
-// KB/VB: bit-widths of the K and V rows (16 = bf16 rows).
-// Per-layer constants of kblock (no divisions inside the block loop).
-struct KbConst {
-  int G;          // group size
-  int szrow;      // bytes of one scale/zero row: 4 * D / G
-  int vgoff;      // byte offset of the lane's V group in a scale/zero row: 4 * (16 gid / G)
-  float sl2;      // softmax scale * log2(e)
-};
-
-template <int KB, int VB>
-__device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
-                                       const uint8_t* vsz, int r0, int n, const KbConst& kcst,
-                                       const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
-                                       int tig, Acc& acc) {
+// QK for one 16-row half [r0, r0 + 16) of a block: S[i] for rows
+// (gid, gid, gid+8, gid+8) x heads (2tig, 2tig+1, 2tig, 2tig+1), log2 units.
+template <int KB, int G>
+__device__ __forceinline__ void qk_half(const uint8_t* kc, const uint8_t* ksz, int r0, float sl2,
+                                        const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
+                                        int tig, float (&S)[4]) {
   constexpr int KROW = KB * kD / 8;
-  constexpr int VROW = VB * kD / 8;
-  const int G = kcst.G;
-  const int szrow = kcst.szrow;
-  const float sl2 = kcst.sl2;
+  constexpr int SZROW = 4 * (kD / G);
   const uint8_t* krow0 = kc + (r0 + gid) * KROW;
-  const uint8_t* krow1 = kc + (r0 + gid + 8) * KROW;
-
-  // ---- S^T = K q^T (scaled to log2 units) ----
+  const uint8_t* krow1 = krow0 + 8 * KROW;
   // One accumulator per k-step pair keeps the MMA dependency chains short.
   float C[4][4];
 #pragma unroll
@@ -314,87 +302,57 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
     mma_f16(C[P], A0, qb[2 * P][0], qb[2 * P][1]);
     mma_f16(C[P], A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
   }
-  float S[4];
   if constexpr (KB == 16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) S[i] = ((C[0][i] + C[1][i]) + (C[2][i] + C[3][i])) * sl2;
   } else {
-    // Sum the pairs of each quantisation group, then apply its scale/zero
-    // (qsP[P] already holds the q sum of the group that contains pair P).
-    S[0] = S[1] = S[2] = S[3] = 0.f;
-    auto apply = [&](const float (&Cg)[4], const float (&qg)[2], int g) {
-      const uint32_t sz0 = lds32(ksz + (r0 + gid) * szrow + 4 * g);
-      const uint32_t sz1 = lds32(ksz + (r0 + gid + 8) * szrow + 4 * g);
-      // sum q c = 2^m (sum q v - sum q): scale 2^m s on C, zero (z - 2^m s) on sum q
-      const float sc = kKScale<KB>() * sl2;
-      const float s0 = f16lo(sz0) * sc, s1 = f16lo(sz1) * sc;
-      const float z0 = fmaf(f16hi(sz0), sl2, -s0), z1 = fmaf(f16hi(sz1), sl2, -s1);
-      S[0] = fmaf(s0, Cg[0], fmaf(z0, qg[0], S[0]));
-      S[1] = fmaf(s0, Cg[1], fmaf(z0, qg[1], S[1]));
-      S[2] = fmaf(s1, Cg[2], fmaf(z1, qg[0], S[2]));
-      S[3] = fmaf(s1, Cg[3], fmaf(z1, qg[1], S[3]));
-    };
-    if (G == 32) {
-      apply(C[0], qsP[0], 0);
-      apply(C[1], qsP[1], 1);
-      apply(C[2], qsP[2], 2);
-      apply(C[3], qsP[3], 3);
-    } else if (G == 64) {
+    // Sum the pairs of each quantisation group, then apply its scale/zero:
+    // sum q c = 2^m (sum q v - sum q), so 2^m s multiplies the group's sum
+    // and (z - 2^m s) multiplies the group's q sum (qsP[P] for any pair P of it).
+    constexpr int PPG = G / 32;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        C[0][i] += C[1][i];
-        C[2][i] += C[3][i];
+    for (int P = 0; P < 4; ++P) {
+      if (P % PPG != 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) C[P - P % PPG][i] += C[P][i];
       }
-      apply(C[0], qsP[0], 0);
-      apply(C[2], qsP[2], 1);
-    } else {
+    }
+    const uint8_t* sz0p = ksz + (r0 + gid) * SZROW;
+    const uint8_t* sz1p = sz0p + 8 * SZROW;
+    const float sc = kKScale<KB>() * sl2;
+    S[0] = S[1] = S[2] = S[3] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) C[0][i] = (C[0][i] + C[1][i]) + (C[2][i] + C[3][i]);
-      apply(C[0], qsP[0], 0);
+    for (int g = 0; g < 4 / PPG; ++g) {
+      const int P = g * PPG;
+      float s0, z0, s1, z1;
+      h2_to_f2(lds32(sz0p + 4 * g), s0, z0);
+      h2_to_f2(lds32(sz1p + 4 * g), s1, z1);
+      s0 *= sc;
+      s1 *= sc;
+      z0 = fmaf(z0, sl2, -s0);
+      z1 = fmaf(z1, sl2, -s1);
+      S[0] = fmaf(s0, C[P][0], fmaf(z0, qsP[P][0], S[0]));
+      S[1] = fmaf(s0, C[P][1], fmaf(z0, qsP[P][1], S[1]));
+      S[2] = fmaf(s1, C[P][2], fmaf(z1, qsP[P][0], S[2]));
+      S[3] = fmaf(s1, C[P][3], fmaf(z1, qsP[P][1], S[3]));
     }
   }
-  const bool ok0 = r0 + gid < n, ok1 = r0 + gid + 8 < n;
-  if (!ok0) S[0] = S[1] = -INFINITY;
-  if (!ok1) S[2] = S[3] = -INFINITY;
+}
 
-  // ---- online softmax (columns = query heads 2tig, 2tig+1) ----
-  float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-  }
-  const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
-  const float b0s = mn0 == -INFINITY ? 0.f : mn0, b1s = mn1 == -INFINITY ? 0.f : mn1;
-  const float c0 = ex2(acc.m[0] - b0s), c1 = ex2(acc.m[1] - b1s);
-  const float P0 = ex2(S[0] - b0s), P1 = ex2(S[1] - b1s);
-  const float P2 = ex2(S[2] - b0s), P3 = ex2(S[3] - b1s);
-  acc.m[0] = mn0;
-  acc.m[1] = mn1;
-  acc.l[0] = fmaf(acc.l[0], c0, P0 + P2);
-  acc.l[1] = fmaf(acc.l[1], c1, P1 + P3);
-  if (!__all_sync(0xffffffffu, c0 == 1.f && c1 == 1.f)) {  // some running max moved
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc.o[mt][0] *= c0;
-      acc.o[mt][1] *= c1;
-      acc.o[mt][2] *= c0;
-      acc.o[mt][3] *= c1;
-    }
-  }
-  // P^T as the B operand of PV: transpose the two 8x8 halves.
-  const uint32_t pb0 = movmatrix_trans(pack_f16x2(P0, P1));
-  const uint32_t pb1 = movmatrix_trans(pack_f16x2(P2, P3));
-
-  // ---- O^T += V^T P^T ----
+// PV for one 16-row half: O^T += V^T P^T with the half's P^T fragments.
+template <int VB, int G>
+__device__ __forceinline__ void pv_half(const uint8_t* vc, const uint8_t* vsz, int r0, int n,
+                                        uint32_t pb0, uint32_t pb1, int gid, int tig, Acc& acc) {
+  constexpr int VROW = VB * kD / 8;
+  constexpr int SZROW = 4 * (kD / G);
   const int t[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
   VData<VB> v;
   v_load<VB>(vc, VROW, gid, t, v);
   uint32_t s2a = 0, z2a = 0, s2c = 0, z2c = 0;
   if constexpr (VB < 16) {
-    const uint8_t* vg = vsz + kcst.vgoff;
-    const uint32_t sa = lds32(vg + t[0] * szrow), sb = lds32(vg + t[1] * szrow);
-    const uint32_t sc = lds32(vg + t[2] * szrow), sd = lds32(vg + t[3] * szrow);
+    const uint8_t* vg = vsz + 4 * ((16 * gid) / G) + r0 * SZROW + 2 * tig * SZROW;
+    const uint32_t sa = lds32(vg), sb = lds32(vg + SZROW);
+    const uint32_t sc = lds32(vg + 8 * SZROW), sd = lds32(vg + 9 * SZROW);
     s2a = prmt(sa, sb, 0x5410u);
     z2a = prmt(sa, sb, 0x7632u);
     s2c = prmt(sc, sd, 0x5410u);
@@ -403,8 +361,11 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   // Rows past n hold stale shared memory (possibly NaN/Inf patterns): zero
   // their V operands so that 0 * garbage cannot reach the accumulators.
   const bool ragged = r0 + 16 > n;
-  const uint32_t ma = (t[0] < n ? 0x0000ffffu : 0u) | (t[1] < n ? 0xffff0000u : 0u);
-  const uint32_t mc = (t[2] < n ? 0x0000ffffu : 0u) | (t[3] < n ? 0xffff0000u : 0u);
+  uint32_t ma = 0xffffffffu, mc = 0xffffffffu;
+  if (ragged) {
+    ma = (t[0] < n ? 0x0000ffffu : 0u) | (t[1] < n ? 0xffff0000u : 0u);
+    mc = (t[2] < n ? 0x0000ffffu : 0u) | (t[3] < n ? 0xffff0000u : 0u);
+  }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t A[4] = {v_pair<VB>(v, 0, 1, mt), v_pair<VB>(v, 0, 1, 8 + mt), v_pair<VB>(v, 2, 3, mt),
@@ -425,21 +386,83 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
   }
 }
 
-template <int KB, int VB>
+// One 32-position block [r0, r0 + 32) of a staged tile (n valid positions):
+// two 16-row MMA halves sharing one online-softmax update.
+template <int KB, int VB, int G>
+__device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
+                                         const uint8_t* vsz, int r0, int n, float sl2,
+                                         const uint32_t (&qb)[8][2], const float (&qsP)[4][2],
+                                         int gid, int tig, Acc& acc) {
+  const bool two = r0 + 16 < n;  // the second half holds valid positions
+  float S[2][4];
+  qk_half<KB, G>(kc, ksz, r0, sl2, qb, qsP, gid, tig, S[0]);
+  if (two) {
+    qk_half<KB, G>(kc, ksz, r0 + 16, sl2, qb, qsP, gid, tig, S[1]);
+  } else {
+    S[1][0] = S[1][1] = S[1][2] = S[1][3] = -INFINITY;
+  }
+  if (r0 + 32 > n) {  // ragged block: mask rows past n
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (r0 + 16 * h + gid >= n) S[h][0] = S[h][1] = -INFINITY;
+      if (r0 + 16 * h + gid + 8 >= n) S[h][2] = S[h][3] = -INFINITY;
+    }
+  }
+
+  // ---- online softmax over the 32 positions (columns = heads 2tig, 2tig+1) ----
+  float mx0 = fmaxf(fmaxf(S[0][0], S[0][2]), fmaxf(S[1][0], S[1][2]));
+  float mx1 = fmaxf(fmaxf(S[0][1], S[0][3]), fmaxf(S[1][1], S[1][3]));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
+  const float b0s = mn0 == -INFINITY ? 0.f : mn0, b1s = mn1 == -INFINITY ? 0.f : mn1;
+  const float c0 = ex2(acc.m[0] - b0s), c1 = ex2(acc.m[1] - b1s);
+  float P[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    P[h][0] = ex2(S[h][0] - b0s);
+    P[h][1] = ex2(S[h][1] - b1s);
+    P[h][2] = ex2(S[h][2] - b0s);
+    P[h][3] = ex2(S[h][3] - b1s);
+  }
+  acc.m[0] = mn0;
+  acc.m[1] = mn1;
+  acc.l[0] = fmaf(acc.l[0], c0, (P[0][0] + P[0][2]) + (P[1][0] + P[1][2]));
+  acc.l[1] = fmaf(acc.l[1], c1, (P[0][1] + P[0][3]) + (P[1][1] + P[1][3]));
+  if (!__all_sync(0xffffffffu, c0 == 1.f && c1 == 1.f)) {  // some running max moved
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc.o[mt][0] *= c0;
+      acc.o[mt][1] *= c1;
+      acc.o[mt][2] *= c0;
+      acc.o[mt][3] *= c1;
+    }
+  }
+  // P^T as the B operand of PV: transpose the 8x8 quarters.
+  const uint32_t pa0 = movmatrix_trans(pack_f16x2(P[0][0], P[0][1]));
+  const uint32_t pa1 = movmatrix_trans(pack_f16x2(P[0][2], P[0][3]));
+  pv_half<VB, G>(vc, vsz, r0, n, pa0, pa1, gid, tig, acc);
+  if (two) {
+    const uint32_t pc0 = movmatrix_trans(pack_f16x2(P[1][0], P[1][1]));
+    const uint32_t pc1 = movmatrix_trans(pack_f16x2(P[1][2], P[1][3]));
+    pv_half<VB, G>(vc, vsz, r0 + 16, n, pc0, pc1, gid, tig, acc);
+  }
+}
+
+template <int KB, int VB, int G>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
   const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
-  const int ppg = p.G >> 5;
-  KbConst kcst;
-  kcst.G = p.G;
-  kcst.szrow = 4 * (kD / p.G);
-  kcst.vgoff = 4 * ((16 * gid) / p.G);
-  kcst.sl2 = p.scale_log2;
+  constexpr int ppg = G / 32;
+  const float sl2 = p.scale_log2;
   uint32_t it = 0;    // tiles seen (stage ring position)
-  uint32_t gblk = 0;  // 16-position blocks dealt so far (round-robin over warps)
+  uint32_t gblk = 0;  // 32-position blocks dealt so far (round-robin over warps)
   for (int u = a.u; u <= u_last; ++u) {
     const int ps = (u == a.u) ? a.p : 0;
     const int pe = (u == e.u) ? e.p : p.plan.T;
@@ -497,16 +520,16 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
       const uint8_t* base = sm.stage[st];
-      const int nb = (n + 15) >> 4;
+      const int nb = (n + 31) >> 5;
       const int first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
       gblk += nb;
       for (int kb = first; kb < nb; kb += kConsumerWarps) {
         if (kind == kTilePacked)
-          kblock<KB, VB>(base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16,
-                         n, kcst, qb, qsP, gid, tig, acc);
+          kblock32<KB, VB, G>(base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz,
+                              kb * 32, n, sl2, qb, qsP, gid, tig, acc);
         else
-          kblock<16, 16>(base, nullptr, base + kBf16VOff, nullptr, kb * 16, n, kcst, qb, qsP, gid, tig,
-                         acc);
+          kblock32<16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2, qb, qsP, gid,
+                              tig, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[st]);
@@ -560,7 +583,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   }
 }
 
-template <int KB, int VB>
+template <int KB, int VB, int G>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -581,7 +604,7 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
     if (lane == 0) producer_loop(p, sm, blockIdx.x);
     return;
   }
-  consumer_loop<KB, VB>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq

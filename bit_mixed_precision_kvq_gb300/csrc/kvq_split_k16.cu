@@ -1,14 +1,27 @@
-// Instantiations of the split-KV kernel for K bit-width 16 (all V widths);
-// one translation unit per K width so that they compile in parallel.
+// Instantiations of the split-KV kernel for K bit-width 16 (all V widths and
+// group sizes); one translation unit per K width so that they compile in
+// parallel.
 #include "kvq_split.cuh"
 
 namespace kvq {
-const void* split_kernel_k16(int vb) {
+namespace {
+template <int VB>
+const void* by_group(int G) {
+  switch (G) {
+    case 32: return reinterpret_cast<const void*>(&split_mma_kernel<16, VB, 32>);
+    case 64: return reinterpret_cast<const void*>(&split_mma_kernel<16, VB, 64>);
+    case 128: return reinterpret_cast<const void*>(&split_mma_kernel<16, VB, 128>);
+  }
+  return nullptr;
+}
+}  // namespace
+
+const void* split_kernel_k16(int vb, int G) {
   switch (vb) {
-    case 2: return reinterpret_cast<const void*>(&split_mma_kernel<16, 2>);
-    case 4: return reinterpret_cast<const void*>(&split_mma_kernel<16, 4>);
-    case 8: return reinterpret_cast<const void*>(&split_mma_kernel<16, 8>);
-    case 16: return reinterpret_cast<const void*>(&split_mma_kernel<16, 16>);
+    case 2: return by_group<2>(G);
+    case 4: return by_group<4>(G);
+    case 8: return by_group<8>(G);
+    case 16: return by_group<16>(G);
   }
   return nullptr;
 }
