@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--T", type=int, default=None, help="history length for the longctx workload")
     ap.add_argument("--layers", type=int, default=None, help="limit layers (parity/debug only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-in-step", choices=["auto", "yes", "no"], default="auto",
+                    help="include kvq_quantize_append of the whole bf16 history in every step "
+                         "(auto: yes for llava_next_13b, whose step includes the prefill)")
     return ap.parse_args()
 
 
@@ -179,6 +182,19 @@ def append_bytes(L, n_tok: int) -> int:
     return 2 * (d.B * d.H_kv * n_tok * 2 * 2 * d.D)
 
 
+def prefill_bytes(L, T: int) -> int:
+    """Quantise-append of positions [0, T): read the bf16 K and V rows, write
+    their cache rows (packed codes + scale/zero for visual rows of packed
+    heads, bf16 otherwise)."""
+    d = L.d
+    n_vis = min(d.vis_end, T) - min(d.vis_start, T)
+    n_txt = T - n_vis
+    read = 2 * d.B * d.H_kv * T * 2 * d.D
+    packed = sum(int(L.row_bytes[s]) for s in range(4))
+    write = d.B * (d.H_kv * n_txt * 4 * d.D + L.n_prot * n_vis * 4 * d.D + L.n_packed * n_vis * packed)
+    return read + write
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -186,12 +202,13 @@ def append_bytes(L, n_tok: int) -> int:
 class Model:
     """Per-layer caches (history quantised once), per-step inputs, outputs."""
 
-    def __init__(self, w: synth.Workload, dev, n_layers: int):
+    def __init__(self, w: synth.Workload, dev, n_layers: int, prefill_in_step: bool = False):
         import bit_mixed_precision_kvq_gb300 as kvq
         self.kvq = kvq
         self.w = w
         self.T_hist = w.T
         self.T = w.T + 1
+        self.prefill_in_step = prefill_in_step
         self.layers = []
         ws_bytes = 0
         for l in range(n_layers):
@@ -202,8 +219,12 @@ class Model:
             k = synth.make_kv(w, l, "k", dev)
             v = synth.make_kv(w, l, "v", dev)
             kvq.quantize_append(L, cache, k, v, 0)
-            del k, v
-            self.layers.append(dict(L=L, cache=cache))
+            layer = dict(L=L, cache=cache)
+            if prefill_in_step:  # the bf16 history stays resident as the step's input
+                layer["k"], layer["v"] = k, v
+            else:
+                del k, v
+            self.layers.append(layer)
             ws_bytes = max(ws_bytes, int(L.workspace_bytes))
         self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         nL = n_layers
@@ -220,6 +241,8 @@ class Model:
         kvq = self.kvq
         for l, ly in enumerate(self.layers):
             L = ly["L"]
+            if self.prefill_in_step:
+                kvq.quantize_append(L, ly["cache"], ly["k"], ly["v"], 0)
             kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
             kvq.decode_attention(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
                                  self.ws)
@@ -229,8 +252,15 @@ class Model:
         self.kvq.decode_attention(ly["L"], ly["cache"], self.q[l], self.T, self.out[l],
                                   self.scale, None, self.ws)
 
+    def prefill_layer(self, l: int):
+        ly = self.layers[l]
+        self.kvq.quantize_append(ly["L"], ly["cache"], ly["k"], ly["v"], 0)
+
     def step_bytes(self) -> int:
-        return sum(decode_bytes(ly["L"], self.T) + append_bytes(ly["L"], 1) for ly in self.layers)
+        b = sum(decode_bytes(ly["L"], self.T) + append_bytes(ly["L"], 1) for ly in self.layers)
+        if self.prefill_in_step:
+            b += sum(prefill_bytes(ly["L"], self.T_hist) for ly in self.layers)
+        return b
 
 
 def run_ours(args, rank, world, local):
@@ -239,7 +269,9 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     w = synth.workload(args.workload, args.T)
     n_layers = args.layers or w.n_layers
-    model = Model(w, dev, n_layers)
+    prefill = (args.prefill_in_step == "yes" or
+               (args.prefill_in_step == "auto" and args.workload == "llava_next_13b"))
+    model = Model(w, dev, n_layers, prefill_in_step=prefill)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -254,7 +286,7 @@ def run_ours(args, rank, world, local):
     with torch.cuda.graph(graph):
         model.step()
     torch.cuda.synchronize()
-    launches_per_step = 3 * n_layers  # append + split + combine per layer
+    launches_per_step = (4 if prefill else 3) * n_layers  # [prefill] + append + split + combine
 
     for _ in range(max(3, args.warmup)):
         flush()
@@ -303,6 +335,26 @@ def run_ours(args, rank, world, local):
         pass
     peak = float(peaks.get("hbm_gbs", 6800.0))
     achieved = layer_bytes / (launch_ms * 1e-3) / 1e9
+
+    append_line = None
+    if prefill:
+        ap_ev = []
+        for r in range(3):
+            for l in range(n_layers):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                model.prefill_layer(l)
+                b.record()
+                ap_ev.append((a, b))
+        torch.cuda.synchronize()
+        ap_ms = float(np.mean([a.elapsed_time(b) for a, b in ap_ev]))
+        ap_bytes = float(np.mean([prefill_bytes(ly["L"], model.T_hist) for ly in model.layers]))
+        ap_gbs = ap_bytes / (ap_ms * 1e-3) / 1e9
+        append_line = {"kernel": "append_kernel (kvq_quantize_append of the bf16 history)",
+                       "per_launch_us": round(ap_ms * 1e3, 2), "per_launch_bytes": int(ap_bytes),
+                       "achieved": round(ap_gbs, 1), "peak": peak, "unit": "GB/s",
+                       "frac": round(ap_gbs / peak, 4)}
 
     # e2e: pinned host buffers in, outputs back, all inside the timed region
     h_q = torch.empty(model.q.shape, dtype=model.q.dtype, pin_memory=True)
@@ -358,6 +410,9 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if append_line is not None:
+        line["append"] = append_line
+        line["config"]["step"] = "per layer: quantise-append of the bf16 history + current token, decode"
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:

@@ -6,9 +6,10 @@
 // quantised (intro checklist).  HeadGuard brief, key ideas: protected KV
 // heads keep their visual K and V in bf16.
 //
-// One warp per (b, h, position); lane l owns elements 4l..4l+3 of the
-// D = 128 row (one 8-byte load).  A quantisation group of G elements spans
-// G/4 lanes, reduced with xor-shuffles.  The arithmetic is the fp32 spec the
+// One warp per (b, h, 8 consecutive positions): 4 lanes per D = 128 row,
+// each lane owning 32 consecutive elements (a whole group for G = 32; for
+// G = 64 / 128 the 2 / 4 lanes of a group combine min and max with
+// shuffles).  The arithmetic is the fp32 spec the
 // oracle restates: r = max - min (RN), s = fp16(r / (2^b - 1)) (IEEE div),
 // z = fp16(min + 0), code = clamp(rint((x - z) / s), 0, 2^b - 1) using the
 // stored s and z, code 0 if s == 0.  Intrinsics pin every rounding so that
@@ -21,54 +22,6 @@
 namespace kvq {
 namespace {
 
-__device__ __forceinline__ void quantize_store(const Params& p, uint8_t* codes_row, uint8_t* sz_row,
-                                               int bits, const float x[4], int lane) {
-  const int lanes_per_group = p.G >> 2;  // 8, 16 or 32
-  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  for (int off = 1; off < lanes_per_group; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
-  mn = __fadd_rn(mn, 0.0f);  // -0 -> +0: signed zeros compare equal
-  const float qmax = static_cast<float>((1 << bits) - 1);
-  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-  const __half sh = __float2half_rn(s32);
-  const __half zh = __float2half_rn(mn);
-  const float sf = __half2float(sh);
-  const float zf = __half2float(zh);
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float r = 0.0f;
-    if (sf != 0.0f) {
-      r = rintf(__fdiv_rn(__fsub_rn(x[i], zf), sf));
-      r = fminf(fmaxf(r, 0.0f), qmax);
-    }
-    c[i] = static_cast<uint32_t>(r);
-  }
-  uint32_t* words = reinterpret_cast<uint32_t*>(codes_row);
-  if (bits == 8) {
-    words[lane] = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-  } else if (bits == 4) {
-    const uint32_t mine = c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12);
-    const uint32_t next = __shfl_down_sync(0xffffffffu, mine, 1);
-    if ((lane & 1) == 0) words[lane >> 1] = mine | (next << 16);
-  } else {  // bits == 2
-    const uint32_t mine = c[0] | (c[1] << 2) | (c[2] << 4) | (c[3] << 6);
-    const uint32_t n1 = __shfl_down_sync(0xffffffffu, mine, 1);
-    const uint32_t n2 = __shfl_down_sync(0xffffffffu, mine, 2);
-    const uint32_t n3 = __shfl_down_sync(0xffffffffu, mine, 3);
-    if ((lane & 3) == 0) words[lane >> 2] = mine | (n1 << 8) | (n2 << 16) | (n3 << 24);
-  }
-  if ((lane & (lanes_per_group - 1)) == 0) {
-    __half2 sz;
-    sz.x = sh;
-    sz.y = zh;
-    reinterpret_cast<__half2*>(sz_row)[(4 * lane) / p.G] = sz;
-  }
-}
-
 struct AppendArgs {
   Params p;
   const uint16_t* kin;
@@ -77,31 +30,139 @@ struct AppendArgs {
   int32_t t0, n_tok;
 };
 
+constexpr int kLaneElems = 32;                      // consecutive elements of a row per lane
+constexpr int kLanesPerRow = kD / kLaneElems;       // 4
+constexpr int kRowsPerWarp = 32 / kLanesPerRow;     // 8
+
+// The correctly rounded quotient, kept out of line: it is needed only for
+// near-ties.
+__device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
+
+__device__ __forceinline__ float bf16x2_min_lohi(uint32_t w) {
+  return fminf(bf16_lo(w), bf16_hi(w));
+}
+
+// Quantise and store the lane's 32 elements (16 bf16 pairs in w[]) of one
+// row.  `gmask` = the 4 lanes of this row (shuffle partners for G > 32).
+template <int BITS>
+__device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, int part, uint32_t gmask,
+                                              uint8_t* codes_row, uint8_t* sz_row) {
+  // group min / max over the lane's elements (packed bf16 pairs), then over
+  // the lanes of the group
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
+  __nv_bfloat162 mx2 = mn2;
+#pragma unroll
+  for (int i = 1; i < 16; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    mn2 = __hmin2(mn2, v);
+    mx2 = __hmax2(mx2, v);
+  }
+  float mn = fminf(__low2float(mn2), __high2float(mn2));
+  float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+  for (int off = 1; off < G / kLaneElems; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(gmask, mn, off, kLanesPerRow));
+    mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, off, kLanesPerRow));
+  }
+  mn = __fadd_rn(mn, 0.0f);  // -0 -> +0: signed zeros compare equal
+  constexpr uint32_t cmax = (1u << BITS) - 1u;
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(cmax));
+  const __half sh = __float2half_rn(s32);
+  const __half zh = __float2half_rn(mn);
+  const float sf = __half2float(sh);
+  const float zf = __half2float(zh);
+  // Store the group's (s, z) once (first lane of the group).
+  if ((part & (G / kLaneElems - 1)) == 0) {
+    __half2 sz;
+    sz.x = sh;
+    sz.y = zh;
+    reinterpret_cast<__half2*>(sz_row)[(part * kLaneElems) / G] = sz;
+  }
+  // code = clamp(rint(fl(fl(x - z) / s))).  The quotient is first formed as
+  // fl(d * fl(1/s)), within 3 * 2^-24 |u| of the correctly rounded one; rint
+  // is constant between half-integers, so both give the same code unless the
+  // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
+  // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
+  // it; only then is the IEEE division evaluated (out of line, rare).
+  constexpr int kWordsPerLane = BITS;  // 32 codes * BITS bits / 32
+  uint32_t words[kWordsPerLane];
+#pragma unroll
+  for (int i = 0; i < kWordsPerLane; ++i) words[i] = 0u;
+  if (sf != 0.0f) {
+    const float rs = __frcp_rn(sf);
+    const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {  // 8 elements at a time
+      float d[8], u[8];
+      uint32_t need = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t pw = w[c8 * 4 + (k >> 1)];
+        const float x = (k & 1) ? bf16_hi(pw) : bf16_lo(pw);
+        d[k] = __fsub_rn(x, zf);
+        u[k] = __fmul_rn(d[k], rs);
+        const float fr = __fsub_rn(__fsub_rn(u[k], floorf(u[k])), 0.5f);  // exact for |u| < 2^23
+        if (fabsf(fr) <= win) need |= 1u << k;
+      }
+      if (__any_sync(gmask, need != 0)) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (need & (1u << k)) u[k] = exact_quotient(d[k], sf);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t code = min(__float2uint_rn(u[k]), cmax);  // round half to even; < 0 -> 0
+        const int e = c8 * 8 + k;                                 // element within the lane
+        words[(e * BITS) >> 5] |= code << ((e * BITS) & 31);
+      }
+    }
+  }
+  // Codes of the lane's 32 elements: BITS words at byte offset part * 4 * BITS.
+  uint8_t* dst = codes_row + part * 4 * BITS;
+  if constexpr (BITS == 2) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+  } else if constexpr (BITS == 4) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(words[4], words[5], words[6], words[7]);
+  }
+}
+
+// One warp per (b, h, 8 consecutive positions); 4 lanes per row, each lane
+// 32 consecutive elements (four 16-byte loads of K and of V, all in flight
+// before any use).
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
   pdl_wait();  // the previous kernel in the stream may still read the cache
   pdl_launch_dependents();
   const Params& p = a.p;
-  const uint16_t* __restrict__ kin = a.kin;
-  const uint16_t* __restrict__ vin = a.vin;
-  const int64_t sb = a.sb, sh = a.sh, st = a.st;
-  const int32_t t0 = a.t0, n_tok = a.n_tok;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nrows = static_cast<int64_t>(p.B) * p.Hkv * n_tok;
-  if (wid >= nrows) return;
-  const int32_t i = static_cast<int32_t>(wid % n_tok);
-  const int64_t bh = wid / n_tok;
+  const int32_t n_chunks = (a.n_tok + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int64_t nwarps = static_cast<int64_t>(p.B) * p.Hkv * n_chunks;
+  if (wid >= nwarps) return;
+  const int rr = lane / kLanesPerRow, part = lane % kLanesPerRow;
+  const uint32_t gmask = 0xfu << (kLanesPerRow * rr);
+  const int32_t i = static_cast<int32_t>(wid % n_chunks) * kRowsPerWarp + rr;
+  if (i >= a.n_tok) return;  // whole 4-lane row groups leave together
+  const int64_t bh = wid / n_chunks;
   const int32_t h = static_cast<int32_t>(bh % p.Hkv);
   const int32_t b = static_cast<int32_t>(bh / p.Hkv);
-  const int32_t t = t0 + i;
-  const int64_t src = b * sb + h * sh + i * st + 4 * lane;
+  const int32_t t = a.t0 + i;
   const bool visual = t >= p.vs && t < p.ve;
   const bool prot = p.prot[h] != 0;
 
+  const int64_t src = b * a.sb + h * a.sh + i * a.st + part * kLaneElems;
+  uint32_t kw[16], vw[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.kin + src) + q);
+    const uint4 y = __ldg(reinterpret_cast<const uint4*>(a.vin + src) + q);
+    kw[4 * q] = x.x; kw[4 * q + 1] = x.y; kw[4 * q + 2] = x.z; kw[4 * q + 3] = x.w;
+    vw[4 * q] = y.x; vw[4 * q + 1] = y.y; vw[4 * q + 2] = y.z; vw[4 * q + 3] = y.w;
+  }
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
-    const uint16_t* in = which ? vin : kin;
-    const uint2 raw = *reinterpret_cast<const uint2*>(in + src);
+    const uint32_t (&w)[16] = which ? vw : kw;
     uint8_t* dst;
     if (!visual) {
       const int64_t tr = t < p.vs ? t : t - p.Tv;
@@ -118,13 +179,16 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
       if (bits < 16) {
         uint8_t* sz = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_V_SZ : KVQ_SEG_K_SZ]) +
                       row * (which ? p.vszrow : p.kszrow);
-        const float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-        quantize_store(p, codes, sz, bits, x, lane);
+        if (bits == 2) quantize_lane<2>(w, p.G, part, gmask, codes, sz);
+        else if (bits == 4) quantize_lane<4>(w, p.G, part, gmask, codes, sz);
+        else quantize_lane<8>(w, p.G, part, gmask, codes, sz);
         continue;
       }
       dst = codes;
     }
-    *reinterpret_cast<uint2*>(dst + 8 * lane) = raw;
+    uint4* o = reinterpret_cast<uint4*>(dst + part * kLaneElems * 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   }
 }
 
@@ -139,9 +203,9 @@ extern "C" kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, cons
   if (st != KVQ_OK) return st;
   if (!cache || !k_bf16 || !v_bf16) return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(cache) % 256 != 0) return KVQ_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(k_bf16) % 8 != 0 || reinterpret_cast<uintptr_t>(v_bf16) % 8 != 0)
+  if (reinterpret_cast<uintptr_t>(k_bf16) % 16 != 0 || reinterpret_cast<uintptr_t>(v_bf16) % 16 != 0)
     return KVQ_ERR_INVALID_ARG;
-  if (stride_b < 0 || stride_h < 0 || stride_t < 0 || stride_b % 4 || stride_h % 4 || stride_t % 4)
+  if (stride_b < 0 || stride_h < 0 || stride_t < 0 || stride_b % 8 || stride_h % 8 || stride_t % 8)
     return KVQ_ERR_INVALID_ARG;
   if (t0 < 0 || n_tok < 0) return KVQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(t0) + n_tok > L->d.T_cap) return KVQ_ERR_CAPACITY;
@@ -150,8 +214,9 @@ extern "C" kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, cons
   kvq_fill_params(L, &p);
   uint8_t* base = static_cast<uint8_t*>(cache);
   for (int s = 0; s < KVQ_NSEG; ++s) p.seg[s] = base + L->off[s];
-  const int64_t rows = static_cast<int64_t>(L->d.B) * L->d.H_kv * n_tok;
-  const int64_t blocks = (rows + 7) / 8;
+  const int64_t warps = static_cast<int64_t>(L->d.B) * L->d.H_kv *
+                       ((n_tok + kvq::kRowsPerWarp - 1) / kvq::kRowsPerWarp);
+  const int64_t blocks = (warps + 7) / 8;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
   kvq::AppendArgs a;
   a.p = p;

@@ -127,7 +127,8 @@ kvq_status kvq_cache_layout(const kvq_layout_desc* desc, kvq_layout* out);
  *   cache    device buffer of L->total_bytes, 256-byte aligned
  *   k_bf16, v_bf16   device bf16 tensors [B][H_kv][n_tok][D]; element
  *            (b, h, i, d) at index b*stride_b + h*stride_h + i*stride_t + d
- *            (strides in elements; d contiguous; 8-byte aligned rows)
+ *            (strides in elements, multiples of 8; d contiguous; tensors
+ *            16-byte aligned)
  *   t0, n_tok  first position and count; n_tok == 0 is a no-op
  * A position in [vis_start, vis_end) of an unprotected head is quantised
  * (bits < 16) and packed; every other position is copied bf16 verbatim.

@@ -245,3 +245,32 @@ def test_quantiser_edge_rows(cuda_dev, kvq):
     append(L, cache, k, v, 0)
     torch.cuda.synchronize()
     check_append(L, c, cache, bits(k), bits(v), 64)
+
+
+def test_quantiser_ties_and_near_ties(cuda_dev, kvq):
+    """Values whose quotient (x - z) / s is exactly k + 1/2 (ties, rounded
+    half to even) or one bf16 step beside it: the codes must match the
+    correctly rounded definition bit for bit."""
+    c = Case(1, 4, 2, 64, 0, 64, 4, 2, 32, [])
+    rows = []
+    rng = np.random.default_rng(17)
+    for r in range(64):
+        g = np.zeros(128, np.float32)
+        for grp in range(4):
+            base = grp * 32
+            # INT4 (K): min 0, max 15/16 -> s = 1/16; ties at (k + 1/2)/16
+            vals = np.array([(k + 0.5) / 16 for k in range(15)] * 2 + [0.0, 15 / 16], np.float32)
+            if r % 3 == 1:  # one bf16 step up from each tie
+                vals[:30] = np.nextafter(torch.tensor(vals[:30]).to(torch.bfloat16).float().numpy(),
+                                         np.float32(2.0))
+            vals = vals * np.float32(2.0) ** int(rng.integers(-6, 6))
+            g[base:base + 32] = vals
+        rows.append(g)
+    x = np.stack(rows).reshape(1, 1, 64, 128)
+    k = torch.tensor(np.concatenate([x, x[:, :, ::-1]], axis=1)).to(torch.bfloat16).to(cuda_dev)
+    v = k.clone()
+    L = c.layout()
+    cache = alloc_cache(L)
+    append(L, cache, k, v, 0)
+    torch.cuda.synchronize()
+    check_append(L, c, cache, bits(k), bits(v), 64)
