@@ -4,9 +4,11 @@
 Workload (default): the LLaVA-OneVision-7B-shaped decode step -- 28 layers,
 B = 1, 28 query / 4 KV heads, D = 128, a history of 14 text + 6273 visual
 positions (K INT4, V INT2, group 64, KV head 0 protected in bf16).  One step
-= for every layer: kvq_quantize_append of the step's own K/V row (a text
-position, kept bf16) and kvq_decode_attention over the history plus that
-row.  The history is quantised once before timing (prefill).
+= for every layer: kvq_decode_step, which stores the step's own K/V row (a
+text position, kept bf16) in the cache and attends over the history plus that
+row in one cooperative launch (--fused no: the two-call form,
+kvq_quantize_append of the row then kvq_decode_attention).  The history is
+quantised once before timing (prefill).
 
 value  = algorithmic bytes per step / device time per step (GB/s), where the
          bytes are the compressed cache rows actually attended, q, out and
@@ -53,6 +55,8 @@ def parse_args():
     ap.add_argument("--T", type=int, default=None, help="history length for the longctx workload")
     ap.add_argument("--layers", type=int, default=None, help="limit layers (parity/debug only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", choices=["yes", "no"], default="yes",
+                    help="kvq_decode_step (one launch per layer) or append + decode (three)")
     ap.add_argument("--prefill-in-step", choices=["auto", "yes", "no"], default="auto",
                     help="include kvq_quantize_append of the whole bf16 history in every step "
                          "(auto: yes for llava_next_13b, whose step includes the prefill)")
@@ -202,9 +206,11 @@ def prefill_bytes(L, T: int) -> int:
 class Model:
     """Per-layer caches (history quantised once), per-step inputs, outputs."""
 
-    def __init__(self, w: synth.Workload, dev, n_layers: int, prefill_in_step: bool = False):
+    def __init__(self, w: synth.Workload, dev, n_layers: int, prefill_in_step: bool = False,
+                 fused: bool = True):
         import bit_mixed_precision_kvq_gb300 as kvq
         self.kvq = kvq
+        self.fused = fused
         self.w = w
         self.T_hist = w.T
         self.T = w.T + 1
@@ -226,7 +232,7 @@ class Model:
                 del k, v
             self.layers.append(layer)
             ws_bytes = max(ws_bytes, int(L.workspace_bytes))
-        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # barrier counter = 0
         nL = n_layers
         # per-step device inputs/outputs, packed per layer so that the e2e leg
         # moves them with one copy each way
@@ -243,14 +249,22 @@ class Model:
             L = ly["L"]
             if self.prefill_in_step:
                 kvq.quantize_append(L, ly["cache"], ly["k"], ly["v"], 0)
+            self.decode_layer(l)
+
+    def decode_layer(self, l: int):
+        """The step's row into the cache + attention over [0, T)."""
+        ly = self.layers[l]
+        kvq, L = self.kvq, ly["L"]
+        if self.fused:
+            kvq.decode_step(L, ly["cache"], self.q[l], self.ks[l], self.vs[l], self.T_hist,
+                            self.out[l], self.scale, None, self.ws)
+        else:
             kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
             kvq.decode_attention(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
                                  self.ws)
 
-    def decode_layer(self, l: int):
-        ly = self.layers[l]
-        self.kvq.decode_attention(ly["L"], ly["cache"], self.q[l], self.T, self.out[l],
-                                  self.scale, None, self.ws)
+    def launches_per_layer(self) -> int:
+        return (1 if self.fused else 3) + (1 if self.prefill_in_step else 0)
 
     def prefill_layer(self, l: int):
         ly = self.layers[l]
@@ -271,7 +285,7 @@ def run_ours(args, rank, world, local):
     n_layers = args.layers or w.n_layers
     prefill = (args.prefill_in_step == "yes" or
                (args.prefill_in_step == "auto" and args.workload == "llava_next_13b"))
-    model = Model(w, dev, n_layers, prefill_in_step=prefill)
+    model = Model(w, dev, n_layers, prefill_in_step=prefill, fused=(args.fused == "yes"))
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -286,7 +300,7 @@ def run_ours(args, rank, world, local):
     with torch.cuda.graph(graph):
         model.step()
     torch.cuda.synchronize()
-    launches_per_step = (4 if prefill else 3) * n_layers  # [prefill] + append + split + combine
+    launches_per_step = model.launches_per_layer() * n_layers
 
     for _ in range(max(3, args.warmup)):
         flush()
@@ -312,8 +326,9 @@ def run_ours(args, rank, world, local):
     ms_per_step = dev_ms / args.steps
     value = total_bytes / (dev_ms * 1e-3) / 1e9
 
-    # roofline: the decode call of one layer (split kernel + combine), timed
-    # per launch with events on the launching stream, L2 flushed before each
+    # roofline: the decode of one layer (the fused step kernel, or append +
+    # split + combine), timed with events on the launching stream, L2 flushed
+    # before each
     reps = 20
     rl_ev = []
     for r in range(reps):
@@ -326,7 +341,8 @@ def run_ours(args, rank, world, local):
             rl_ev.append((a, b))
     torch.cuda.synchronize()
     launch_ms = float(np.mean([a.elapsed_time(b) for a, b in rl_ev]))
-    layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) for ly in model.layers]))
+    layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) + append_bytes(ly["L"], 1)
+                                 for ly in model.layers]))
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -398,7 +414,9 @@ def run_ours(args, rank, world, local):
                                f"protected {w.layers[0].protected}",
                    "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
                    "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attention (split + combine launches)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("split_mma_kernel<..., step> (kvq_decode_step, one launch)" if model.fused
+                                else "kvq_quantize_append + kvq_decode_attention (3 launches)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "per_launch_bytes": int(layer_bytes), "per_launch_us": round(launch_ms * 1e3, 3),

@@ -18,6 +18,7 @@ __all__ = [
     "KvqError", "load", "lib_path", "cache_layout", "quantize_append", "decode_attention",
     "kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention", "KVQ_MAX_HEADS",
     "decode_attention_static_ws", "kvq_decode_attention_static_ws", "STATIC_WS_BYTES",
+    "decode_step", "kvq_decode_step",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
@@ -29,6 +30,7 @@ KVQ_NSEG = 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
 EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
+                    "kvq_decode_step",
                     "kvq_decode_attention_static_ws", "kvq_last_cuda_error", "kvq_status_string"]
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
@@ -93,6 +95,8 @@ def load() -> ctypes.CDLL:
     lib.kvq_quantize_append.restype = ctypes.c_int
     lib.kvq_decode_attention.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P, sz, P]
     lib.kvq_decode_attention.restype = ctypes.c_int
+    lib.kvq_decode_step.argtypes = [ctypes.POINTER(Layout), P, P, P, P, i32, f32, P, P, P, sz, P]
+    lib.kvq_decode_step.restype = ctypes.c_int
     lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
     lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
     lib.kvq_last_cuda_error.argtypes = []
@@ -168,6 +172,24 @@ def decode_attention(L: Layout, cache, q, T: int, out, softmax_scale: Optional[f
                                      _addr(workspace), int(ws_bytes), _stream(stream))
     if st != 0:
         raise KvqError(st, "kvq_decode_attention")
+
+
+def decode_step(L: Layout, cache, q, k_new, v_new, t_new: int, out,
+                softmax_scale: Optional[float] = None, lse=None, workspace=None,
+                ws_bytes: Optional[int] = None, stream=None) -> None:
+    """kvq_decode_step: one fused decode step.  Stores the new token's bf16 K/V
+    rows ([B, H_kv, D]) at text position t_new and attends q over [0, t_new]
+    in one cooperative launch.  The workspace's first 4 bytes must be zero
+    before its first use (every call leaves them zero)."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kvq_decode_step(ctypes.byref(L), _addr(cache), _addr(q), _addr(k_new),
+                                _addr(v_new), int(t_new), float(softmax_scale), _addr(out),
+                                _addr(lse), _addr(workspace), int(ws_bytes), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_step")
 
 
 def decode_attention_static_ws(L: Layout, cache, q, T: int, out,

@@ -34,6 +34,7 @@ constexpr int kD = 128;          // head dimension supported by the kernels
 constexpr int kNH = KVQ_HEADS_PER_UNIT;  // query heads per unit (MMA N = 8)
 constexpr int kBf16PosBytes = 4 * kD;    // K + V bf16 rows of one position
 constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
+constexpr int kWsHeader = 256;           // workspace header: grid-barrier words
 // Work balance: a position costs its cache bytes plus this many byte
 // equivalents of unpack / tensor-core / softmax work, so that chunks of
 // cheap packed rows do not get several times more positions to compute.
@@ -135,6 +136,11 @@ struct Params {
   float* lse;          // [B][Hq] or null
   float* ws_o;         // [slots][kNH][kD]
   float* ws_ml;        // [slots][kNH][2]
+  // fused decode step only
+  const uint16_t* k_new;  // bf16 [B][Hkv][D]
+  const uint16_t* v_new;
+  int32_t t_new;          // the step's position (= T - 1), a text position
+  uint32_t* bar;          // grid barrier words: [0] arrivals, [1] generation
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
   Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host

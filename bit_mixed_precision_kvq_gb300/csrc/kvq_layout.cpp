@@ -82,9 +82,11 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
     off = align_up(off + L.bytes[s] + kPad, kAlign);
   }
   L.total_bytes = off;
-  // Workspace: one partial (o[8][D] fp32, (m, l)[8]) per slot, slots <= units + C - 1.
+  // Workspace: one partial (o[8][D] fp32, (m, l)[8]) per slot, slots <= units + C - 1,
+  // after a 256-byte header (grid-barrier words of the fused decode step).
   const int64_t slots = static_cast<int64_t>(L.units) + KVQ_MAX_CTAS - 1;
-  L.workspace_bytes = align_up(slots * kvq::kNH * D * 4, kAlign) + align_up(slots * kvq::kNH * 8, kAlign);
+  L.workspace_bytes = kvq::kWsHeader + align_up(slots * kvq::kNH * D * 4, kAlign) +
+                      align_up(slots * kvq::kNH * 8, kAlign);
   L.eff_bits_k = d.k_bits < 16 ? d.k_bits + 32.0 / d.group_size : 16.0;
   L.eff_bits_v = d.v_bits < 16 ? d.v_bits + 32.0 / d.group_size : 16.0;
   *out = L;

@@ -44,6 +44,7 @@ constexpr int kStageBytes = 32 * 1024;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
+constexpr uint32_t kBarrierPolls = 1u << 25;   // bounded grid-barrier wait (~2 s)
 constexpr uint32_t kF16Magic = 0x64006400u;    // two fp16 1024.0
 constexpr uint32_t kF16One = 0x3C003C00u;      // two fp16 1.0
 
@@ -55,6 +56,7 @@ struct SplitSmem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
+  uint32_t gen0;  // grid-barrier generation seen at kernel start (fused step)
 };
 
 enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2 };
@@ -79,6 +81,7 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // ---------------------------------------------------------------------------
 // Producer
 // ---------------------------------------------------------------------------
+template <bool kStep>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
@@ -108,8 +111,21 @@ __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, in
         }
         const uint32_t bytes = static_cast<uint32_t>(n) * (2 * kD);
         mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
-        bulk_g2s(dst, ks + row * (2 * kD), bytes, &sm.full[st]);
-        bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), bytes, &sm.full[st]);
+        if (kStep && kind == kTileText && t0 + n == p.plan.T) {
+          // The step's own row (position T - 1) comes from the input, not
+          // from the cache row that this launch is writing.
+          const uint32_t head = static_cast<uint32_t>(n - 1) * (2 * kD);
+          const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
+          if (head) {
+            bulk_g2s(dst, ks + row * (2 * kD), head, &sm.full[st]);
+            bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), head, &sm.full[st]);
+          }
+          bulk_g2s(dst + head, p.k_new + nrow, 2 * kD, &sm.full[st]);
+          bulk_g2s(dst + kBf16VOff + head, p.v_new + nrow, 2 * kD, &sm.full[st]);
+        } else {
+          bulk_g2s(dst, ks + row * (2 * kD), bytes, &sm.full[st]);
+          bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), bytes, &sm.full[st]);
+        }
       } else {
         const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
         const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
@@ -452,7 +468,104 @@ __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, 
   }
 }
 
-template <int KB, int VB, int G>
+// ---------------------------------------------------------------------------
+// Cross-split combine of one output row (b, hq): NW warps fold the unit's
+// partial slots with online rescaling (lane l owns d = 4l .. 4l+3), then the
+// warp states are merged through shared memory.  A NaN partial max (a failed
+// wait) makes the row NaN.  Partials are read from L2 (they were written by
+// other SMs).  `bar` synchronises the NW warps.
+// ---------------------------------------------------------------------------
+template <int NW, typename Bar>
+__device__ __forceinline__ void combine_row(const Params& p, int bq, int warp, int lane,
+                                            float (*sm_ml)[2], float4 (*sm_o)[32], bool force_nan,
+                                            Bar&& bar) {
+  const int b = bq / p.Hq;
+  const int hq = bq - b * p.Hq;
+  const int h = hq / p.g;
+  const int r = hq - h * p.g;
+  const int hc = r / kNH;
+  const int j = r - hc * kNH;
+  const int u = unit_of(p, b, h, hc);
+  int cf, cl;
+  plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool bad = force_nan;
+  // Warp w folds slots cf + 8w + {0..7}, then the next 8 * NW; the eight
+  // loads of a batch are issued before any of them is used.
+  for (int c0 = cf + 8 * warp; c0 <= cl; c0 += 8 * NW) {
+    float mb[8], lb[8];
+    float4 ob[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      mb[k] = -INFINITY;
+      lb[k] = 0.f;
+      ob[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 + k <= cl) {
+        const int64_t s = static_cast<int64_t>(u + c0 + k) * kNH + j;
+        mb[k] = __ldcg(p.ws_ml + s * 2);
+        lb[k] = __ldcg(p.ws_ml + s * 2 + 1);
+        ob[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + s * kD) + lane);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float m = mb[k];
+      if (m != m) bad = true;
+      if (m == -INFINITY || m != m) continue;
+      const float Mn = fmaxf(M, m);
+      const float a = exp2f(M - Mn), w = exp2f(m - Mn);
+      L = L * a + lb[k] * w;
+      O.x = O.x * a + ob[k].x * w;
+      O.y = O.y * a + ob[k].y * w;
+      O.z = O.z * a + ob[k].z * w;
+      O.w = O.w * a + ob[k].w * w;
+      M = Mn;
+    }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sm_ml[warp][0] = bad ? __int_as_float(0x7fffffff) : M;
+    sm_ml[warp][1] = L;
+  }
+  sm_o[warp][lane] = O;
+  bar();
+  if (warp == 0) {
+    float Mt = -INFINITY;
+    bool nan = false;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float m = sm_ml[w][0];
+      if (m != m) nan = true; else Mt = fmaxf(Mt, m);
+    }
+    float Lt = 0.f;
+    float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float m = sm_ml[w][0];
+      if (m == -INFINITY || m != m) continue;
+      const float sc = exp2f(m - Mt);
+      Lt = fmaf(sm_ml[w][1], sc, Lt);
+      const float4 o = sm_o[w][lane];
+      Ot.x = fmaf(o.x, sc, Ot.x);
+      Ot.y = fmaf(o.y, sc, Ot.y);
+      Ot.z = fmaf(o.z, sc, Ot.z);
+      Ot.w = fmaf(o.w, sc, Ot.w);
+    }
+    float inv = 1.0f / Lt;
+    if (nan) inv = __int_as_float(0x7fffffff);
+    uint2 packed;
+    packed.x = static_cast<uint32_t>(f32_to_bf16_bits(Ot.x * inv)) |
+               (static_cast<uint32_t>(f32_to_bf16_bits(Ot.y * inv)) << 16);
+    packed.y = static_cast<uint32_t>(f32_to_bf16_bits(Ot.z * inv)) |
+               (static_cast<uint32_t>(f32_to_bf16_bits(Ot.w * inv)) << 16);
+    reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(bq) * kD)[lane] = packed;
+    if (lane == 0 && p.lse) p.lse[bq] = nan ? inv : 0.69314718055994531f * (Mt + log2f(Lt));
+  }
+  bar();  // the shared scratch is reused by the next row
+}
+
+template <int KB, int VB, int G, bool kStep>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
@@ -520,6 +633,18 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
       const uint8_t* base = sm.stage[st];
+      if (kStep && kind == kTileText && t0 + n == p.plan.T && ui.hc == 0 && warp == 0) {
+        // Write the step's row (staged from the input) into the cache's text
+        // segment: lanes 0-15 the K row, lanes 16-31 the V row.
+        const int tr = p.t_new < p.vs ? p.t_new : p.t_new - p.Tv;
+        const int64_t row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
+        const int half = lane >> 4, q = lane & 15;
+        const uint4 w = *reinterpret_cast<const uint4*>(base + (half ? kBf16VOff : 0) +
+                                                       (n - 1) * (2 * kD) + 16 * q);
+        uint8_t* dst = const_cast<uint8_t*>(p.seg[half ? KVQ_SEG_TEXT_V : KVQ_SEG_TEXT_K]) +
+                       row * (2 * kD) + 16 * q;
+        *reinterpret_cast<uint4*>(dst) = w;
+      }
       const int nb = (n + 31) >> 5;
       const int first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
       gblk += nb;
@@ -581,9 +706,41 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     }
     named_bar(1, kConsumerWarps * 32);
   }
+
+  if constexpr (kStep) {
+    // ---- grid barrier: every CTA's partials are written ----
+    __threadfence();
+    named_bar(1, kConsumerWarps * 32);
+    if (ctid == 0) {
+      const uint32_t gen0 = sm.gen0;
+      if (atomicAdd(&p.bar[0], 1u) == gridDim.x - 1) {
+        p.bar[0] = 0u;  // leave the arrival counter at zero for the next call
+        __threadfence();
+        atomicAdd(&p.bar[1], 1u);
+      } else {
+        uint32_t polls = 0;
+        while (*reinterpret_cast<volatile uint32_t*>(&p.bar[1]) == gen0) {
+          if (++polls > kBarrierPolls) {
+            sm.abort = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      __threadfence();
+    }
+    named_bar(1, kConsumerWarps * 32);
+    // ---- combine: CTA c takes output rows c, c + C, ... ----
+    float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
+    float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
+    const bool failed = sm.abort != 0;
+    for (int bq = c; bq < p.B * p.Hq; bq += gridDim.x)
+      combine_row<kConsumerWarps>(p, bq, warp, lane, sm_ml, sm_o, failed,
+                                  []() { named_bar(1, kConsumerWarps * 32); });
+  }
 }
 
-template <int KB, int VB, int G>
+template <int KB, int VB, int G, bool kStep>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -599,12 +756,13 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
   }
   __syncthreads();
   pdl_wait();  // the previous kernel in the stream may have written q or the cache
+  if (kStep && threadIdx.x == 0) sm.gen0 = *reinterpret_cast<volatile uint32_t*>(&p.bar[1]);
   pdl_launch_dependents();
   if (warp == kConsumerWarps) {
-    if (lane == 0) producer_loop(p, sm, blockIdx.x);
+    if (lane == 0) producer_loop<kStep>(p, sm, blockIdx.x);
     return;
   }
-  consumer_loop<KB, VB, G>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G, kStep>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq

@@ -159,6 +159,31 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
                                 int32_t T, float softmax_scale, void* out_bf16, float* lse,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * kvq_decode_step -- one decode step of one layer in a single launch: the
+ * step's own K/V row is written into the cache at text position t_new
+ * (never quantised: "VLM_KV_Quantization", intro checklist) and the step's
+ * query attends to positions [0, t_new] (WSVD summary, section 2.라 flash
+ * decoding with on-chip reconstruction).  Same result as
+ * kvq_quantize_append(t0 = t_new, n_tok = 1) followed by
+ * kvq_decode_attention(T = t_new + 1), with the append, the split-KV pass and
+ * the cross-split combine fused into one cooperative kernel (a grid-wide
+ * barrier between the split pass and the combine).
+ *   k_new_bf16, v_new_bf16  device bf16 [B][H_kv][D], contiguous, 16-byte aligned
+ *   t_new      0 <= t_new < T_cap, outside [vis_start, vis_end)
+ *   workspace  as for kvq_decode_attention, and in addition its first 4
+ *              bytes (the barrier's arrival counter) must be zero before the
+ *              first kvq_decode_step call that uses it; every call leaves
+ *              them zero again.  Other workspace bytes are ignored on entry.
+ * If the grid barrier is not reached within a bounded wait (which only a
+ * fault elsewhere can cause) the call still terminates and its outputs are
+ * NaN.
+ */
+kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
+                           const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,
+                           float softmax_scale, void* out_bf16, float* lse, void* workspace,
+                           size_t ws_bytes, void* stream);
+
 /* Size in bytes of the device scratch array used by
  * kvq_decode_attention_static_ws (16 MiB: enough for layouts with up to
  * 3008 units, i.e. B * H_kv * ceil(g/8) <= 3008). */

@@ -90,7 +90,7 @@ def test_layout_matches_formula(lib, case):
     if kb < 16:
         assert L.row_bytes[kvq.SEG_K_CODES] * 8 == kb * D
     slots = L.units + 1024 - 1
-    assert L.workspace_bytes == _align(slots * 8 * D * 4, 256) + _align(slots * 8 * 8, 256)
+    assert L.workspace_bytes == 256 + _align(slots * 8 * D * 4, 256) + _align(slots * 8 * 8, 256)
 
 
 BAD_DESCS = [
@@ -158,6 +158,25 @@ def test_decode_argument_checks(lib):
         assert e.value.status == code, bad
     with pytest.raises(kvq.KvqError):
         kvq.decode_attention(L, FAKE, FAKE, 10, FAKE, float("nan"), 0, FAKE, ws, stream=0)
+
+
+def test_decode_step_argument_checks(lib):
+    # text 0-9 and 200-255, visual 10-199
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ws = L.workspace_bytes
+    ok = dict(cache=FAKE, q=FAKE, kn=FAKE, vn=FAKE, t=220, out=FAKE, lse=0, ws=FAKE, ws_bytes=ws)
+    for bad, code in ((dict(kn=0), 1), (dict(vn=0), 1), (dict(kn=FAKE + 8), 1),
+                      (dict(vn=FAKE + 2), 1), (dict(t=-1), 1), (dict(t=256), 1), (dict(t=10), 1),
+                      (dict(t=199), 1), (dict(cache=0), 1), (dict(q=FAKE + 8), 1),
+                      (dict(ws=0), 1), (dict(ws=FAKE + 64), 1), (dict(ws_bytes=ws - 1), 3)):
+        a = dict(ok)
+        a.update(bad)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_step(L, a["cache"], a["q"], a["kn"], a["vn"], a["t"], a["out"], 0.1,
+                            a["lse"], a["ws"], a["ws_bytes"], stream=0)
+        assert e.value.status == code, bad
+    with pytest.raises(kvq.KvqError):
+        kvq.decode_step(L, FAKE, FAKE, FAKE, FAKE, 220, FAKE, float("inf"), 0, FAKE, ws, stream=0)
 
 
 def test_corrupted_layout_rejected(lib):
