@@ -6,7 +6,7 @@ B = 1, 28 query / 4 KV heads, D = 128, a history of 14 text + 6273 visual
 positions (K INT4, V INT2, group 64, KV head 0 protected in bf16).  One step
 = for every layer: kvq_decode_step, which stores the step's own K/V row (a
 text position, kept bf16) in the cache and attends over the history plus that
-row in one cooperative launch (--fused no: the two-call form,
+row in one launch (--fused no: the two-call form,
 kvq_quantize_append of the row then kvq_decode_attention).  The history is
 quantised once before timing (prefill).
 
@@ -216,7 +216,7 @@ class Model:
         self.T = w.T + 1
         self.prefill_in_step = prefill_in_step
         self.layers = []
-        ws_bytes = 0
+        self.ws = {}  # one workspace per unit count (its counter area is sized by it)
         for l in range(n_layers):
             ls = w.layers[l]
             L = kvq.cache_layout(w.B, w.H_q, w.H_kv, w.D, self.T, w.vis_start, w.vis_end,
@@ -231,8 +231,10 @@ class Model:
             else:
                 del k, v
             self.layers.append(layer)
-            ws_bytes = max(ws_bytes, int(L.workspace_bytes))
-        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # barrier counter = 0
+            n = int(L.units)
+            if n not in self.ws or self.ws[n].numel() < int(L.workspace_bytes):
+                self.ws[n] = torch.zeros(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
+            layer["ws"] = self.ws[n]
         nL = n_layers
         # per-step device inputs/outputs, packed per layer so that the e2e leg
         # moves them with one copy each way
@@ -257,11 +259,11 @@ class Model:
         kvq, L = self.kvq, ly["L"]
         if self.fused:
             kvq.decode_step(L, ly["cache"], self.q[l], self.ks[l], self.vs[l], self.T_hist,
-                            self.out[l], self.scale, None, self.ws)
+                            self.out[l], self.scale, None, ly["ws"])
         else:
             kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
             kvq.decode_attention(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
-                                 self.ws)
+                                 ly["ws"])
 
     def launches_per_layer(self) -> int:
         return (1 if self.fused else 3) + (1 if self.prefill_in_step else 0)

@@ -29,13 +29,22 @@ const void* split_kernel_k16(int vb, int G, bool step);
 
 constexpr int kCombineWarps = 16;
 
-// Combine: one CTA per (b, hq), 16 warps (combine_row in kvq_split.cuh).
+// Combine: one CTA per output row (b, hq), 16 warps (combine_row).
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ Params p) {
   __shared__ float sm_ml[kCombineWarps][2];
   __shared__ float4 sm_o[kCombineWarps][32];
+  const int bq = blockIdx.x;
+  const int b = bq / p.Hq;
+  const int hq = bq - b * p.Hq;
+  const int h = hq / p.g;
+  const int r = hq - h * p.g;
+  const int hc = r / kNH;
+  const int u = unit_of(p, b, h, hc);
+  int cf, cl;
+  plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
   pdl_wait();
-  combine_row<kCombineWarps>(p, blockIdx.x, threadIdx.x >> 5, threadIdx.x & 31, sm_ml, sm_o, false,
-                             []() { __syncthreads(); });
+  combine_row<kCombineWarps>(p, u, r - hc * kNH, cf, cl, bq, threadIdx.x >> 5, threadIdx.x & 31, sm_ml,
+                             sm_o, false, []() { __syncthreads(); });
 }
 
 }  // namespace kvq
@@ -109,14 +118,15 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   p->lse = lse;
   const int64_t slots = static_cast<int64_t>(L->units) + KVQ_MAX_CTAS - 1;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p->bar = reinterpret_cast<uint32_t*>(ws);
-  p->ws_o = reinterpret_cast<float*>(ws + kvq::kWsHeader);
+  const int64_t cnt_bytes = kvq::ws_counter_bytes(L->units);
+  p->cnt = reinterpret_cast<uint32_t*>(ws);
+  p->ws_o = reinterpret_cast<float*>(ws + cnt_bytes);
   const int64_t o_bytes = (slots * kvq::kNH * kvq::kD * 4 + 255) / 256 * 256;
-  p->ws_ml = reinterpret_cast<float*>(ws + kvq::kWsHeader + o_bytes);
+  p->ws_ml = reinterpret_cast<float*>(ws + cnt_bytes + o_bytes);
   p->scale_log2 = softmax_scale * 1.4426950408889634f;
   packed_tile_geometry(p);
   p->plan = kvq_make_plan(L, T, n_sm);  // one CTA per SM
-  for (int c = 0; c <= p->plan.C; ++c) p->cuts[c] = kvq::plan_cut(p->plan, c);
+  kvq_plan_cuts(&p->plan, p->cuts);
   return KVQ_OK;
 }
 
@@ -167,9 +177,9 @@ extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const vo
   const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true);
   if (!fn) return KVQ_ERR_UNSUPPORTED;
   if ((st = prepare_split(fn, kSplitSmemBytes)) != KVQ_OK) return st;
-  // Cooperative launch: the grid barrier needs every CTA resident (one per
-  // SM, grid <= SM count).  Programmatic serialisation is added when the
-  // runtime accepts both attributes.
+  // Cooperative launch: a combining CTA may wait for other CTAs of its unit,
+  // so all CTAs must be resident together (one per SM, C <= SM count).
+  // Programmatic serialisation is added while the runtime accepts both.
   static int pdl_ok = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.plan.C);

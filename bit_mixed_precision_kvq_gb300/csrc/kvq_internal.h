@@ -9,13 +9,20 @@
 //     bytes -- 512 (bf16 K + V rows), or for a visual position of a packed
 //     head the packed K and V rows plus their fp16 scale/zero -- plus a
 //     fixed compute cost (kPosCost).
-//   * the concatenated cost stream of all units is cut into C chunks of
-//     equal cost; CTA c processes [cut(c), cut(c+1)).  Cuts inside a packed
-//     visual range are rounded down to a multiple of 16 rows so every staged
-//     tile starts on a 16-byte boundary in every segment.
+//   * chunks: when there are at least as many chunks C as units, every unit
+//     gets its own chunks, in number proportional to its cost (at least
+//     one), cut at equal cost inside the unit -- no chunk spans two units.
+//     Otherwise the concatenated cost stream of all units is cut into C
+//     chunks of equal cost.  CTA c processes [cut(c), cut(c+1)).  Cuts
+//     inside a packed visual range are rounded down to a multiple of 16
+//     rows so every staged tile starts on a 16-byte boundary in every
+//     segment.
 //   * CTA c writes one partial result (o, m, l) per unit it touches into
 //     workspace slot u + c.  The (u, c) pairs form a monotone staircase, so
 //     u + c is unique; there are at most units + C - 1 slots.
+//   * the fused decode step combines a unit's partials in the CTA that
+//     finishes the unit's last chunk (per-unit arrival counters at the start
+//     of the workspace).
 #pragma once
 
 #include <stdint.h>
@@ -34,7 +41,6 @@ constexpr int kD = 128;          // head dimension supported by the kernels
 constexpr int kNH = KVQ_HEADS_PER_UNIT;  // query heads per unit (MMA N = 8)
 constexpr int kBf16PosBytes = 4 * kD;    // K + V bf16 rows of one position
 constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
-constexpr int kWsHeader = 256;           // workspace header: grid-barrier words
 // Work balance: a position costs its cache bytes plus this many byte
 // equivalents of unpack / tensor-core / softmax work, so that chunks of
 // cheap packed rows do not get several times more positions to compute.
@@ -52,6 +58,9 @@ struct Plan {
   int64_t ub_p, ub_u; // cost of a protected / packed unit
   int64_t P_bytes;    // U_p * ub_p
   int64_t total;      // cost of all units
+  // per-unit chunks (aligned != 0, when C >= U): n_p per protected and n_q
+  // per packed unit, plus one for each of the first R units
+  int32_t aligned, n_p, n_q, R;
 };
 
 struct Cut {
@@ -59,46 +68,42 @@ struct Cut {
   int32_t p;  // position inside the unit
 };
 
-// Start of chunk c, 0 <= c <= C.  Monotone in c (lexicographic in (u, p)).
-KVQ_HD Cut plan_cut(const Plan& P, int32_t c) {
-  Cut r;
-  if (c >= P.C) {
-    r.u = P.U;
-    r.p = 0;
-    return r;
-  }
-  const int64_t X = (P.total * static_cast<int64_t>(c)) / P.C;
-  if (X < P.P_bytes) {
-    const int64_t u = X / P.ub_p;
-    const int64_t rem = X - u * P.ub_p;
-    r.u = static_cast<int32_t>(u);
-    r.p = static_cast<int32_t>(rem / kBf16PosCost);
-    return r;
-  }
-  const int64_t Xu = X - P.P_bytes;
-  const int64_t u = Xu / P.ub_u;
-  const int64_t rem = Xu - u * P.ub_u;
-  r.u = P.U_p + static_cast<int32_t>(u);
+// Position inside a unit at cost offset `rem` (0 <= rem < unit cost).
+KVQ_HD int32_t unit_cut_pos(const Plan& P, bool prot, int64_t rem) {
+  if (prot) return static_cast<int32_t>(rem / kBf16PosCost);
   const int64_t pre = static_cast<int64_t>(P.vsa) * kBf16PosCost;
   const int64_t vis = static_cast<int64_t>(P.vea - P.vsa) * P.w_vis;
-  if (rem < pre) {
-    r.p = static_cast<int32_t>(rem / kBf16PosCost);
-  } else if (rem < pre + vis) {
+  if (rem < pre) return static_cast<int32_t>(rem / kBf16PosCost);
+  if (rem < pre + vis) {
     int64_t row = (rem - pre) / P.w_vis;
     row -= row % kVisAlign;
-    r.p = P.vsa + static_cast<int32_t>(row);
-  } else {
-    r.p = P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosCost);
+    return P.vsa + static_cast<int32_t>(row);
   }
-  return r;
+  return P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosCost);
 }
 
-// Chunks that hold a piece of unit u: [c_first, c_last], by binary search
-// over a table of the cuts (cuts[c] = plan_cut(P, c), c = 0..C).
+// Last unit of chunk c: a chunk that ends exactly at the start of a unit
+// (cut (u, 0)) does not touch that unit.
+KVQ_HD int32_t chunk_last_unit(const Cut* cuts, int32_t c, int32_t U) {
+  const Cut a = cuts[c], e = cuts[c + 1];
+  if (e.p == 0 && e.u > a.u) return e.u - 1;
+  return e.u < U ? e.u : U - 1;
+}
+
+// Chunks that hold a piece of unit u: [c_first, c_last]; closed form for
+// per-unit chunks, else a binary search over the cut table (cuts[0..C]).
 //   c_last  = max c with cuts[c].u <= u
-//   c_first = min c with min(cuts[c+1].u, U-1) >= u
+//   c_first = min c with chunk_last_unit(c) >= u
 KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t* c_first,
                              int32_t* c_last) {
+  if (P.aligned) {  // closed form of the per-unit allocation
+    const int32_t base = u <= P.U_p ? u * P.n_p : P.U_p * P.n_p + (u - P.U_p) * P.n_q;
+    const int32_t c0 = base + (u < P.R ? u : P.R);
+    const int32_t n = (u < P.U_p ? P.n_p : P.n_q) + (u < P.R ? 1 : 0);
+    *c_first = c0;
+    *c_last = c0 + n - 1;
+    return;
+  }
   int32_t lo = 0, hi = P.C - 1;  // invariant: cuts[lo].u <= u
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) / 2;
@@ -106,15 +111,16 @@ KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t*
   }
   *c_last = lo;
   lo = 0;
-  hi = P.C - 1;  // end unit of C-1 is U-1 >= u
+  hi = P.C - 1;  // the last chunk ends with unit U-1 >= u
   while (lo < hi) {
     const int32_t mid = (lo + hi) / 2;
-    int32_t eu = cuts[mid + 1].u;
-    if (eu > P.U - 1) eu = P.U - 1;
-    if (eu >= u) hi = mid; else lo = mid + 1;
+    if (chunk_last_unit(cuts, mid, P.U) >= u) hi = mid; else lo = mid + 1;
   }
   *c_first = lo;
 }
+
+// Bytes of the per-unit counter area at the start of the workspace.
+KVQ_HD int64_t ws_counter_bytes(int32_t units) { return (4 * static_cast<int64_t>(units) + 255) / 256 * 256; }
 
 // Everything a kernel needs about one layer and one call (passed by value).
 struct Params {
@@ -140,7 +146,7 @@ struct Params {
   const uint16_t* k_new;  // bf16 [B][Hkv][D]
   const uint16_t* v_new;
   int32_t t_new;          // the step's position (= T - 1), a text position
-  uint32_t* bar;          // grid barrier words: [0] arrivals, [1] generation
+  uint32_t* cnt;          // per-unit arrival counters (zero between calls)
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
   Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host
@@ -183,6 +189,9 @@ KVQ_HD int32_t unit_of(const Params& p, int32_t b, int32_t h, int32_t hc) {
 kvq_status kvq_check_layout(const kvq_layout* L);
 void kvq_fill_params(const kvq_layout* L, kvq::Params* p);
 kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target);
+// The cut table cuts[0..P->C] of a plan (see the decomposition above); sets
+// the plan's per-unit chunk fields.
+void kvq_plan_cuts(kvq::Plan* P, kvq::Cut* cuts);
 int kvq_device_sm_count(int* n_sm);
 // Record a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.
 kvq_status kvq_cuda_fail(int err);

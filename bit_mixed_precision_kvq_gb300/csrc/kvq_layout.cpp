@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -85,7 +86,7 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   // Workspace: one partial (o[8][D] fp32, (m, l)[8]) per slot, slots <= units + C - 1,
   // after a 256-byte header (grid-barrier words of the fused decode step).
   const int64_t slots = static_cast<int64_t>(L.units) + KVQ_MAX_CTAS - 1;
-  L.workspace_bytes = kvq::kWsHeader + align_up(slots * kvq::kNH * D * 4, kAlign) +
+  L.workspace_bytes = kvq::ws_counter_bytes(L.units) + align_up(slots * kvq::kNH * D * 4, kAlign) +
                       align_up(slots * kvq::kNH * 8, kAlign);
   L.eff_bits_k = d.k_bits < 16 ? d.k_bits + 32.0 / d.group_size : 16.0;
   L.eff_bits_v = d.v_bits < 16 ? d.v_bits + 32.0 / d.group_size : 16.0;
@@ -179,6 +180,49 @@ kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target)
   if (C < 1) C = 1;
   P.C = static_cast<int32_t>(C);
   return P;
+}
+
+void kvq_plan_cuts(kvq::Plan* Pp, kvq::Cut* cuts) {
+  using kvq::Cut;
+  kvq::Plan& P = *Pp;
+  cuts[P.C] = Cut{P.U, 0};
+  P.aligned = P.C >= P.U ? 1 : 0;
+  P.n_p = P.n_q = P.R = 0;
+  if (!P.aligned) {
+    // Equal-cost cuts of the concatenated stream of units.
+    for (int32_t c = 0; c < P.C; ++c) {
+      const int64_t X = (P.total * static_cast<int64_t>(c)) / P.C;
+      if (X < P.P_bytes) {
+        const int64_t u = X / P.ub_p;
+        cuts[c] = Cut{static_cast<int32_t>(u), kvq::unit_cut_pos(P, true, X - u * P.ub_p)};
+      } else {
+        const int64_t u = (X - P.P_bytes) / P.ub_u;
+        cuts[c] = Cut{P.U_p + static_cast<int32_t>(u),
+                      kvq::unit_cut_pos(P, false, X - P.P_bytes - u * P.ub_u)};
+      }
+    }
+    return;
+  }
+  // Per-unit chunks, n_p for each protected and n_q for each packed unit in
+  // proportion to their costs (at least one each); the R chunks left over
+  // go one each to the first R units.
+  const int64_t U_q = P.U - P.U_p;
+  int64_t n_p = P.U_p ? std::max<int64_t>(1, P.C * P.ub_p / P.total) : 0;
+  int64_t n_q = U_q ? std::max<int64_t>(1, P.C * P.ub_u / P.total) : 0;
+  while (n_p * P.U_p + n_q * U_q > P.C) {  // only when a share was raised to 1
+    if (n_p > 1 && (n_q <= 1 || n_p * P.ub_u >= n_q * P.ub_p)) --n_p; else --n_q;
+  }
+  const int64_t R = P.C - n_p * P.U_p - n_q * U_q;
+  P.n_p = static_cast<int32_t>(n_p);
+  P.n_q = static_cast<int32_t>(n_q);
+  P.R = static_cast<int32_t>(R);
+  int32_t c = 0;
+  for (int32_t u = 0; u < P.U; ++u) {
+    const bool prot = u < P.U_p;
+    const int64_t n = (prot ? n_p : n_q) + (u < R ? 1 : 0);
+    const int64_t cost = prot ? P.ub_p : P.ub_u;
+    for (int64_t k = 0; k < n; ++k) cuts[c++] = Cut{u, kvq::unit_cut_pos(P, prot, cost * k / n)};
+  }
 }
 
 namespace {

@@ -44,7 +44,7 @@ constexpr int kStageBytes = 32 * 1024;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
-constexpr uint32_t kBarrierPolls = 1u << 25;   // bounded grid-barrier wait (~2 s)
+constexpr uint32_t kSpinPolls = 1u << 21;      // bounded inter-CTA wait (fused step)
 constexpr uint32_t kF16Magic = 0x64006400u;    // two fp16 1024.0
 constexpr uint32_t kF16One = 0x3C003C00u;      // two fp16 1.0
 
@@ -56,7 +56,8 @@ struct SplitSmem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
-  uint32_t gen0;  // grid-barrier generation seen at kernel start (fused step)
+  int role;   // fused step: combine role of this CTA for the current unit
+  int ncomb;  // fused step: CTAs combining the current unit
 };
 
 enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2 };
@@ -81,64 +82,97 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // ---------------------------------------------------------------------------
 // Producer
 // ---------------------------------------------------------------------------
-template <bool kStep>
-__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
+// The bulk copies of one tile, as f(stage offset, source, bytes) calls (2 to
+// 4 of them).  In the fused step the step's own row (position T - 1, the
+// last row of the last text tile) comes from the k_new / v_new inputs rather
+// than from the cache row that the launch itself writes.
+template <bool kStep, typename F>
+__device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int kind, int t0,
+                                             int n, F&& f) {
+  if (kind != kTilePacked) {
+    int64_t row;
+    const uint8_t *ks, *vs;
+    if (kind == kTileText) {
+      const int tr = t0 < p.vs ? t0 : t0 - p.Tv;
+      row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
+      ks = p.seg[KVQ_SEG_TEXT_K];
+      vs = p.seg[KVQ_SEG_TEXT_V];
+    } else {
+      row = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
+      ks = p.seg[KVQ_SEG_PROT_K];
+      vs = p.seg[KVQ_SEG_PROT_V];
+    }
+    const uint32_t bytes = static_cast<uint32_t>(n) * (2 * kD);
+    if (kStep && kind == kTileText && t0 + n == p.plan.T) {
+      const uint32_t head = bytes - 2 * kD;
+      const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
+      if (head) {
+        f(0u, ks + row * (2 * kD), head);
+        f(static_cast<uint32_t>(kBf16VOff), vs + row * (2 * kD), head);
+      }
+      f(head, reinterpret_cast<const uint8_t*>(p.k_new + nrow), static_cast<uint32_t>(2 * kD));
+      f(kBf16VOff + head, reinterpret_cast<const uint8_t*>(p.v_new + nrow), static_cast<uint32_t>(2 * kD));
+    } else {
+      f(0u, ks + row * (2 * kD), bytes);
+      f(static_cast<uint32_t>(kBf16VOff), vs + row * (2 * kD), bytes);
+    }
+  } else {
+    const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
+    const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
+    const uint32_t bks = round16(n * p.kszrow), bvs = round16(n * p.vszrow);
+    f(0u, p.seg[KVQ_SEG_K_CODES] + row * p.krow, bk);
+    f(static_cast<uint32_t>(p.pk_off_vc), p.seg[KVQ_SEG_V_CODES] + row * p.vrow, bv);
+    if (bks) f(static_cast<uint32_t>(p.pk_off_ksz), p.seg[KVQ_SEG_K_SZ] + row * p.kszrow, bks);
+    if (bvs) f(static_cast<uint32_t>(p.pk_off_vsz), p.seg[KVQ_SEG_V_SZ] + row * p.vszrow, bvs);
+  }
+}
+
+// Walk the CTA's tiles: f(unit info, kind, t0, n).
+template <typename F>
+__device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
-  const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
-  uint32_t it = 0;
+  const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
   for (int u = a.u; u <= u_last; ++u) {
     const int ps = (u == a.u) ? a.p : 0;
     const int pe = (u == e.u) ? e.p : p.plan.T;
     const UnitInfo ui = unit_info(p, u);
-    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) {
-      const int st = it % kStages;
-      const uint32_t round = it / kStages;
-      if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
-      uint8_t* dst = sm.stage[st];
-      if (kind != kTilePacked) {
-        int64_t row;
-        const uint8_t *ks, *vs;
-        if (kind == kTileText) {
-          const int tr = t0 < p.vs ? t0 : t0 - p.Tv;
-          row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
-          ks = p.seg[KVQ_SEG_TEXT_K];
-          vs = p.seg[KVQ_SEG_TEXT_V];
-        } else {
-          row = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
-          ks = p.seg[KVQ_SEG_PROT_K];
-          vs = p.seg[KVQ_SEG_PROT_V];
-        }
-        const uint32_t bytes = static_cast<uint32_t>(n) * (2 * kD);
-        mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
-        if (kStep && kind == kTileText && t0 + n == p.plan.T) {
-          // The step's own row (position T - 1) comes from the input, not
-          // from the cache row that this launch is writing.
-          const uint32_t head = static_cast<uint32_t>(n - 1) * (2 * kD);
-          const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
-          if (head) {
-            bulk_g2s(dst, ks + row * (2 * kD), head, &sm.full[st]);
-            bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), head, &sm.full[st]);
-          }
-          bulk_g2s(dst + head, p.k_new + nrow, 2 * kD, &sm.full[st]);
-          bulk_g2s(dst + kBf16VOff + head, p.v_new + nrow, 2 * kD, &sm.full[st]);
-        } else {
-          bulk_g2s(dst, ks + row * (2 * kD), bytes, &sm.full[st]);
-          bulk_g2s(dst + kBf16VOff, vs + row * (2 * kD), bytes, &sm.full[st]);
-        }
-      } else {
-        const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
-        const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
-        const uint32_t bks = round16(n * p.kszrow), bvs = round16(n * p.vszrow);
-        mbar_arrive_expect_tx(&sm.full[st], bk + bv + bks + bvs);
-        bulk_g2s(dst, p.seg[KVQ_SEG_K_CODES] + row * p.krow, bk, &sm.full[st]);
-        bulk_g2s(dst + p.pk_off_vc, p.seg[KVQ_SEG_V_CODES] + row * p.vrow, bv, &sm.full[st]);
-        if (bks) bulk_g2s(dst + p.pk_off_ksz, p.seg[KVQ_SEG_K_SZ] + row * p.kszrow, bks, &sm.full[st]);
-        if (bvs) bulk_g2s(dst + p.pk_off_vsz, p.seg[KVQ_SEG_V_SZ] + row * p.vszrow, bvs, &sm.full[st]);
-      }
-      ++it;
-    });
+    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) { f(ui, kind, t0, n); });
   }
+}
+
+// Before griddepcontrol.wait: pull the first kStages stages' worth of the
+// CTA's cache rows into L2.  L2 is coherent with every SM's stores, so a
+// line that the previous kernel writes later is simply updated there; the
+// copies into shared memory all come after the wait.
+__device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
+  uint32_t budget = kStages * kStageBytes;
+  walk_chunk(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+    if (budget == 0) return;
+    tile_sources<false>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
+      const uint32_t b = min(bytes, budget);
+      if (b) prefetch_l2(src, b);
+      budget -= b;
+    });
+  });
+}
+
+template <bool kStep>
+__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
+  uint32_t it = 0;
+  walk_chunk(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+    const int st = it % kStages;
+    const uint32_t round = it / kStages;
+    if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
+    uint8_t* dst = sm.stage[st];
+    uint32_t total = 0;
+    tile_sources<kStep>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
+    mbar_arrive_expect_tx(&sm.full[st], total);
+    tile_sources<kStep>(p, ui, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
+      bulk_g2s(dst + off, src, bytes, &sm.full[st]);
+    });
+    ++it;
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -469,30 +503,22 @@ __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, 
 }
 
 // ---------------------------------------------------------------------------
-// Cross-split combine of one output row (b, hq): NW warps fold the unit's
-// partial slots with online rescaling (lane l owns d = 4l .. 4l+3), then the
-// warp states are merged through shared memory.  A NaN partial max (a failed
-// wait) makes the row NaN.  Partials are read from L2 (they were written by
-// other SMs).  `bar` synchronises the NW warps.
+// Cross-split combine of one output row: column j of unit u, whose partials
+// sit in slots u + cf .. u + cl.  NW warps fold the slots with online
+// rescaling (warp w takes slots cf + 8w .. cf + 8w + 7, then the next 8 NW;
+// the eight loads of a batch are issued before any is used; lane l owns
+// d = 4l .. 4l+3), the warp states are merged through shared memory and
+// warp 0 writes out[orow] and lse[orow].  Partials are read from L2 (other
+// SMs wrote them).  A NaN partial max (a failed wait) or force_nan makes the
+// row NaN.  `bar` synchronises the NW warps.
 // ---------------------------------------------------------------------------
 template <int NW, typename Bar>
-__device__ __forceinline__ void combine_row(const Params& p, int bq, int warp, int lane,
-                                            float (*sm_ml)[2], float4 (*sm_o)[32], bool force_nan,
-                                            Bar&& bar) {
-  const int b = bq / p.Hq;
-  const int hq = bq - b * p.Hq;
-  const int h = hq / p.g;
-  const int r = hq - h * p.g;
-  const int hc = r / kNH;
-  const int j = r - hc * kNH;
-  const int u = unit_of(p, b, h, hc);
-  int cf, cl;
-  plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
+__device__ __forceinline__ void combine_row(const Params& p, int u, int j, int cf, int cl,
+                                            int64_t orow, int warp, int lane, float (*sm_ml)[2],
+                                            float4 (*sm_o)[32], bool force_nan, Bar&& bar) {
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   bool bad = force_nan;
-  // Warp w folds slots cf + 8w + {0..7}, then the next 8 * NW; the eight
-  // loads of a batch are issued before any of them is used.
   for (int c0 = cf + 8 * warp; c0 <= cl; c0 += 8 * NW) {
     float mb[8], lb[8];
     float4 ob[8];
@@ -502,9 +528,10 @@ __device__ __forceinline__ void combine_row(const Params& p, int bq, int warp, i
       lb[k] = 0.f;
       ob[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c0 + k <= cl) {
-        const int64_t s = static_cast<int64_t>(u + c0 + k) * kNH + j;
-        mb[k] = __ldcg(p.ws_ml + s * 2);
-        lb[k] = __ldcg(p.ws_ml + s * 2 + 1);
+        const int64_t s = (static_cast<int64_t>(u) + c0 + k) * kNH + j;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + s);
+        mb[k] = ml.x;
+        lb[k] = ml.y;
         ob[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + s * kD) + lane);
       }
     }
@@ -559,10 +586,20 @@ __device__ __forceinline__ void combine_row(const Params& p, int bq, int warp, i
                (static_cast<uint32_t>(f32_to_bf16_bits(Ot.y * inv)) << 16);
     packed.y = static_cast<uint32_t>(f32_to_bf16_bits(Ot.z * inv)) |
                (static_cast<uint32_t>(f32_to_bf16_bits(Ot.w * inv)) << 16);
-    reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(bq) * kD)[lane] = packed;
-    if (lane == 0 && p.lse) p.lse[bq] = nan ? inv : 0.69314718055994531f * (Mt + log2f(Lt));
+    reinterpret_cast<uint2*>(p.out + orow * kD)[lane] = packed;
+    if (lane == 0 && p.lse) p.lse[orow] = nan ? inv : 0.69314718055994531f * (Mt + log2f(Lt));
   }
-  bar();  // the shared scratch is reused by the next row
+  bar();  // the shared scratch is reused next
+}
+
+// Fused step: wait (bounded) until the unit's last arrival has reset its
+// counter to zero.
+__device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt) {
+  for (uint32_t i = 0; i < kSpinPolls; ++i) {
+    if (ld_acquire_gpu(cnt) == 0u) return true;
+    __nanosleep(32);
+  }
+  return false;
 }
 
 template <int KB, int VB, int G, bool kStep>
@@ -571,7 +608,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
-  const int u_last = e.u < p.plan.U ? e.u : p.plan.U - 1;
+  const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
   constexpr int ppg = G / 32;
   const float sl2 = p.scale_log2;
   uint32_t it = 0;    // tiles seen (stage ring position)
@@ -582,6 +619,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     const UnitInfo ui = unit_info(p, u);
     const int hq0 = ui.h * p.g + ui.hc * kNH;
     const int nh = min(kNH, p.g - ui.hc * kNH);
+    if (u == a.u) pdl_wait();  // q (and the cache) may come from the previous kernel
 
     // q of head column gid as the B operand, in the permuted d order; group sums.
     uint32_t qb[8][2];
@@ -681,6 +719,12 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
       sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
     }
+    // The fused step finishes a unit held by this CTA alone right here;
+    // otherwise the partial goes to slot u + c.
+    int cf = c, cl = c;
+    if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
+    const bool sole = kStep && cf == cl;
+    const int64_t row0 = static_cast<int64_t>(ui.b) * p.Hq + hq0;
     named_bar(1, kConsumerWarps * 32);
     const int64_t slot = static_cast<int64_t>(u) + c;
     for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
@@ -698,45 +742,56 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         }
       }
       if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
-      p.ws_o[(slot * kNH + j) * kD + d] = O;
-      if (d == 0) {
-        p.ws_ml[(slot * kNH + j) * 2] = M;
-        p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
-      }
-    }
-    named_bar(1, kConsumerWarps * 32);
-  }
-
-  if constexpr (kStep) {
-    // ---- grid barrier: every CTA's partials are written ----
-    __threadfence();
-    named_bar(1, kConsumerWarps * 32);
-    if (ctid == 0) {
-      const uint32_t gen0 = sm.gen0;
-      if (atomicAdd(&p.bar[0], 1u) == gridDim.x - 1) {
-        p.bar[0] = 0u;  // leave the arrival counter at zero for the next call
-        __threadfence();
-        atomicAdd(&p.bar[1], 1u);
+      if (sole) {
+        const float inv = (M != M) ? M : 1.0f / L;
+        p.out[(row0 + j) * kD + d] = f32_to_bf16_bits(O * inv);
+        if (d == 0 && p.lse) p.lse[row0 + j] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
       } else {
-        uint32_t polls = 0;
-        while (*reinterpret_cast<volatile uint32_t*>(&p.bar[1]) == gen0) {
-          if (++polls > kBarrierPolls) {
-            sm.abort = 1;
-            break;
-          }
-          __nanosleep(64);
+        p.ws_o[(slot * kNH + j) * kD + d] = O;
+        if (d == 0) {
+          p.ws_ml[(slot * kNH + j) * 2] = M;
+          p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
         }
       }
-      __threadfence();
     }
     named_bar(1, kConsumerWarps * 32);
-    // ---- combine: CTA c takes output rows c, c + C, ... ----
-    float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
-    float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
-    const bool failed = sm.abort != 0;
-    for (int bq = c; bq < p.B * p.Hq; bq += gridDim.x)
-      combine_row<kConsumerWarps>(p, bq, warp, lane, sm_ml, sm_o, failed,
-                                  []() { named_bar(1, kConsumerWarps * 32); });
+    if constexpr (kStep) {
+      if (!sole) {
+        // Publish the partial.  The last min(n, nh) arrivals at the unit's
+        // counter (n = its chunks) combine its rows, arrival n - nh + r
+        // taking rows r, r + min(n, nh), ...; the very last one resets the
+        // counter to zero (for the next call), which also releases the
+        // others, who wait for that.
+        if (ctid == 0) {
+          __threadfence();
+          const uint32_t n = static_cast<uint32_t>(cl - cf + 1);
+          const uint32_t nc = min(n, static_cast<uint32_t>(nh));
+          const uint32_t k = atomicAdd(&p.cnt[u], 1u);
+          int role = -1;
+          if (k == n - 1) {
+            __threadfence();
+            atomicExch(&p.cnt[u], 0u);
+            role = static_cast<int>(nc) - 1;
+          } else if (k >= n - nc) {
+            role = static_cast<int>(k - (n - nc));
+            if (!wait_unit_released(&p.cnt[u])) sm.abort = 1;
+          }
+          __threadfence();
+          sm.role = role;
+          sm.ncomb = static_cast<int>(nc);
+        }
+        named_bar(1, kConsumerWarps * 32);
+        const int role = sm.role, nc = sm.ncomb;
+        if (role >= 0) {
+          const bool bad = sm.abort != 0;
+          float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
+          float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
+          for (int j = role; j < nh; j += nc)
+            combine_row<kConsumerWarps>(p, u, j, cf, cl, row0 + j, warp, lane, sm_ml, sm_o, bad,
+                                        []() { named_bar(1, kConsumerWarps * 32); });
+        }
+      }
+    }
   }
 }
 
@@ -754,12 +809,14 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
     sm.abort = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-  pdl_wait();  // the previous kernel in the stream may have written q or the cache
-  if (kStep && threadIdx.x == 0) sm.gen0 = *reinterpret_cast<volatile uint32_t*>(&p.bar[1]);
   pdl_launch_dependents();
+  __syncthreads();
   if (warp == kConsumerWarps) {
-    if (lane == 0) producer_loop<kStep>(p, sm, blockIdx.x);
+    if (lane == 0) {
+      producer_prefetch(p, blockIdx.x);
+      pdl_wait();  // the previous kernel in the stream may have written the cache
+      producer_loop<kStep>(p, sm, blockIdx.x);
+    }
     return;
   }
   consumer_loop<KB, VB, G, kStep>(p, sm, blockIdx.x, warp, lane);

@@ -166,18 +166,25 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
  * query attends to positions [0, t_new] (WSVD summary, section 2.라 flash
  * decoding with on-chip reconstruction).  Same result as
  * kvq_quantize_append(t0 = t_new, n_tok = 1) followed by
- * kvq_decode_attention(T = t_new + 1), with the append, the split-KV pass and
- * the cross-split combine fused into one cooperative kernel (a grid-wide
- * barrier between the split pass and the combine).
+ * kvq_decode_attention(T = t_new + 1), up to the summation order of the
+ * cross-split combine.  The append, the split-KV pass and the combine run in
+ * one kernel: each (b, KV head, query-head chunk) unit is combined by the
+ * CTA that finishes the unit's last split, found with a per-unit arrival
+ * counter; nothing waits on another CTA.
  *   k_new_bf16, v_new_bf16  device bf16 [B][H_kv][D], contiguous, 16-byte aligned
  *   t_new      0 <= t_new < T_cap, outside [vis_start, vis_end)
- *   workspace  as for kvq_decode_attention, and in addition its first 4
- *              bytes (the barrier's arrival counter) must be zero before the
- *              first kvq_decode_step call that uses it; every call leaves
- *              them zero again.  Other workspace bytes are ignored on entry.
- * If the grid barrier is not reached within a bounded wait (which only a
- * fault elsewhere can cause) the call still terminates and its outputs are
- * NaN.
+ *   workspace  as for kvq_decode_attention; in addition its first
+ *              ceil(4 * L->units / 256) * 256 bytes hold the arrival
+ *              counters and must be zero before the first kvq_decode_step
+ *              call that uses the workspace (zero the whole workspace once
+ *              after allocating it).  Every call leaves them zero again.
+ *              Other workspace bytes are ignored on entry.  Calls sharing
+ *              one workspace must be ordered (one stream), and use layouts
+ *              with the same L->units (the counter area's size), or zero
+ *              the workspace again when switching.
+ * If a staged tile does not arrive within a bounded wait (which only a
+ * fault elsewhere can cause) the call still terminates and the affected
+ * outputs are NaN.
  */
 kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
                            const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,

@@ -3,8 +3,10 @@ the two-call path it fuses (kvq_quantize_append of the step's row, then
 kvq_decode_attention over [0, t_new]).
 
 Bar: the step's bf16 row lands in the cache bit-identically; outputs within
-4e-3 * max|V_hat| of the fp64 oracle; and, since both paths use the same
-work plan and arithmetic, out and lse bit-identical to the two-call path.
+4e-3 * max|V_hat| of the fp64 oracle.  Both paths use the same work plan and
+split arithmetic and differ only in the summation order of the cross-split
+combine, so they agree to a few fp32 rounding steps: at most one bf16 ulp
+of the output apart (asserted as 2^-7 |o| + 1e-5 max|V_hat|).
 """
 import math
 
@@ -20,10 +22,18 @@ pytestmark = pytest.mark.gpu
 SCALE = 1.0 / math.sqrt(128)
 
 
+def _cnt_bytes(L):
+    return (4 * int(L.units) + 255) // 256 * 256
+
+
 def _ws(L, dev):
     ws = torch.full((int(L.workspace_bytes),), 0x5A, dtype=torch.uint8, device=dev)
-    ws[:4] = 0  # the barrier's arrival counter
+    ws[:_cnt_bytes(L)] = 0  # the per-unit arrival counters
     return ws
+
+
+def _counters_zero(L, ws) -> bool:
+    return bool((ws[:_cnt_bytes(L)] == 0).all().item())
 
 
 def _step(L, cache, q, ks, vs, t_new, ws):
@@ -71,7 +81,6 @@ def test_steps_match_oracle_and_two_call_path(cuda_dev, kvq, ci):
     append(L, fused, k, v, 0)
     append(L, split, k, v, 0)
     ws = _ws(L, cuda_dev)
-    gen = int(ws[4:8].view(torch.int32).item())
     for i in range(n_steps):
         t = hist + i
         q = _q(c, 720 + ci, i, cuda_dev)
@@ -80,18 +89,22 @@ def test_steps_match_oracle_and_two_call_path(cuda_dev, kvq, ci):
         kvq.quantize_append(L, split, kr.unsqueeze(2), vr.unsqueeze(2), t)
         out_s, lse_s = decode(L, split, q, t + 1)
         torch.cuda.synchronize()
-        assert torch.equal(out_f.view(torch.int16), out_s.view(torch.int16)), (ci, i)
-        assert torch.equal(lse_f, lse_s), (ci, i)
         kf = torch.cat([k, ks[:, :, :i + 1]], 2)
         vf = torch.cat([v, vs_[:, :, :i + 1]], 2)
         ref, lr, vmax = oracle_decode(c, bits(q), bits(kf), bits(vf), t + 1, SCALE)
         check_decode(c, out_f, lse_f, ref, lr, vmax)
+        g = c.H_q // c.H_kv
+        a = out_f.float().cpu().numpy()
+        b = out_s.float().cpu().numpy()
+        for hq in range(c.H_q):
+            bar = 2.0 ** -7 * np.maximum(np.abs(a[:, hq]), np.abs(b[:, hq])) + \
+                1e-5 * vmax[:, hq // g][:, None]
+            assert np.all(np.abs(a[:, hq] - b[:, hq]) <= bar), (ci, i, hq)
+        assert np.allclose(lse_f.cpu().numpy(), lse_s.cpu().numpy(), rtol=0, atol=1e-4), (ci, i)
     assert torch.equal(fused, split)  # same cache bytes after the steps
     kf, vf = torch.cat([k, ks], 2), torch.cat([v, vs_], 2)
     check_append(L, c, fused, bits(kf), bits(vf), c.T_cap)
-    hdr = ws[:8].view(torch.int32).cpu().tolist()
-    assert hdr[0] == 0                     # arrival counter left at zero
-    assert (hdr[1] - gen) % (1 << 32) == n_steps  # one barrier generation per call
+    assert _counters_zero(L, ws)  # every call leaves the arrival counters at zero
 
 
 def test_step_before_visual_span(cuda_dev, kvq):
@@ -115,7 +128,7 @@ def test_step_before_visual_span(cuda_dev, kvq):
 
 def test_step_at_capacity_and_in_graph(cuda_dev, kvq):
     """The last slot of the cache (t_new = T_cap - 1), run eagerly and as a
-    replayed CUDA graph (the workspace counter survives replays)."""
+    replayed CUDA graph (the arrival counters return to zero every call)."""
     c = Case(1, 28, 4, 1000, 14, 990, 4, 2, 64, [0])
     L = c.layout()
     _, k, v = synth.random_case(900, c.B, c.H_q, c.H_kv, c.D, c.T_cap, cuda_dev)
@@ -142,4 +155,24 @@ def test_step_at_capacity_and_in_graph(cuda_dev, kvq):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
         assert torch.equal(lse, lse0)
-    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert _counters_zero(L, ws)
+
+
+def test_single_unit_many_chunks_and_many_units_few_chunks(cuda_dev, kvq):
+    """Both cut regimes: one unit split over many CTAs (B = 1, H_kv = 1,
+    long history), and more units than CTAs (B = 24, MHA: units are
+    combined inside the CTA that holds them)."""
+    for ci, c in enumerate([Case(1, 8, 1, 20000, 16, 19990, 2, 2, 32, []),
+                            Case(24, 48, 48, 96, 8, 90, 4, 4, 64, [5, 9])]):
+        L = c.layout()
+        t = c.T_cap - 1
+        _, k, v = synth.random_case(950 + ci, c.B, c.H_q, c.H_kv, c.D, c.T_cap, cuda_dev)
+        cache = alloc_cache(L)
+        append(L, cache, k[:, :, :t].contiguous(), v[:, :, :t].contiguous(), 0)
+        q = _q(c, 960 + ci, 0, cuda_dev)
+        ws = _ws(L, cuda_dev)
+        out, lse = _step(L, cache, q, k[:, :, t].contiguous(), v[:, :, t].contiguous(), t, ws)
+        torch.cuda.synchronize()
+        ref, lr, vmax = oracle_decode(c, bits(q), bits(k), bits(v), c.T_cap, SCALE)
+        check_decode(c, out, lse, ref, lr, vmax)
+        assert _counters_zero(L, ws)

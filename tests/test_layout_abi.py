@@ -90,7 +90,8 @@ def test_layout_matches_formula(lib, case):
     if kb < 16:
         assert L.row_bytes[kvq.SEG_K_CODES] * 8 == kb * D
     slots = L.units + 1024 - 1
-    assert L.workspace_bytes == 256 + _align(slots * 8 * D * 4, 256) + _align(slots * 8 * 8, 256)
+    assert L.workspace_bytes == (_align(4 * L.units, 256) + _align(slots * 8 * D * 4, 256)
+                                 + _align(slots * 8 * 8, 256))
 
 
 BAD_DESCS = [
