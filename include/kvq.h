@@ -17,14 +17,27 @@
  *     chip inside a flash-decoding pipeline (QK, softmax, PV fused) and never
  *     write the reconstructed tensors back to device memory.
  *
- * Readings where the pages are silent (all listed in the design doc):
+ * Readings where the pages are silent:
  *   quantiser = group-wise asymmetric min-max along D, groups of G consecutive
  *   elements, scale s = fp16((max - min) / (2^b - 1)), zero z = fp16(min + 0),
  *   code = clamp(rint_half_even((x - z) / s), 0, 2^b - 1) in fp32 with the
  *   stored fp16 s and z (code 0 if s == 0); dequantised value = code * s + z.
- *   Codes are packed little-endian into uint32 words: element d goes to word
- *   d / (32/b) at bit b * (d mod (32/b)).  bits == 16 keeps bf16.  Query head
- *   hq reads KV head hq / (H_q / H_kv).
+ *   bits == 16 keeps bf16.  Query head hq reads KV head hq / (H_q / H_kv).
+ *
+ * Storage order of a packed row (this library's own layout; the pages only
+ * ask that a b-bit code really take b bits).  The D = 128 codes of one
+ * position of one head fill 128 slots, slot j at bit b * (j mod (32/b)) of
+ * uint32 word j / (32/b) (little-endian).  Element d sits in slot
+ *   K rows, d = 32P + 8t + 4e + i (P, t, i in [0,4), e in {0,1}):
+ *     b = 2:  32t + 16*floor(i/2) + 8e + c,  c = {{4,7},{3,6},{2,5},{0,1}}[P][i mod 2]
+ *     b = 4:  32t + 8i + 4e + P
+ *     b = 8:  32t + 4*(2P + floor(i/2)) + 2e + (i mod 2)
+ *   V rows, d = 16m + 8r + n (m, n in [0,8), r in {0,1}), every b:
+ *     16n + 2m + r
+ * so that each tensor-core operand register of the decode kernel comes out
+ * of one masked word.  The scale/zero row of a packed row
+ * holds fp16 [z_0 .. z_{D/G-1}, s_0 .. s_{D/G-1}] (group g = elements
+ * [gG, gG + G)).
  *
  * Conventions for every entry point:
  *   - All device buffers are allocated and owned by the caller.  The library
@@ -63,8 +76,8 @@ typedef enum kvq_status {
 
 /* Segments of one layer's cache buffer (see kvq_layout.off / .bytes). */
 enum kvq_segment {
-  KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv_pad][D*k_bits/32]; bf16 rows if k_bits == 16 */
-  KVQ_SEG_K_SZ = 1,    /* half2 (s, z) [B][n_packed][Tv_pad][D/G]; empty if k_bits == 16 */
+  KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv_pad][D*k_bits/32] (storage order above); bf16 rows if k_bits == 16 */
+  KVQ_SEG_K_SZ = 1,    /* fp16 [B][n_packed][Tv_pad][2*D/G] = [z.., s..]; empty if k_bits == 16 */
   KVQ_SEG_V_CODES = 2, /* as K_CODES with v_bits */
   KVQ_SEG_V_SZ = 3,    /* as K_SZ with v_bits */
   KVQ_SEG_PROT_K = 4,  /* bf16 [B][n_prot][Tv][D]: visual K of protected heads */

@@ -68,6 +68,10 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.oracle_pack_row.restype = i32
     lib.oracle_quantize_pack_rows.argtypes = [P, i64, i32, i32, i32, P, P, P]
     lib.oracle_quantize_pack_rows.restype = i32
+    lib.oracle_code_slot.argtypes = [i32, i32, i32]
+    lib.oracle_code_slot.restype = i32
+    lib.oracle_quantize_pack_rows_stored.argtypes = [P, i64, i32, i32, i32, i32, P, P]
+    lib.oracle_quantize_pack_rows_stored.restype = i32
     lib.oracle_dequant_row.argtypes = [P, P, P, i32, i32, P]
     lib.oracle_dequant_row.restype = None
     lib.oracle_is_packed.argtypes = [i32, i32, i32, i32, i32]
@@ -134,6 +138,26 @@ def quantize_pack_rows(x_bf16: np.ndarray, G: int, bits: int, plant: int = 0):
     if rc != 0:
         raise ValueError("oracle_quantize_pack_rows rejected its arguments")
     return words, s, z
+
+
+def code_slot(kind: str, bits: int, d: int, plant: int = 0) -> int:
+    """Storage slot of element d in a packed K ("k") or V ("v") row."""
+    return int(load(plant).oracle_code_slot(0 if kind == "k" else 1, bits, d))
+
+
+def quantize_pack_rows_stored(x_bf16: np.ndarray, G: int, bits: int, kind: str, plant: int = 0):
+    """x_bf16 uint16 [..., 128] -> (words uint32 [n, 128*bits/32] in the cache's
+    storage order, sz uint16 [n, 2*128/G] = [z_0.., s_0..])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    D = x.shape[-1]
+    n = x.size // D
+    words = np.zeros((n, D * bits // 32), np.uint32)
+    sz = np.zeros((n, 2 * (D // G)), np.uint16)
+    rc = load(plant).oracle_quantize_pack_rows_stored(_ptr(x), n, D, G, bits,
+                                                      0 if kind == "k" else 1, _ptr(words), _ptr(sz))
+    if rc != 0:
+        raise ValueError("oracle_quantize_pack_rows_stored rejected its arguments")
+    return words, sz
 
 
 def dequant_row(codes, s, z, G: int, plant: int = 0) -> np.ndarray:

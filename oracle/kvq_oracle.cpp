@@ -18,7 +18,7 @@
 //   [WSVD] gist.science summary of WSVD, §2.라 (fused kernel): reconstruct
 //          K/V on chip and feed QK, softmax and PV directly.
 //
-// Readings taken where the pages are silent (each one listed in the design doc):
+// Readings taken where the pages are silent:
 //   * the quantiser is group-wise asymmetric min-max along D with a float
 //     zero equal to the group minimum, scale = (max-min)/(2^b-1), both
 //     stored as IEEE binary16;
@@ -27,8 +27,13 @@
 //     u = (x - z) / s (separate round-to-nearest subtraction and IEEE
 //     division), code = clamp(rint_half_even(u), 0, 2^b-1); a group whose
 //     stored scale is 0 gets all-zero codes;
-//   * packing: element d of a row goes to word d / (32/b) at bit offset
-//     b * (d mod (32/b)); bits == 16 means the row is kept as bf16;
+//   * packing: a sequence of codes goes to 32-bit words little-endian, code
+//     j to word j / (32/b) at bit offset b * (j mod (32/b)); bits == 16
+//     means the row is kept as bf16;
+//   * storage order (the cache layout of this library, not a page's): a
+//     packed K or V row holds element d at sequence slot sigma(d), defined
+//     in include/kvq.h and restated in oracle_code_slot below; the stored
+//     scale/zero row is [z_0 .. z_{D/G-1}, s_0 .. s_{D/G-1}];
 //   * a position is quantised iff it lies in the visual range, its KV head
 //     is not protected and the tensor's bit-width is below 16;
 //   * query head hq reads KV head hq / (H_q / H_kv);
@@ -221,6 +226,57 @@ int oracle_quantize_pack_rows(const uint16_t* x, int64_t n_rows, int D, int G, i
                             z_bits + r * (D / G)) != 0)
       return -1;
     if (oracle_pack_row(codes.data(), D, bits, words + r * W) != 0) return -1;
+  }
+  return 0;
+}
+
+// Storage slot of element d (D = 128) in a packed row of the cache, kind 0
+// = K, 1 = V (the layout documented in include/kvq.h, restated here from
+// that definition).  K: d = 32P + 8t + 4e + i with P, t, i in [0,4) and e in
+// {0,1};  V: d = 16m + 8r + n with m, n in [0,8) and r in {0,1}.  Returns -1
+// for an unsupported argument.
+int oracle_code_slot(int kind, int bits, int d) {
+  if (d < 0 || d >= 128 || !(bits == 2 || bits == 4 || bits == 8)) return -1;
+  if (kind == 1) {
+    const int m = d / 16, r = (d / 8) % 2, n = d % 8;
+    return 16 * n + 2 * m + r;
+  }
+  if (kind != 0) return -1;
+  const int P = d / 32, t = (d / 8) % 4, e = (d / 4) % 2, i = d % 4;
+  if (bits == 2) {
+    // crumb of register (P, i mod 2) inside its half-word
+    static const int crumb[4][2] = {{4, 7}, {3, 6}, {2, 5}, {0, 1}};
+#if ORACLE_PLANT == 10
+    return 32 * t + 16 * (i / 2) + 8 * e + crumb[P][(i + 1) % 2];  // planted: members swapped
+#else
+    return 32 * t + 16 * (i / 2) + 8 * e + crumb[P][i % 2];
+#endif
+  }
+  if (bits == 4) return 32 * t + 8 * i + 4 * e + P;
+  return 32 * t + 4 * (2 * P + i / 2) + 2 * e + i % 2;
+}
+
+// Quantise and pack n_rows rows of D = 128 values in the cache's storage
+// order: words[n_rows][D*bits/32] (slot sequence of oracle_code_slot) and the
+// stored scale/zero rows sz[n_rows][2*D/G] = [z_0.., s_0..].
+int oracle_quantize_pack_rows_stored(const uint16_t* x, int64_t n_rows, int D, int G, int bits,
+                                     int kind, uint32_t* words, uint16_t* sz) {
+  if (D != 128 || G <= 0 || D % G != 0) return -1;
+  std::vector<uint8_t> codes(D), slotted(D);
+  std::vector<uint16_t> s(D / G), z(D / G);
+  const int W = D * bits / 32, ng = D / G;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    if (oracle_quantize_row(x + r * D, D, G, bits, codes.data(), s.data(), z.data()) != 0) return -1;
+    for (int d = 0; d < D; ++d) {
+      const int j = oracle_code_slot(kind, bits, d);
+      if (j < 0) return -1;
+      slotted[j] = codes[d];
+    }
+    if (oracle_pack_row(slotted.data(), D, bits, words + r * W) != 0) return -1;
+    for (int g = 0; g < ng; ++g) {
+      sz[r * 2 * ng + g] = z[g];
+      sz[r * 2 * ng + ng + g] = s[g];
+    }
   }
   return 0;
 }

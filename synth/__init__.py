@@ -13,7 +13,7 @@ definition runs on CPU and GPU tensors):
   * normal = sqrt(-2 ln u1) * cos(2 pi u2)     (Box-Muller, fp64), then -> bf16.
 splitmix64 is Steele, Lea and Flood's 64-bit mixer (2014).
 
-Workload shapes (from the pages; see the design doc for the full recipe):
+Workload shapes (from the pages):
   * LLaVA-OneVision-7B: GQA 28 query / 4 KV heads, D = 128, 32 frames x ~196
     visual tokens ~ 6,273, 14 historical text tokens before them, K stored
     after RoPE ("VLM_KV_Quantization", §2).

@@ -218,6 +218,39 @@ def pin_pack_roundtrip(plant: int = 0):
         assert back == [int(c) for c in codes]
 
 
+def pin_slot_worked_examples(plant: int = 0):
+    """Storage slots of a few elements, derived by hand from the layout."""
+    with open(os.path.join(GOLDEN, "slot_order_examples.json")) as f:
+        ex = json.load(f)
+    for bits, pairs in ex["k"].items():
+        for d, slot in pairs:
+            assert oracle.code_slot("k", int(bits), d, plant) == slot, ("k", bits, d)
+    for bits in (2, 4, 8):
+        for d, slot in ex["v"]:
+            assert oracle.code_slot("v", bits, d, plant) == slot, ("v", bits, d)
+
+
+def pin_slot_order_is_permutation(plant: int = 0):
+    """Every element gets its own slot, and the stored words hold exactly the
+    row's codes (read back through the slot order)."""
+    rng = np.random.default_rng(5)
+    for kind in ("k", "v"):
+        for bits in (2, 4, 8):
+            slots = [oracle.code_slot(kind, bits, d, plant) for d in range(128)]
+            assert sorted(slots) == list(range(128)), (kind, bits)
+            for G in (32, 64, 128):
+                x = _bf16_bits_from_float(rng.standard_normal((3, 128)) * 3.0)
+                words, sz = oracle.quantize_pack_rows_stored(x, G, bits, kind, plant)
+                w_seq, s_seq, z_seq = oracle.quantize_pack_rows(x, G, bits, plant)
+                per, mask = 32 // bits, (1 << bits) - 1
+                for r in range(3):
+                    seq = [(int(w_seq[r, d // per]) >> (bits * (d % per))) & mask for d in range(128)]
+                    got = [(int(words[r, j // per]) >> (bits * (j % per))) & mask for j in slots]
+                    assert got == seq, (kind, bits, G, r)
+                    ng = 128 // G
+                    assert list(sz[r, :ng]) == list(z_seq[r]) and list(sz[r, ng:]) == list(s_seq[r])
+
+
 # ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------
@@ -351,6 +384,8 @@ ALL_PINS = [
     pin_round_trip_bound,
     pin_pack_worked_examples,
     pin_pack_roundtrip,
+    pin_slot_worked_examples,
+    pin_slot_order_is_permutation,
     pin_attention_single_position,
     pin_attention_uniform,
     pin_attention_weights_sum,

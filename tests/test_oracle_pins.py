@@ -22,6 +22,7 @@ PLANTS = {
     7: "binary16 conversion truncates",
     8: "softmax scale dropped",
     9: "scale uses 2^b steps instead of 2^b - 1",
+    10: "2-bit K storage slots of a register pair swapped",
 }
 
 
