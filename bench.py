@@ -329,20 +329,25 @@ def run_ours(args, rank, world, local):
     value = total_bytes / (dev_ms * 1e-3) / 1e9
 
     # roofline: the decode of one layer (the fused step kernel, or append +
-    # split + combine), timed with events on the launching stream, L2 flushed
-    # before each
+    # split + combine), timed with events on the launching stream around a
+    # CUDA graph of every layer's decode (back-to-back, as in the step), L2
+    # flushed before each replay; per launch = replay time / layers
+    rl_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rl_graph):
+        for l in range(n_layers):
+            model.decode_layer(l)
+    torch.cuda.synchronize()
     reps = 20
     rl_ev = []
     for r in range(reps):
-        for l in range(n_layers):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            model.decode_layer(l)
-            b.record()
-            rl_ev.append((a, b))
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rl_graph.replay()
+        b.record()
+        rl_ev.append((a, b))
     torch.cuda.synchronize()
-    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in rl_ev]))
+    launch_ms = float(np.median([a.elapsed_time(b) for a, b in rl_ev])) / n_layers
     layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) + append_bytes(ly["L"], 1)
                                  for ly in model.layers]))
     peaks = {}

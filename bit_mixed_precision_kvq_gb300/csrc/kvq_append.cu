@@ -38,13 +38,34 @@ constexpr int kRowsPerWarp = 32 / kLanesPerRow;     // 8
 // near-ties.
 __device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
 
-__device__ __forceinline__ float bf16x2_min_lohi(uint32_t w) {
-  return fminf(bf16_lo(w), bf16_hi(w));
+// Value of blk[sel] for a runtime sel in [0, 4) without local memory.
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&blk)[4], int sel) {
+  const uint32_t lo = (sel & 1) ? blk[1] : blk[0];
+  const uint32_t hi = (sel & 1) ? blk[3] : blk[2];
+  return (sel & 2) ? hi : lo;
 }
 
-// Quantise and store the lane's 32 elements (16 bf16 pairs in w[]) of one
-// row.  `gmask` = the 4 lanes of this row (shuffle partners for G > 32).
-template <int BITS>
+// Quantise the lane's 32 elements (16 bf16 pairs in w[]) of one row and
+// store them in the cache's storage order (slot sigma(d) of the row, see
+// kvq.h).  The lane (part) owns elements d = 32 part + e, e in [0, 32).  Its
+// codes land in every lane's slice of the row, so each lane first builds,
+// for each of the row's 4 lanes, the words of that lane's slice with its own
+// codes already in place (zeros elsewhere); a 4-lane exchange (3 xor-shuffle
+// rounds) then gives every lane the pieces of its own slice, which it ORs
+// and stores.
+//   K, d = 32P + 8t + 4e' + i (P = part): slice t (slots 32t ..) belongs to
+//     lane t.  Code (t, e', i) goes to slice word / bit
+//       b = 2: word floor(i/2), bit 16e' + 2c(P, i mod 2)
+//       b = 4: word i,          bit 16e' + 4P
+//       b = 8: word 2P + floor(i/2), bit 16e' + 8 (i mod 2)
+//   V, d = 16m + 8r + n (m = 2 part + m'): slices 2l, 2l+1 (slots 16n ..)
+//     belong to lane l = floor(n/2).  Code (m', r, n) goes to bit
+//       b = 2: 8 part + 2c'            of the slice's word
+//       b = 4: 16 (part mod 2) + 4c'   of the slice's word floor(part/2)
+//       b = 8: 8c'                     of the slice's word part
+//     with c' = 2m' + r.
+// `gmask` = the 4 lanes of this row (shuffle partners).
+template <int BITS, bool kV>
 __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, int part, uint32_t gmask,
                                               uint8_t* codes_row, uint8_t* sz_row) {
   // group min / max over the lane's elements (packed bf16 pairs), then over
@@ -70,28 +91,38 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, in
   const __half zh = __float2half_rn(mn);
   const float sf = __half2float(sh);
   const float zf = __half2float(zh);
-  // Store the group's (s, z) once (first lane of the group).
+  // Store the group's z and s once (first lane of the group): fp16 row
+  // [z_0 .. z_{ng-1}, s_0 .. s_{ng-1}].
   if ((part & (G / kLaneElems - 1)) == 0) {
-    __half2 sz;
-    sz.x = sh;
-    sz.y = zh;
-    reinterpret_cast<__half2*>(sz_row)[(part * kLaneElems) / G] = sz;
+    const int ng = kD / G, g = (part * kLaneElems) / G;
+    reinterpret_cast<__half*>(sz_row)[g] = zh;
+    reinterpret_cast<__half*>(sz_row)[ng + g] = sh;
   }
+  // blk[x][l]: word x of what this lane sends to row lane l
+  constexpr int kSend = (!kV && BITS == 4) ? 4 : 2;
+  uint32_t blk[kSend][4];
+#pragma unroll
+  for (int x = 0; x < kSend; ++x)
+#pragma unroll
+    for (int l = 0; l < 4; ++l) blk[x][l] = 0u;
+  // crumb table of 2-bit K registers: c(P, 0), c(P, 1)
+  const uint32_t c0 = (0x0234u >> (4 * part)) & 0xFu;  // P = 0..3 -> 4, 3, 2, 0
+  const uint32_t c1 = (0x1567u >> (4 * part)) & 0xFu;  // P = 0..3 -> 7, 6, 5, 1
   // code = clamp(rint(fl(fl(x - z) / s))).  The quotient is first formed as
   // fl(d * fl(1/s)), within 3 * 2^-24 |u| of the correctly rounded one; rint
   // is constant between half-integers, so both give the same code unless the
   // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
   // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
   // it; only then is the IEEE division evaluated (out of line, rare).
-  constexpr int kWordsPerLane = BITS;  // 32 codes * BITS bits / 32
-  uint32_t words[kWordsPerLane];
-#pragma unroll
-  for (int i = 0; i < kWordsPerLane; ++i) words[i] = 0u;
-  if (sf != 0.0f) {
-    const float rs = __frcp_rn(sf);
+  // A group whose stored scale is 0 gets code 0 everywhere: with rs = 0 every
+  // quotient is 0 (or NaN for an infinite input, which also converts to 0)
+  // and no near-tie is flagged.  Every lane runs the same code so that the
+  // row's shuffles and votes stay converged.
+  {
+    const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
     const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {  // 8 elements at a time
+    for (int c8 = 0; c8 < 4; ++c8) {  // 8 elements at a time: e = 8 c8 + k
       float d[8], u[8];
       uint32_t need = 0;
 #pragma unroll
@@ -111,20 +142,75 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, in
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t code = min(__float2uint_rn(u[k]), cmax);  // round half to even; < 0 -> 0
-        const int e = c8 * 8 + k;                                 // element within the lane
-        words[(e * BITS) >> 5] |= code << ((e * BITS) & 31);
+        if constexpr (!kV) {
+          // K: destination lane t = c8, e' = k / 4, i = k % 4
+          const int ep = k >> 2, i = k & 3;
+          if constexpr (BITS == 2) {
+            blk[i >> 1][c8] |= code << (16 * ep + 2 * ((i & 1) ? c1 : c0));
+          } else if constexpr (BITS == 4) {
+            blk[i][c8] |= code << (16 * ep + 4 * part);
+          } else {
+            blk[i >> 1][c8] |= code << (16 * ep + 8 * (i & 1));
+          }
+        } else {
+          // V: c' = c8 (= 2m' + r), n = k -> destination lane k / 2, slice k % 2
+          if constexpr (BITS == 2) {
+            blk[k & 1][k >> 1] |= code << (8 * part + 2 * c8);
+          } else if constexpr (BITS == 4) {
+            blk[k & 1][k >> 1] |= code << (16 * (part & 1) + 4 * c8);
+          } else {
+            blk[k & 1][k >> 1] |= code << (8 * c8);
+          }
+        }
       }
     }
   }
-  // Codes of the lane's 32 elements: BITS words at byte offset part * 4 * BITS.
+  // 4-lane exchange: in round r each lane swaps with lane part ^ r.
+  uint32_t piece[kSend][4];  // piece[x][src]: word x received from row lane src
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int peer = part ^ r;
+#pragma unroll
+    for (int x = 0; x < kSend; ++x) {
+      const uint32_t mine = pick4(blk[x], peer);
+      const uint32_t got = r ? __shfl_xor_sync(gmask, mine, r, kLanesPerRow) : mine;
+#pragma unroll
+      for (int src = 0; src < 4; ++src)
+        if (peer == src) piece[x][src] = got;  // selects: stays in registers
+    }
+  }
+  // This lane's BITS words: its K slice, or its two V slices (2 part, 2 part + 1).
+  uint32_t out[BITS];
+#pragma unroll
+  for (int q = 0; q < BITS; ++q) out[q] = 0u;
+#pragma unroll
+  for (int src = 0; src < 4; ++src) {
+    if constexpr (!kV) {
+      if constexpr (BITS == 8) {
+        out[2 * src] = piece[0][src];
+        out[2 * src + 1] = piece[1][src];
+      } else {
+#pragma unroll
+        for (int x = 0; x < kSend; ++x) out[x] |= piece[x][src];
+      }
+    } else {
+      constexpr int kSliceWords = BITS / 2;
+#pragma unroll
+      for (int sl = 0; sl < 2; ++sl) {
+        if constexpr (BITS == 2) out[sl] |= piece[sl][src];
+        else if constexpr (BITS == 4) out[kSliceWords * sl + src / 2] |= piece[sl][src];
+        else out[kSliceWords * sl + src] = piece[sl][src];
+      }
+    }
+  }
   uint8_t* dst = codes_row + part * 4 * BITS;
   if constexpr (BITS == 2) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
   } else if constexpr (BITS == 4) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
   } else {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
-    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(words[4], words[5], words[6], words[7]);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(out[4], out[5], out[6], out[7]);
   }
 }
 
@@ -179,9 +265,15 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
       if (bits < 16) {
         uint8_t* sz = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_V_SZ : KVQ_SEG_K_SZ]) +
                       row * (which ? p.vszrow : p.kszrow);
-        if (bits == 2) quantize_lane<2>(w, p.G, part, gmask, codes, sz);
-        else if (bits == 4) quantize_lane<4>(w, p.G, part, gmask, codes, sz);
-        else quantize_lane<8>(w, p.G, part, gmask, codes, sz);
+        if (which) {
+          if (bits == 2) quantize_lane<2, true>(w, p.G, part, gmask, codes, sz);
+          else if (bits == 4) quantize_lane<4, true>(w, p.G, part, gmask, codes, sz);
+          else quantize_lane<8, true>(w, p.G, part, gmask, codes, sz);
+        } else {
+          if (bits == 2) quantize_lane<2, false>(w, p.G, part, gmask, codes, sz);
+          else if (bits == 4) quantize_lane<4, false>(w, p.G, part, gmask, codes, sz);
+          else quantize_lane<8, false>(w, p.G, part, gmask, codes, sz);
+        }
         continue;
       }
       dst = codes;

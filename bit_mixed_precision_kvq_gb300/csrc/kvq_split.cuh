@@ -45,12 +45,10 @@ constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
 constexpr uint32_t kSpinPolls = 1u << 21;      // bounded inter-CTA wait (fused step)
-constexpr uint32_t kF16Magic = 0x64006400u;    // two fp16 1024.0
-constexpr uint32_t kF16One = 0x3C003C00u;      // two fp16 1.0
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
-  float merge_o[kConsumerWarps][kNH][kD];
+  float merge_o[kConsumerWarps][kNH][kD + 4];  // padded rows: fewer bank conflicts
   float merge_ml[kConsumerWarps][kNH][2];
   float qsum[kConsumerWarps][kNH][4];
   uint64_t full[kStages];
@@ -184,18 +182,22 @@ __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, in
 // d in [32P, 32P+32), lane tig owns d0 = 32P + 8*tig .. d0+7 and places
 //   k-step 2P  : slots (2tig, 2tig+1) <- (d0, d0+4), slots (2tig+8, 2tig+9) <- (d0+1, d0+5)
 //   k-step 2P+1: slots (2tig, 2tig+1) <- (d0+2, d0+6), slots (2tig+8, 2tig+9) <- (d0+3, d0+7)
-// The q operand (B) is loaded with the same permutation.  Each k-step pair
-// stays inside one quantisation group (G >= 32).
+// i.e. register i of pair P holds (d0 + i, d0 + i + 4).  The q operand (B)
+// is loaded with the same permutation.  Each k-step pair stays inside one
+// quantisation group (G >= 32).
+//
+// Packed codes enter the tensor cores as exact fp16 subnormals: a b-bit
+// code masked in place at mantissa bits [p, p + b) of a half is the value
+// c * 2^(p - 24), so one AND (after at most one shift of the word) yields
+// a whole operand register.  The storage order of the rows (kvq.h) puts
+// the codes of each register at one bit offset p, and makes p the same for
+// the four registers of a K k-step pair; V registers may differ in p from
+// row to row of the output (their factor is applied per row).
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-
-// Masked code-field pair -> exact fp16 codes (c_lo, c_hi).
-__device__ __forceinline__ uint32_t codes_f16(uint32_t x, uint32_t mask) {
-  return hsub2_u(and_or(x, mask, kF16Magic), kF16Magic);
-}
 
 // bf16 elements -> fp16 pair.
 __device__ __forceinline__ uint32_t bf16pair_f16(uint32_t lo_word, bool lo_hi, uint32_t hi_word, bool hi_hi) {
@@ -204,122 +206,108 @@ __device__ __forceinline__ uint32_t bf16pair_f16(uint32_t lo_word, bool lo_hi, u
   return pack_f16x2(a, b);
 }
 
-// Four fp16 pairs (d0,d0+4), (d0+1,d0+5), (d0+2,d0+6), (d0+3,d0+7) of one
-// row's 8 elements starting at d0.  KB = bits (16 = bf16 row).
-// K code pair -> fp16 (v_lo, v_hi) with v = 1 + c * 2^-m: mask the code
-// into the mantissa under the exponent of 1.0.
-__device__ __forceinline__ uint32_t kcode_pair(uint32_t x, uint32_t mask) { return and_or(x, mask, kF16One); }
+// bf16x2 -> f16x2 (lo stays lo).
+__device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t x) { return pack_f16x2(bf16_lo(x), bf16_hi(x)); }
 
 // Four fp16 pairs (d0,d0+4), (d0+1,d0+5), (d0+2,d0+6), (d0+3,d0+7) of one
-// row's 8 elements starting at d0.  KB = bits (16 = bf16 row).  For packed
-// rows the pairs hold 1 + c * 2^-m (m = kKShift<KB>).
-template <int KB>
-__device__ __forceinline__ void k_row_pairs(const uint8_t* row, int P, int tig, uint32_t (&f)[4]) {
-  if constexpr (KB == 4) {
-    // nibble k at bits 4k (and 16 + 4k) -> mantissa bits 6..9
-    const uint32_t w = lds32(row + 4 * (4 * P + tig));
-    f[0] = kcode_pair(w << 6, 0x03C003C0u);
-    f[1] = kcode_pair(w << 2, 0x03C003C0u);
-    f[2] = kcode_pair(w >> 2, 0x03C003C0u);
-    f[3] = kcode_pair(w >> 6, 0x03C003C0u);
-  } else if constexpr (KB == 2) {
-    // bytes of the lane's half-word split into the two halves, then
-    // crumb k at bits 2k (and 16 + 2k) -> mantissa bits 8..9
-    const uint32_t w = lds32(row + 4 * (2 * P + (tig >> 1)));
-    const uint32_t h = tig & 1;
-    const uint32_t r = prmt(w, 0u, (2 * h) | (4u << 4) | ((2 * h + 1) << 8) | (4u << 12));
-    f[0] = kcode_pair(r << 8, 0x03000300u);
-    f[1] = kcode_pair(r << 6, 0x03000300u);
-    f[2] = kcode_pair(r << 4, 0x03000300u);
-    f[3] = kcode_pair(r << 2, 0x03000300u);
-  } else if constexpr (KB == 8) {
-    // byte k of the two words -> mantissa bits 0..7
-    const uint2 w = lds64(row + 4 * (8 * P + 2 * tig));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t x = prmt(w.x, w.y, k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-      f[k] = kcode_pair(x, 0x00FF00FFu);
-    }
-  } else {  // bf16 row
-    const uint4 r = lds128(row + 2 * (32 * P + 8 * tig));
-    f[0] = bf16pair_f16(r.x, false, r.z, false);
-    f[1] = bf16pair_f16(r.x, true, r.z, true);
-    f[2] = bf16pair_f16(r.y, false, r.w, false);
-    f[3] = bf16pair_f16(r.y, true, r.w, true);
-  }
+// bf16 row's 8 elements starting at d0 = 32P + 8 tig.
+__device__ __forceinline__ void k_bf16_pairs(const uint8_t* row, int P, int tig, uint32_t (&f)[4]) {
+  const uint4 r = lds128(row + 2 * (32 * P + 8 * tig));
+  f[0] = bf16pair_f16(r.x, false, r.z, false);
+  f[1] = bf16pair_f16(r.x, true, r.z, true);
+  f[2] = bf16pair_f16(r.y, false, r.w, false);
+  f[3] = bf16pair_f16(r.y, true, r.w, true);
 }
 
-// 2^m of the K code placement above.
+// Packed K: all 16 operand registers f[P][i] (pair P, register i) of one
+// row from the lane's slice (slots 32 tig .. 32 tig + 31).  Bit offsets:
+//   b = 2: word floor(i/2); P = 0..3 at p = 8, 6, 4, 2 -- member i mod 2 = 0
+//          from the word (P = 3: the word << 2), member 1 from the word >> 6
+//          (P = 3: the word itself)
+//   b = 4: word i; nibble P, P = 0, 1 from the word, 2, 3 from the word >> 8;
+//          p = 0, 4, 0, 4
+//   b = 8: word 2P + floor(i/2); byte i mod 2 (the word, the word >> 8); p = 0
 template <int KB>
-__host__ __device__ constexpr float kKScale() { return KB == 4 ? 16.f : (KB == 2 ? 4.f : 1024.f); }
-
-// PV A operand (rows = d, K index = positions).  Lane gid owns
-// d in [16 gid, 16 gid + 16): m-tile mt row gid <-> d = 16 gid + mt,
-// row gid+8 <-> d = 16 gid + 8 + mt.  Positions: a0/a1 use (2tig, 2tig+1),
-// a2/a3 use (2tig+8, 2tig+9).
-//
-// VData holds one lane's 16 d of 4 positions in the storage format.
-template <int VB>
-struct VData {
-  static constexpr int kWords = VB == 16 ? 8 : VB / 2;  // 32-bit words per position
-  uint32_t w[4][kWords];
-};
-
-template <int VB>
-__device__ __forceinline__ void v_load(const uint8_t* vrows, int row_bytes, int gid, const int (&t)[4],
-                                       VData<VB>& v) {
+__device__ __forceinline__ void k_packed_regs(const uint8_t* row, int tig, uint32_t (&f)[4][4]) {
+  if constexpr (KB == 2) {
+    const uint2 w = lds64(row + 8 * tig);
+    const uint32_t x[2] = {w.x, w.y};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint8_t* r = vrows + t[i] * row_bytes;
-    if constexpr (VB == 2) {
-      v.w[i][0] = lds32(r + 4 * gid);
-    } else if constexpr (VB == 4) {
-      const uint2 x = lds64(r + 8 * gid);
-      v.w[i][0] = x.x;
-      v.w[i][1] = x.y;
-    } else if constexpr (VB == 8) {
-      const uint4 x = lds128(r + 16 * gid);
-      v.w[i][0] = x.x; v.w[i][1] = x.y; v.w[i][2] = x.z; v.w[i][3] = x.w;
-    } else {
-      const uint4 x = lds128(r + 32 * gid);
-      const uint4 y = lds128(r + 32 * gid + 16);
-      v.w[i][0] = x.x; v.w[i][1] = x.y; v.w[i][2] = x.z; v.w[i][3] = x.w;
-      v.w[i][4] = y.x; v.w[i][5] = y.y; v.w[i][6] = y.z; v.w[i][7] = y.w;
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t y = x[h] >> 6, z = x[h] << 2;
+      f[0][2 * h] = x[h] & 0x03000300u;
+      f[0][2 * h + 1] = y & 0x03000300u;
+      f[1][2 * h] = x[h] & 0x00C000C0u;
+      f[1][2 * h + 1] = y & 0x00C000C0u;
+      f[2][2 * h] = x[h] & 0x00300030u;
+      f[2][2 * h + 1] = y & 0x00300030u;
+      f[3][2 * h] = z & 0x000C000Cu;
+      f[3][2 * h + 1] = x[h] & 0x000C000Cu;
     }
-  }
-}
-
-// Code pair (position i0, position i1) for local element e in [0, 16) of the
-// lane's d range, as exact fp16 (bf16 rows: the value itself).
-template <int VB>
-__device__ __forceinline__ uint32_t v_pair(const VData<VB>& v, int i0, int i1, int e) {
-  if constexpr (VB == 2) {
-    const uint32_t x = prmt(v.w[i0][0], v.w[i1][0], e < 8 ? 0x5410u : 0x7632u);
-    return codes_f16(x >> (2 * (e & 7)), 0x00030003u);
-  } else if constexpr (VB == 4) {
-    const int wi = e >> 3, ee = e & 7;
-    const uint32_t x = prmt(v.w[i0][wi], v.w[i1][wi], ee < 4 ? 0x5410u : 0x7632u);
-    return codes_f16(x >> (4 * (ee & 3)), 0x000F000Fu);
-  } else if constexpr (VB == 8) {
-    const int wi = e >> 2, b = e & 3;
-    const uint32_t x = prmt(v.w[i0][wi], v.w[i1][wi], b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12));
-    return codes_f16(x, 0x00FF00FFu);
+  } else if constexpr (KB == 4) {
+    const uint4 w = lds128(row + 16 * tig);
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t y = x[i] >> 8;
+      f[0][i] = x[i] & 0x000F000Fu;
+      f[1][i] = x[i] & 0x00F000F0u;
+      f[2][i] = y & 0x000F000Fu;
+      f[3][i] = y & 0x00F000F0u;
+    }
   } else {
-    const int wi = e >> 1;
-    const bool hi = e & 1;
-    return bf16pair_f16(v.w[i0][wi], hi, v.w[i1][wi], hi);
+    const uint4 a = lds128(row + 32 * tig), b = lds128(row + 32 * tig + 16);
+    const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v = x[2 * P + (i >> 1)];
+        f[P][i] = ((i & 1) ? (v >> 8) : v) & 0x00FF00FFu;
+      }
   }
 }
 
-// ---------------------------------------------------------------------------
-// Consumers
-// ---------------------------------------------------------------------------
+// 2^e as a compile-time float.
+__host__ __device__ constexpr float pow2i(int e) {
+  float r = 1.f;
+  for (int i = 0; i < (e < 0 ? -e : e); ++i) r = e < 0 ? r * 0.5f : r * 2.f;
+  return r;
+}
+
+// Bit offset p of K pair P, and 2^(24 - p) (undoes the subnormal placement).
+template <int KB>
+__host__ __device__ constexpr int kKShift(int P) {
+  return KB == 2 ? 8 - 2 * P : (KB == 4 ? 4 * (P & 1) : 0);
+}
+template <int KB>
+__host__ __device__ constexpr float kKFactor(int P) { return pow2i(24 - kKShift<KB>(P)); }
+
+// V operand registers.  Packed V rows: lane gid reads its slice (slots
+// 16 gid .. 16 gid + 15 = elements d = 16m + 8r + gid, code index k = 2m + r)
+// of the positions of a register pair, merges the two rows' half-words with
+// one PRMT and masks every code in place:
+//   b = 2: half-word floor(k/8), crumb c = k mod 8 at p = 2c (c <= 4) or
+//          from the merged word >> 6 at p = 2c - 6 (c >= 5)
+//   b = 4: half-word floor(k/4), nibble c = k mod 4; c = 0, 1 from the
+//          merged word, 2, 3 from it >> 8; p = 0, 4, 0, 4
+//   b = 8: half-word m, byte r; p = 0
+// Output row (m-tile m, row gid + 8r) <-> element d = 16m + 8r + gid.
+template <int VB>
+__host__ __device__ constexpr int kVShift(int m, int r) {
+  return VB == 2 ? ((2 * m + r) % 8 <= 4 ? 2 * ((2 * m + r) % 8) : 2 * ((2 * m + r) % 8) - 6)
+                 : VB == 4 ? 4 * (r & 1) : 0;
+}
 
 // Online-softmax state of one warp for its unit: m, l for the lane's two
 // query-head columns (2tig, 2tig+1); o^T fragments for 8 m-tiles of d.
+// Packed units with packed V keep, while in "packed" accumulation, o rows
+// in units of 2^(p - 24) of the row's V codes times scales, and zo (an MMA
+// fragment: row = group, columns = heads) the sum of p * z per group.
 struct Acc {
   float m[2], l[2];
   float o[8][4];
+  float zo[4];
 };
 
 // Both halves of a half2 register as floats (the split is a register view).
@@ -329,103 +317,122 @@ __device__ __forceinline__ void h2_to_f2(uint32_t w, float& lo, float& hi) {
       : "r"(w));
 }
 
-// QK for one 16-row half [r0, r0 + 16) of a block: S[i] for rows
-// (gid, gid, gid+8, gid+8) x heads (2tig, 2tig+1, 2tig, 2tig+1), log2 units.
-template <int KB, int G>
-__device__ __forceinline__ void qk_half(const uint8_t* kc, const uint8_t* ksz, int r0, float sl2,
-                                        const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
-                                        int tig, float (&S)[4]) {
-  constexpr int KROW = KB * kD / 8;
-  constexpr int SZROW = 4 * (kD / G);
-  const uint8_t* krow0 = kc + (r0 + gid) * KROW;
-  const uint8_t* krow1 = krow0 + 8 * KROW;
-  // One accumulator per k-step pair keeps the MMA dependency chains short.
+// QK for one 16-row half [r0, r0 + 16) of a block of bf16 K rows: S[i] for
+// rows (gid, gid, gid+8, gid+8) x heads (2tig, 2tig+1, 2tig, 2tig+1), log2
+// units.
+__device__ __forceinline__ void qk_bf16(const uint8_t* kc, int r0, float sl2, const uint32_t (&qb)[8][2],
+                                        int gid, int tig, float (&S)[4]) {
+  const uint8_t* krow0 = kc + (r0 + gid) * (2 * kD);
+  const uint8_t* krow1 = krow0 + 8 * (2 * kD);
   float C[4][4];
 #pragma unroll
   for (int P = 0; P < 4; ++P) {
     C[P][0] = C[P][1] = C[P][2] = C[P][3] = 0.f;
     uint32_t f0[4], f1[4];
-    k_row_pairs<KB>(krow0, P, tig, f0);
-    k_row_pairs<KB>(krow1, P, tig, f1);
+    k_bf16_pairs(krow0, P, tig, f0);
+    k_bf16_pairs(krow1, P, tig, f1);
     const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
     const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
     mma_f16(C[P], A0, qb[2 * P][0], qb[2 * P][1]);
     mma_f16(C[P], A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
   }
-  if constexpr (KB == 16) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[i] = ((C[0][i] + C[1][i]) + (C[2][i] + C[3][i])) * sl2;
-  } else {
-    // Sum the pairs of each quantisation group, then apply its scale/zero:
-    // sum q c = 2^m (sum q v - sum q), so 2^m s multiplies the group's sum
-    // and (z - 2^m s) multiplies the group's q sum (qsP[P] for any pair P of it).
-    constexpr int PPG = G / 32;
+  for (int i = 0; i < 4; ++i) S[i] = ((C[0][i] + C[1][i]) + (C[2][i] + C[3][i])) * sl2;
+}
+
+// QK for one 16-row half of packed K rows.  Per quantisation group g:
+//   q . k_hat = s_g * sum_g q c + z_g * sum_g q,  sum_g q c = 2^(24-p) * (MMA)
+// The scale/zero row is fp16 [z_0 .., s_0 ..].
+template <int KB, int G>
+__device__ __forceinline__ void qk_packed(const uint8_t* kc, const uint8_t* ksz, int r0, float sl2,
+                                          const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
+                                          int tig, float (&S)[4]) {
+  constexpr int KROW = KB * kD / 8;
+  constexpr int NG = kD / G;
+  constexpr int SZROW = 4 * NG;
+  constexpr int PPG = G / 32;
+  uint32_t f0[4][4], f1[4][4];
+  k_packed_regs<KB>(kc + (r0 + gid) * KROW, tig, f0);
+  k_packed_regs<KB>(kc + (r0 + gid + 8) * KROW, tig, f1);
+  float C[4][4];
 #pragma unroll
-    for (int P = 0; P < 4; ++P) {
-      if (P % PPG != 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) C[P - P % PPG][i] += C[P][i];
-      }
+  for (int P = 0; P < 4; ++P) {
+    C[P][0] = C[P][1] = C[P][2] = C[P][3] = 0.f;
+    const uint32_t A0[4] = {f0[P][0], f1[P][0], f0[P][1], f1[P][1]};
+    const uint32_t A1[4] = {f0[P][2], f1[P][2], f0[P][3], f1[P][3]};
+    mma_f16(C[P], A0, qb[2 * P][0], qb[2 * P][1]);
+    mma_f16(C[P], A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
+  }
+  // z and s of rows gid and gid + 8 as floats: zs[row][0..NG-1] = z, [NG..] = s
+  float zs0[2 * NG], zs1[2 * NG];
+  {
+    const uint8_t* p0 = ksz + (r0 + gid) * SZROW;
+    const uint8_t* p1 = p0 + 8 * SZROW;
+    if constexpr (NG == 4) {
+      const uint4 a = lds128(p0), b = lds128(p1);
+      h2_to_f2(a.x, zs0[0], zs0[1]); h2_to_f2(a.y, zs0[2], zs0[3]);
+      h2_to_f2(a.z, zs0[4], zs0[5]); h2_to_f2(a.w, zs0[6], zs0[7]);
+      h2_to_f2(b.x, zs1[0], zs1[1]); h2_to_f2(b.y, zs1[2], zs1[3]);
+      h2_to_f2(b.z, zs1[4], zs1[5]); h2_to_f2(b.w, zs1[6], zs1[7]);
+    } else if constexpr (NG == 2) {
+      const uint2 a = lds64(p0), b = lds64(p1);
+      h2_to_f2(a.x, zs0[0], zs0[1]); h2_to_f2(a.y, zs0[2], zs0[3]);
+      h2_to_f2(b.x, zs1[0], zs1[1]); h2_to_f2(b.y, zs1[2], zs1[3]);
+    } else {
+      h2_to_f2(lds32(p0), zs0[0], zs0[1]);
+      h2_to_f2(lds32(p1), zs1[0], zs1[1]);
     }
-    const uint8_t* sz0p = ksz + (r0 + gid) * SZROW;
-    const uint8_t* sz1p = sz0p + 8 * SZROW;
-    const float sc = kKScale<KB>() * sl2;
-    S[0] = S[1] = S[2] = S[3] = 0.f;
+  }
+  S[0] = S[1] = S[2] = S[3] = 0.f;
 #pragma unroll
-    for (int g = 0; g < 4 / PPG; ++g) {
-      const int P = g * PPG;
-      float s0, z0, s1, z1;
-      h2_to_f2(lds32(sz0p + 4 * g), s0, z0);
-      h2_to_f2(lds32(sz1p + 4 * g), s1, z1);
-      s0 *= sc;
-      s1 *= sc;
-      z0 = fmaf(z0, sl2, -s0);
-      z1 = fmaf(z1, sl2, -s1);
-      S[0] = fmaf(s0, C[P][0], fmaf(z0, qsP[P][0], S[0]));
-      S[1] = fmaf(s0, C[P][1], fmaf(z0, qsP[P][1], S[1]));
-      S[2] = fmaf(s1, C[P][2], fmaf(z1, qsP[P][0], S[2]));
-      S[3] = fmaf(s1, C[P][3], fmaf(z1, qsP[P][1], S[3]));
+  for (int g = 0; g < NG; ++g) {
+    const int P0 = g * PPG;
+    float Cg[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      Cg[i] = C[P0][i] * kKFactor<KB>(P0);
+#pragma unroll
+      for (int k = 1; k < PPG; ++k) Cg[i] = fmaf(C[P0 + k][i], kKFactor<KB>(P0 + k), Cg[i]);
     }
+    const float s0 = zs0[NG + g] * sl2, s1 = zs1[NG + g] * sl2;
+    const float z0 = zs0[g] * sl2, z1 = zs1[g] * sl2;
+    S[0] = fmaf(s0, Cg[0], fmaf(z0, qsP[P0][0], S[0]));
+    S[1] = fmaf(s0, Cg[1], fmaf(z0, qsP[P0][1], S[1]));
+    S[2] = fmaf(s1, Cg[2], fmaf(z1, qsP[P0][0], S[2]));
+    S[3] = fmaf(s1, Cg[3], fmaf(z1, qsP[P0][1], S[3]));
   }
 }
 
-// PV for one 16-row half: O^T += V^T P^T with the half's P^T fragments.
-template <int VB, int G>
-__device__ __forceinline__ void pv_half(const uint8_t* vc, const uint8_t* vsz, int r0, int n,
-                                        uint32_t pb0, uint32_t pb1, int gid, int tig, Acc& acc) {
-  constexpr int VROW = VB * kD / 8;
-  constexpr int SZROW = 4 * (kD / G);
+// Masks of the halves of a position pair (t, t+1) that lie below n.
+__device__ __forceinline__ uint32_t pair_mask(int t, int n) {
+  return (t < n ? 0x0000ffffu : 0u) | (t + 1 < n ? 0xffff0000u : 0u);
+}
+
+// PV for one 16-row half, bf16 V rows, output rows d = 16 gid + mt (row gid)
+// and 16 gid + 8 + mt (row gid + 8) -- the protected-unit mapping.
+__device__ __forceinline__ void pv_bf16_lanecols(const uint8_t* vc, int r0, int n, uint32_t pb0,
+                                                 uint32_t pb1, int gid, int tig, Acc& acc) {
   const int t[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
-  VData<VB> v;
-  v_load<VB>(vc, VROW, gid, t, v);
-  uint32_t s2a = 0, z2a = 0, s2c = 0, z2c = 0;
-  if constexpr (VB < 16) {
-    const uint8_t* vg = vsz + 4 * ((16 * gid) / G) + r0 * SZROW + 2 * tig * SZROW;
-    const uint32_t sa = lds32(vg), sb = lds32(vg + SZROW);
-    const uint32_t sc = lds32(vg + 8 * SZROW), sd = lds32(vg + 9 * SZROW);
-    s2a = prmt(sa, sb, 0x5410u);
-    z2a = prmt(sa, sb, 0x7632u);
-    s2c = prmt(sc, sd, 0x5410u);
-    z2c = prmt(sc, sd, 0x7632u);
+  uint32_t w[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t* r = vc + t[i] * (2 * kD) + 32 * gid;
+    const uint4 x = lds128(r), y = lds128(r + 16);
+    w[i][0] = x.x; w[i][1] = x.y; w[i][2] = x.z; w[i][3] = x.w;
+    w[i][4] = y.x; w[i][5] = y.y; w[i][6] = y.z; w[i][7] = y.w;
   }
   // Rows past n hold stale shared memory (possibly NaN/Inf patterns): zero
   // their V operands so that 0 * garbage cannot reach the accumulators.
   const bool ragged = r0 + 16 > n;
-  uint32_t ma = 0xffffffffu, mc = 0xffffffffu;
-  if (ragged) {
-    ma = (t[0] < n ? 0x0000ffffu : 0u) | (t[1] < n ? 0xffff0000u : 0u);
-    mc = (t[2] < n ? 0x0000ffffu : 0u) | (t[3] < n ? 0xffff0000u : 0u);
-  }
+  const uint32_t ma = ragged ? pair_mask(t[0], n) : 0xffffffffu;
+  const uint32_t mc = ragged ? pair_mask(t[2], n) : 0xffffffffu;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    uint32_t A[4] = {v_pair<VB>(v, 0, 1, mt), v_pair<VB>(v, 0, 1, 8 + mt), v_pair<VB>(v, 2, 3, mt),
-                     v_pair<VB>(v, 2, 3, 8 + mt)};
-    if constexpr (VB < 16) {
-      A[0] = hfma2_u(A[0], s2a, z2a);
-      A[1] = hfma2_u(A[1], s2a, z2a);
-      A[2] = hfma2_u(A[2], s2c, z2c);
-      A[3] = hfma2_u(A[3], s2c, z2c);
-    }
+    const int e0 = mt, e1 = 8 + mt;  // local elements of rows gid, gid + 8
+    uint32_t A[4] = {bf16pair_f16(w[0][e0 >> 1], e0 & 1, w[1][e0 >> 1], e0 & 1),
+                     bf16pair_f16(w[0][e1 >> 1], e1 & 1, w[1][e1 >> 1], e1 & 1),
+                     bf16pair_f16(w[2][e0 >> 1], e0 & 1, w[3][e0 >> 1], e0 & 1),
+                     bf16pair_f16(w[2][e1 >> 1], e1 & 1, w[3][e1 >> 1], e1 & 1)};
     if (ragged) {
       A[0] &= ma;
       A[1] &= ma;
@@ -436,18 +443,190 @@ __device__ __forceinline__ void pv_half(const uint8_t* vc, const uint8_t* vsz, i
   }
 }
 
+// ldmatrix .x4 .trans: four transposed 8x8 b16 tiles; lane L supplies the
+// row address of tile L / 8.
+__device__ __forceinline__ void ldsm_x4_trans(const uint8_t* addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(addr)));
+}
+
+// PV for one 16-row half, bf16 V rows, packed-unit mapping (output row
+// gid + 8r of m-tile m <-> d = 16m + 8r + gid): the V^T operand of m-tile m
+// is the transpose of V[t0 .. t0+15][16m .. 16m+15], loaded with ldmatrix.
+__device__ __forceinline__ void pv_bf16_dcols(const uint8_t* vc, int r0, int n, uint32_t pb0, uint32_t pb1,
+                                              int tig, int lane, Acc& acc) {
+  const uint8_t* base = vc + (r0 + (lane & 7) + ((lane >> 4) & 1) * 8) * (2 * kD) + ((lane >> 3) & 1) * 16;
+  const bool ragged = r0 + 16 > n;
+  const uint32_t ma = ragged ? pair_mask(r0 + 2 * tig, n) : 0xffffffffu;
+  const uint32_t mc = ragged ? pair_mask(r0 + 2 * tig + 8, n) : 0xffffffffu;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    uint32_t r[4];
+    ldsm_x4_trans(base + 32 * m, r);
+    uint32_t A[4] = {bf16x2_f16x2(r[0]) & ma, bf16x2_f16x2(r[1]) & ma, bf16x2_f16x2(r[2]) & mc,
+                     bf16x2_f16x2(r[3]) & mc};
+    mma_f16(acc.o[m], A, pb0, pb1);
+  }
+}
+
+// PV for one 16-row half of packed V rows (packed accumulation):
+//   sum_t p_t v_hat_td = 2^(24-p_d) * sum_t (c_td 2^(p_d-24)) (s_tg p_t) + sum_t z_tg p_t
+// The first sum runs on the tensor cores with B = s * P^T per group; the
+// second accumulates into zo by one more MMA (rows = groups, A = z).
+template <int VB, int G>
+__device__ __forceinline__ void pv_packed(const uint8_t* vc, const uint8_t* vsz, int r0, int n,
+                                          uint32_t pb0, uint32_t pb1, int gid, int tig, Acc& acc) {
+  constexpr int VROW = VB * kD / 8;
+  constexpr int SLICE = 2 * VB;  // bytes of a lane slice
+  constexpr int NG = kD / G;
+  constexpr int SZROW = 4 * NG;
+  const int t[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
+  const bool ragged = r0 + 16 > n;
+  const uint32_t ma = ragged ? pair_mask(t[0], n) : 0xffffffffu;
+  const uint32_t mc = ragged ? pair_mask(t[2], n) : 0xffffffffu;
+  // scale/zero rows of the four positions
+  uint32_t sz[4][(2 * NG + 1) / 2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t* p = vsz + t[i] * SZROW;
+    if constexpr (NG == 4) {
+      const uint4 a = lds128(p);
+      sz[i][0] = a.x; sz[i][1] = a.y; sz[i][2] = a.z; sz[i][3] = a.w;
+    } else if constexpr (NG == 2) {
+      const uint2 a = lds64(p);
+      sz[i][0] = a.x; sz[i][1] = a.y;
+    } else {
+      sz[i][0] = lds32(p);
+    }
+  }
+  // fp16 halves: z_g at half g, s_g at half NG + g
+  auto half_sel = [](int h) { return (h & 1) ? 0x7632u : 0x5410u; };
+  uint32_t b0[NG], b1[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int hs = NG + g;
+    const uint32_t sa = prmt(sz[0][hs >> 1], sz[1][hs >> 1], half_sel(hs)) & ma;
+    const uint32_t sc = prmt(sz[2][hs >> 1], sz[3][hs >> 1], half_sel(hs)) & mc;
+    b0[g] = hmul2_u(pb0, sa);
+    b1[g] = hmul2_u(pb1, sc);
+  }
+  // zo += Z (rows = groups) x P^T
+  {
+    uint32_t za = 0u, zc = 0u;
+    if (gid < NG) {
+      const int wsel = gid >> 1;
+      const uint32_t w0 = (NG == 4 && wsel) ? sz[0][1] : sz[0][0];
+      const uint32_t w1 = (NG == 4 && wsel) ? sz[1][1] : sz[1][0];
+      const uint32_t w2 = (NG == 4 && wsel) ? sz[2][1] : sz[2][0];
+      const uint32_t w3 = (NG == 4 && wsel) ? sz[3][1] : sz[3][0];
+      za = prmt(w0, w1, half_sel(gid)) & ma;
+      zc = prmt(w2, w3, half_sel(gid)) & mc;
+    }
+    const uint32_t Z[4] = {za, 0u, zc, 0u};
+    mma_f16(acc.zo, Z, pb0, pb1);
+  }
+  // code words of the lane's slice for the four positions
+  constexpr int NW = VB / 2;  // words per slice
+  uint32_t cw[4][NW];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t* p = vc + t[i] * VROW + SLICE * gid;
+    if constexpr (VB == 2) {
+      cw[i][0] = lds32(p);
+    } else if constexpr (VB == 4) {
+      const uint2 a = lds64(p);
+      cw[i][0] = a.x; cw[i][1] = a.y;
+    } else {
+      const uint4 a = lds128(p);
+      cw[i][0] = a.x; cw[i][1] = a.y; cw[i][2] = a.z; cw[i][3] = a.w;
+    }
+  }
+  constexpr int NH = 16 / VB;   // codes per half-word
+  constexpr int MPH = NH / 2;   // m-tiles per half-word (>= 1)
+#pragma unroll
+  for (int h = 0; h < VB; ++h) {  // half-words of the slice
+    const uint32_t xa = prmt(cw[0][h >> 1], cw[1][h >> 1], half_sel(h));
+    const uint32_t xc = prmt(cw[2][h >> 1], cw[3][h >> 1], half_sel(h));
+    const uint32_t ya = VB == 2 ? (xa >> 6) : (xa >> 8);
+    const uint32_t yc = VB == 2 ? (xc >> 6) : (xc >> 8);
+#pragma unroll
+    for (int mm = 0; mm < MPH; ++mm) {
+      const int m = h * MPH + mm;
+      uint32_t A[4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int c = 2 * mm + r;  // code index inside the half-word
+        const bool hi = VB == 2 ? (c >= 5) : (VB == 4 ? (c >= 2) : (c >= 1));
+        const uint32_t mask = (VB == 2 ? 0x00030003u : (VB == 4 ? 0x000F000Fu : 0x00FF00FFu))
+                              << kVShift<VB>(m, r);
+        A[r] = (hi ? ya : xa) & mask;
+        A[2 + r] = (hi ? yc : xc) & mask;
+      }
+      const int g = (16 * m) / G;
+      mma_f16(acc.o[m], A, b0[g], b1[g]);
+    }
+  }
+}
+
+// Switch a packed unit's accumulator between bf16 ("true") rows and packed
+// accumulation.  to_packed: o <- o * 2^(p-24), zo <- 0.  to_true: o <- o *
+// 2^(24-p) + zo[group of the row], zo <- 0 (zo of group g for heads 2tig,
+// 2tig+1 lives in lane 4g + tig).
+template <int VB>
+__device__ __forceinline__ void acc_to_packed(Acc& acc) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float f0 = pow2i(kVShift<VB>(m, 0) - 24);
+    const float f1 = pow2i(kVShift<VB>(m, 1) - 24);
+    acc.o[m][0] *= f0;
+    acc.o[m][1] *= f0;
+    acc.o[m][2] *= f1;
+    acc.o[m][3] *= f1;
+  }
+  acc.zo[0] = acc.zo[1] = acc.zo[2] = acc.zo[3] = 0.f;
+}
+
+template <int VB, int G>
+__device__ __forceinline__ void acc_to_true(Acc& acc, int tig) {
+  constexpr int NG = kD / G;
+  float z0[NG], z1[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    z0[g] = __shfl_sync(0xffffffffu, acc.zo[0], 4 * g + tig);
+    z1[g] = __shfl_sync(0xffffffffu, acc.zo[1], 4 * g + tig);
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float f0 = pow2i(24 - kVShift<VB>(m, 0));
+    const float f1 = pow2i(24 - kVShift<VB>(m, 1));
+    const int g = (16 * m) / G;
+    acc.o[m][0] = fmaf(acc.o[m][0], f0, z0[g]);
+    acc.o[m][1] = fmaf(acc.o[m][1], f0, z1[g]);
+    acc.o[m][2] = fmaf(acc.o[m][2], f1, z0[g]);
+    acc.o[m][3] = fmaf(acc.o[m][3], f1, z1[g]);
+  }
+  acc.zo[0] = acc.zo[1] = acc.zo[2] = acc.zo[3] = 0.f;
+}
+
+// K / V paths of a block.
+enum KPath { kKBf16 = 0, kKPacked = 1 };
+enum VPath { kVBf16Lane = 0, kVBf16D = 1, kVPacked = 2 };
+
 // One 32-position block [r0, r0 + 32) of a staged tile (n valid positions):
 // two 16-row MMA halves sharing one online-softmax update.
-template <int KB, int VB, int G>
+template <int KP, int VP, int KB, int VB, int G>
 __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
                                          const uint8_t* vsz, int r0, int n, float sl2,
                                          const uint32_t (&qb)[8][2], const float (&qsP)[4][2],
-                                         int gid, int tig, Acc& acc) {
+                                         int gid, int tig, int lane, Acc& acc) {
   const bool two = r0 + 16 < n;  // the second half holds valid positions
   float S[2][4];
-  qk_half<KB, G>(kc, ksz, r0, sl2, qb, qsP, gid, tig, S[0]);
+  if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0, sl2, qb, qsP, gid, tig, S[0]);
+  else qk_bf16(kc, r0, sl2, qb, gid, tig, S[0]);
   if (two) {
-    qk_half<KB, G>(kc, ksz, r0 + 16, sl2, qb, qsP, gid, tig, S[1]);
+    if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0 + 16, sl2, qb, qsP, gid, tig, S[1]);
+    else qk_bf16(kc, r0 + 16, sl2, qb, gid, tig, S[1]);
   } else {
     S[1][0] = S[1][1] = S[1][2] = S[1][3] = -INFINITY;
   }
@@ -490,16 +669,21 @@ __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, 
       acc.o[mt][2] *= c0;
       acc.o[mt][3] *= c1;
     }
+    if constexpr (VP == kVPacked) {  // zo is non-zero only during packed accumulation
+      acc.zo[0] *= c0;
+      acc.zo[1] *= c1;
+      acc.zo[2] *= c0;
+      acc.zo[3] *= c1;
+    }
   }
   // P^T as the B operand of PV: transpose the 8x8 quarters.
-  const uint32_t pa0 = movmatrix_trans(pack_f16x2(P[0][0], P[0][1]));
-  const uint32_t pa1 = movmatrix_trans(pack_f16x2(P[0][2], P[0][3]));
-  pv_half<VB, G>(vc, vsz, r0, n, pa0, pa1, gid, tig, acc);
-  if (two) {
-    const uint32_t pc0 = movmatrix_trans(pack_f16x2(P[1][0], P[1][1]));
-    const uint32_t pc1 = movmatrix_trans(pack_f16x2(P[1][2], P[1][3]));
-    pv_half<VB, G>(vc, vsz, r0 + 16, n, pc0, pc1, gid, tig, acc);
-  }
+  auto pv = [&](int h, uint32_t pa0, uint32_t pa1) {
+    if constexpr (VP == kVPacked) pv_packed<VB, G>(vc, vsz, r0 + 16 * h, n, pa0, pa1, gid, tig, acc);
+    else if constexpr (VP == kVBf16D) pv_bf16_dcols(vc, r0 + 16 * h, n, pa0, pa1, tig, lane, acc);
+    else pv_bf16_lanecols(vc, r0 + 16 * h, n, pa0, pa1, gid, tig, acc);
+  };
+  pv(0, movmatrix_trans(pack_f16x2(P[0][0], P[0][1])), movmatrix_trans(pack_f16x2(P[0][2], P[0][3])));
+  if (two) pv(1, movmatrix_trans(pack_f16x2(P[1][0], P[1][1])), movmatrix_trans(pack_f16x2(P[1][2], P[1][3])));
 }
 
 // ---------------------------------------------------------------------------
@@ -665,15 +849,18 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     acc.l[0] = acc.l[1] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) acc.o[mt][0] = acc.o[mt][1] = acc.o[mt][2] = acc.o[mt][3] = 0.f;
+    acc.zo[0] = acc.zo[1] = acc.zo[2] = acc.zo[3] = 0.f;
+    bool packed_acc = false;  // packed accumulation (see Acc); packed units only
 
-    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) {
+    // Wait for a tile; in the fused step the CTA holding the step's row
+    // (the last row of the last text tile) also writes it into the cache.
+    auto begin_tile = [&](int kind, int t0, int n) -> const uint8_t* {
       const int st = it % kStages;
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
       const uint8_t* base = sm.stage[st];
       if (kStep && kind == kTileText && t0 + n == p.plan.T && ui.hc == 0 && warp == 0) {
-        // Write the step's row (staged from the input) into the cache's text
-        // segment: lanes 0-15 the K row, lanes 16-31 the V row.
+        // lanes 0-15 the K row, lanes 16-31 the V row
         const int tr = p.t_new < p.vs ? p.t_new : p.t_new - p.Tv;
         const int64_t row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
         const int half = lane >> 4, q = lane & 15;
@@ -683,23 +870,66 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
                        row * (2 * kD) + 16 * q;
         *reinterpret_cast<uint4*>(dst) = w;
       }
-      const int nb = (n + 31) >> 5;
-      const int first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
-      gblk += nb;
-      for (int kb = first; kb < nb; kb += kConsumerWarps) {
-        if (kind == kTilePacked)
-          kblock32<KB, VB, G>(base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz,
-                              kb * 32, n, sl2, qb, qsP, gid, tig, acc);
-        else
-          kblock32<16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2, qb, qsP, gid,
-                              tig, acc);
-      }
+      return base;
+    };
+    // Release the tile's stage once this warp is done with it.
+    auto end_tile = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[st]);
+      if (lane == 0) mbar_arrive(&sm.empty[it % kStages]);
       ++it;
-    });
+    };
+    // This warp's 32-position blocks of a tile of n rows: first, first + 11, ...
+    auto deal = [&](int n, int& first) {
+      const int nb = (n + 31) >> 5;
+      first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
+      gblk += nb;
+      return nb;
+    };
+    if (ui.prot) {  // protected unit: bf16 rows only
+      walk_piece(p, true, ps, pe, [&](int kind, int t0, int n) {
+        const uint8_t* base = begin_tile(kind, t0, n);
+        int first;
+        const int nb = deal(n, first);
+        for (int kb = first; kb < nb; kb += kConsumerWarps)
+          kblock32<kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
+                                                 qb, qsP, gid, tig, lane, acc);
+        end_tile();
+      });
+    } else {
+      walk_piece(p, false, ps, pe, [&](int kind, int t0, int n) {
+        const uint8_t* base = begin_tile(kind, t0, n);
+        int first;
+        const int nb = deal(n, first);
+        if (kind == kTilePacked) {
+          if constexpr (VB < 16) {
+            if (first < nb && !packed_acc) {
+              acc_to_packed<VB>(acc);
+              packed_acc = true;
+            }
+          }
+          for (int kb = first; kb < nb; kb += kConsumerWarps)
+            kblock32<(KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
+                base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 32, n, sl2, qb,
+                qsP, gid, tig, lane, acc);
+        } else {  // text rows of a packed unit
+          if constexpr (VB < 16) {
+            if (first < nb && packed_acc) {
+              acc_to_true<VB, G>(acc, tig);
+              packed_acc = false;
+            }
+          }
+          for (int kb = first; kb < nb; kb += kConsumerWarps)
+            kblock32<kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
+                                                qb, qsP, gid, tig, lane, acc);
+        }
+        end_tile();
+      });
+    }
 
-    // ---- merge the 4 warps' states and write the partial of (u, c) ----
+    if constexpr (VB < 16) {
+      if (packed_acc) acc_to_true<VB, G>(acc, tig);
+    }
+    // ---- merge the warps' states and write the partial of (u, c) ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], off);
@@ -711,14 +941,20 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       sm.merge_ml[warp][2 * tig + 1][0] = acc.m[1];
       sm.merge_ml[warp][2 * tig + 1][1] = acc.l[1];
     }
+    // output rows: protected units d = 16 gid + mt (+ 8); packed units
+    // d = 16 mt + gid (+ 8) (kept as two compile-time patterns)
+    auto store_rows = [&](int dbase, int dstep) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int d0 = 16 * gid + mt, d1 = d0 + 8;
-      sm.merge_o[warp][2 * tig][d0] = acc.o[mt][0];
-      sm.merge_o[warp][2 * tig + 1][d0] = acc.o[mt][1];
-      sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
-      sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
-    }
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = dbase + dstep * mt, d1 = d0 + 8;
+        sm.merge_o[warp][2 * tig][d0] = acc.o[mt][0];
+        sm.merge_o[warp][2 * tig + 1][d0] = acc.o[mt][1];
+        sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
+        sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
+      }
+    };
+    if (ui.prot) store_rows(16 * gid, 1);
+    else store_rows(gid, 16);
     // The fused step finishes a unit held by this CTA alone right here;
     // otherwise the partial goes to slot u + c.
     int cf = c, cl = c;

@@ -77,7 +77,8 @@ def seg(L, cache_np: np.ndarray, s: int, dtype) -> np.ndarray:
 def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.ndarray,
                  t_hi: int, b_sel: Optional[Sequence[int]] = None) -> int:
     """Every position in [0, t_hi) of the cache against the oracle:
-    packed codes, scales and zeros word-for-word, bf16 rows bit-identical.
+    packed codes (in the cache's storage order), scales and zeros
+    word-for-word, bf16 rows bit-identical.
     k_np/v_np: uint16 [B', H_kv, >= t_hi, D] for the batch entries b_sel.
     Returns the number of packed rows compared."""
     cn = cache.cpu().numpy()
@@ -114,19 +115,19 @@ def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.nda
                 assert np.array_equal(raw[b, :, :nvis], x_np[i][pack][:, c.vs:c.vs + nvis])
             continue
         W = D * nbits // 32
+        ng = D // c.G
         words = seg(L, cn, sc, np.uint32).reshape(B, len(pack), Tvp, W)
-        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pack), Tvp, D // c.G, 2)
+        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pack), Tvp, 2 * ng)
         for i, b in enumerate(b_sel):
             xin = np.ascontiguousarray(x_np[i][pack][:, c.vs:c.vs + nvis])
-            w_ref, s_ref, z_ref = oracle.quantize_pack_rows(xin, c.G, nbits)
+            w_ref, sz_ref = oracle.quantize_pack_rows_stored(xin, c.G, nbits, which)
             got_w = words[b, :, :nvis].reshape(-1, W)
-            got_s = sz[b, :, :nvis, :, 0].reshape(-1, D // c.G)
-            got_z = sz[b, :, :nvis, :, 1].reshape(-1, D // c.G)
+            got_sz = sz[b, :, :nvis].reshape(-1, 2 * ng)
             if not np.array_equal(got_w, w_ref):
                 bad = np.argwhere(got_w != w_ref)[:4]
                 raise AssertionError(f"{which} codes differ b={b} at {bad.tolist()}")
-            assert np.array_equal(got_s, s_ref), f"{which} scales differ b={b}"
-            assert np.array_equal(got_z, z_ref), f"{which} zeros differ b={b}"
+            assert np.array_equal(got_sz[:, ng:], sz_ref[:, ng:]), f"{which} scales differ b={b}"
+            assert np.array_equal(got_sz[:, :ng], sz_ref[:, :ng]), f"{which} zeros differ b={b}"
             n_rows += got_w.shape[0]
     return n_rows
 

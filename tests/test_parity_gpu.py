@@ -238,6 +238,8 @@ def test_quantiser_edge_rows(cuda_dev, kvq):
     x[0, 0, 3, :] *= 1e-3
     x[0, 1, 4, 9] = 60000.0                  # large outlier (inside fp16 range)
     x[0, 1, 5, :] = np.float32(2.0) ** -20   # zero below binary16 normal range
+    x[0, 1, 6, 32:64] = 0.75                 # one constant group inside a varying row
+    x[0, 0, 7, 96:] = -2.5                   # (both tensors, other lanes of the row)
     k = torch.tensor(x).to(torch.bfloat16).to(cuda_dev)
     v = k.flip(2).contiguous()
     L = c.layout()
