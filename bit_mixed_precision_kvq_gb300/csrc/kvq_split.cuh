@@ -342,10 +342,14 @@ __device__ __forceinline__ void qk_bf16(const uint8_t* kc, int r0, float sl2, co
 
 // QK for one 16-row half of packed K rows.  Per quantisation group g:
 //   q . k_hat = s_g * sum_g q c + z_g * sum_g q,  sum_g q c = 2^(24-p) * (MMA)
+// The z-term runs on the tensor cores too: A = the rows' z (fp16, rows =
+// positions, K index = group), B = zb = sl2 * 2^-6 * (sum of q over each
+// group) as an fp16 hi + lo pair (two MMAs, ~22 bits), scaled back by 2^6.
 // The scale/zero row is fp16 [z_0 .., s_0 ..].
+constexpr float kZbScale = 64.f;  // zb holds the q sums / 64 (fp16 range)
 template <int KB, int G>
 __device__ __forceinline__ void qk_packed(const uint8_t* kc, const uint8_t* ksz, int r0, float sl2,
-                                          const uint32_t (&qb)[8][2], const float (&qsP)[4][2], int gid,
+                                          const uint32_t (&qb)[8][2], const uint32_t (&zb)[2], int gid,
                                           int tig, float (&S)[4]) {
   constexpr int KROW = KB * kD / 8;
   constexpr int NG = kD / G;
@@ -363,43 +367,58 @@ __device__ __forceinline__ void qk_packed(const uint8_t* kc, const uint8_t* ksz,
     mma_f16(C[P], A0, qb[2 * P][0], qb[2 * P][1]);
     mma_f16(C[P], A1, qb[2 * P + 1][0], qb[2 * P + 1][1]);
   }
-  // z and s of rows gid and gid + 8 as floats: zs[row][0..NG-1] = z, [NG..] = s
-  float zs0[2 * NG], zs1[2 * NG];
+  const uint8_t* p0 = ksz + (r0 + gid) * SZROW;
+  const uint8_t* p1 = p0 + 8 * SZROW;
+  // z-term
+  float Z[4] = {0.f, 0.f, 0.f, 0.f};
   {
-    const uint8_t* p0 = ksz + (r0 + gid) * SZROW;
-    const uint8_t* p1 = p0 + 8 * SZROW;
-    if constexpr (NG == 4) {
-      const uint4 a = lds128(p0), b = lds128(p1);
-      h2_to_f2(a.x, zs0[0], zs0[1]); h2_to_f2(a.y, zs0[2], zs0[3]);
-      h2_to_f2(a.z, zs0[4], zs0[5]); h2_to_f2(a.w, zs0[6], zs0[7]);
-      h2_to_f2(b.x, zs1[0], zs1[1]); h2_to_f2(b.y, zs1[2], zs1[3]);
-      h2_to_f2(b.z, zs1[4], zs1[5]); h2_to_f2(b.w, zs1[6], zs1[7]);
-    } else if constexpr (NG == 2) {
-      const uint2 a = lds64(p0), b = lds64(p1);
-      h2_to_f2(a.x, zs0[0], zs0[1]); h2_to_f2(a.y, zs0[2], zs0[3]);
-      h2_to_f2(b.x, zs1[0], zs1[1]); h2_to_f2(b.y, zs1[2], zs1[3]);
-    } else {
-      h2_to_f2(lds32(p0), zs0[0], zs0[1]);
-      h2_to_f2(lds32(p1), zs1[0], zs1[1]);
+    uint32_t za = 0u, zc = 0u;
+    if (tig < (NG + 1) / 2) {  // z halves 2 tig, 2 tig + 1
+      za = lds32(p0 + 4 * tig);
+      zc = lds32(p1 + 4 * tig);
+      if constexpr (NG == 1) {  // the word's high half is s_0
+        za &= 0x0000ffffu;
+        zc &= 0x0000ffffu;
+      }
     }
+    const uint32_t A[4] = {za, zc, 0u, 0u};
+    mma_f16(Z, A, zb[0], 0u);
+    mma_f16(Z, A, zb[1], 0u);
   }
-  S[0] = S[1] = S[2] = S[3] = 0.f;
+  // scales of rows gid and gid + 8
+  float s0f[NG], s1f[NG];
+  if constexpr (NG == 4) {
+    const uint2 a = lds64(p0 + 8), b = lds64(p1 + 8);
+    h2_to_f2(a.x, s0f[0], s0f[1]);
+    h2_to_f2(a.y, s0f[2], s0f[3]);
+    h2_to_f2(b.x, s1f[0], s1f[1]);
+    h2_to_f2(b.y, s1f[2], s1f[3]);
+  } else if constexpr (NG == 2) {
+    h2_to_f2(lds32(p0 + 4), s0f[0], s0f[1]);
+    h2_to_f2(lds32(p1 + 4), s1f[0], s1f[1]);
+  } else {
+    float zz;
+    h2_to_f2(lds32(p0), zz, s0f[0]);
+    h2_to_f2(lds32(p1), zz, s1f[0]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S[i] = Z[i] * kZbScale;
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int P0 = g * PPG;
     float Cg[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      Cg[i] = C[P0][i] * kKFactor<KB>(P0);
+      Cg[i] = C[P0][i];
 #pragma unroll
-      for (int k = 1; k < PPG; ++k) Cg[i] = fmaf(C[P0 + k][i], kKFactor<KB>(P0 + k), Cg[i]);
+      for (int k = 1; k < PPG; ++k) Cg[i] = fmaf(C[P0 + k][i], kKFactor<KB>(P0 + k) / kKFactor<KB>(P0), Cg[i]);
     }
-    const float s0 = zs0[NG + g] * sl2, s1 = zs1[NG + g] * sl2;
-    const float z0 = zs0[g] * sl2, z1 = zs1[g] * sl2;
-    S[0] = fmaf(s0, Cg[0], fmaf(z0, qsP[P0][0], S[0]));
-    S[1] = fmaf(s0, Cg[1], fmaf(z0, qsP[P0][1], S[1]));
-    S[2] = fmaf(s1, Cg[2], fmaf(z1, qsP[P0][0], S[2]));
-    S[3] = fmaf(s1, Cg[3], fmaf(z1, qsP[P0][1], S[3]));
+    const float kf = sl2 * kKFactor<KB>(P0);
+    const float a0 = s0f[g] * kf, a1 = s1f[g] * kf;
+    S[0] = fmaf(a0, Cg[0], S[0]);
+    S[1] = fmaf(a0, Cg[1], S[1]);
+    S[2] = fmaf(a1, Cg[2], S[2]);
+    S[3] = fmaf(a1, Cg[3], S[3]);
   }
 }
 
@@ -506,8 +525,12 @@ __device__ __forceinline__ void pv_packed(const uint8_t* vc, const uint8_t* vsz,
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int hs = NG + g;
-    const uint32_t sa = prmt(sz[0][hs >> 1], sz[1][hs >> 1], half_sel(hs)) & ma;
-    const uint32_t sc = prmt(sz[2][hs >> 1], sz[3][hs >> 1], half_sel(hs)) & mc;
+    uint32_t sa = prmt(sz[0][hs >> 1], sz[1][hs >> 1], half_sel(hs));
+    uint32_t sc = prmt(sz[2][hs >> 1], sz[3][hs >> 1], half_sel(hs));
+    if (ragged) {
+      sa &= ma;
+      sc &= mc;
+    }
     b0[g] = hmul2_u(pb0, sa);
     b1[g] = hmul2_u(pb1, sc);
   }
@@ -520,8 +543,12 @@ __device__ __forceinline__ void pv_packed(const uint8_t* vc, const uint8_t* vsz,
       const uint32_t w1 = (NG == 4 && wsel) ? sz[1][1] : sz[1][0];
       const uint32_t w2 = (NG == 4 && wsel) ? sz[2][1] : sz[2][0];
       const uint32_t w3 = (NG == 4 && wsel) ? sz[3][1] : sz[3][0];
-      za = prmt(w0, w1, half_sel(gid)) & ma;
-      zc = prmt(w2, w3, half_sel(gid)) & mc;
+      za = prmt(w0, w1, half_sel(gid));
+      zc = prmt(w2, w3, half_sel(gid));
+      if (ragged) {
+        za &= ma;
+        zc &= mc;
+      }
     }
     const uint32_t Z[4] = {za, 0u, zc, 0u};
     mma_f16(acc.zo, Z, pb0, pb1);
@@ -618,14 +645,14 @@ enum VPath { kVBf16Lane = 0, kVBf16D = 1, kVPacked = 2 };
 template <int KP, int VP, int KB, int VB, int G>
 __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
                                          const uint8_t* vsz, int r0, int n, float sl2,
-                                         const uint32_t (&qb)[8][2], const float (&qsP)[4][2],
+                                         const uint32_t (&qb)[8][2], const uint32_t (&zb)[2],
                                          int gid, int tig, int lane, Acc& acc) {
   const bool two = r0 + 16 < n;  // the second half holds valid positions
   float S[2][4];
-  if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0, sl2, qb, qsP, gid, tig, S[0]);
+  if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0, sl2, qb, zb, gid, tig, S[0]);
   else qk_bf16(kc, r0, sl2, qb, gid, tig, S[0]);
   if (two) {
-    if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0 + 16, sl2, qb, qsP, gid, tig, S[1]);
+    if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0 + 16, sl2, qb, zb, gid, tig, S[1]);
     else qk_bf16(kc, r0 + 16, sl2, qb, gid, tig, S[1]);
   } else {
     S[1][0] = S[1][1] = S[1][2] = S[1][3] = -INFINITY;
@@ -832,16 +859,26 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       for (int P = 0; P < 4; ++P) sm.qsum[warp][gid][P] = qpart[P];
     }
     __syncwarp();
-    float qsP[4][2];  // sum of q over the quantisation group of k-step pair P
-#pragma unroll
-    for (int P = 0; P < 4; ++P) {
-      const int g0 = (P / ppg) * ppg;
+    // zb: B operand of the K z-term MMA -- (k = groups 2 tig, 2 tig + 1, n =
+    // head gid) of sl2 / 64 * (sum of q over the group), as hi + lo fp16.
+    uint32_t zb[2];
+    {
+      constexpr int NG = kD / G;
+      float x[2] = {0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        float s = 0.f;
-        for (int i = 0; i < ppg; ++i) s += sm.qsum[warp][2 * tig + cc][g0 + i];
-        qsP[P][cc] = s;
+        const int g = 2 * tig + cc;
+        if (g < NG) {
+          float s = 0.f;
+#pragma unroll
+          for (int i = 0; i < ppg; ++i) s += sm.qsum[warp][gid][g * ppg + i];
+          x[cc] = s * (sl2 / kZbScale);
+        }
       }
+      zb[0] = pack_f16x2(x[0], x[1]);
+      float h0, h1;
+      h2_to_f2(zb[0], h0, h1);
+      zb[1] = pack_f16x2(x[0] - h0, x[1] - h1);
     }
 
     Acc acc;
@@ -892,7 +929,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         const int nb = deal(n, first);
         for (int kb = first; kb < nb; kb += kConsumerWarps)
           kblock32<kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
-                                                 qb, qsP, gid, tig, lane, acc);
+                                                 qb, zb, gid, tig, lane, acc);
         end_tile();
       });
     } else {
@@ -910,7 +947,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           for (int kb = first; kb < nb; kb += kConsumerWarps)
             kblock32<(KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
                 base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 32, n, sl2, qb,
-                qsP, gid, tig, lane, acc);
+                zb, gid, tig, lane, acc);
         } else {  // text rows of a packed unit
           if constexpr (VB < 16) {
             if (first < nb && packed_acc) {
@@ -920,7 +957,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
             kblock32<kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
-                                                qb, qsP, gid, tig, lane, acc);
+                                                qb, zb, gid, tig, lane, acc);
         }
         end_tile();
       });
