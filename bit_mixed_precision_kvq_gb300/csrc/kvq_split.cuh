@@ -43,6 +43,7 @@ constexpr int kStages = 5;
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
+constexpr uint32_t kPrefetchBytes = kStageBytes;  // L2 prefetch before the dependency wait
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
 constexpr uint32_t kSpinPolls = 1u << 21;      // bounded inter-CTA wait (fused step)
 
@@ -139,12 +140,13 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   }
 }
 
-// Before griddepcontrol.wait: pull the first kStages stages' worth of the
-// CTA's cache rows into L2.  L2 is coherent with every SM's stores, so a
+// Before griddepcontrol.wait: pull the first stage's worth of the CTA's
+// cache rows into L2 (more only delays the first tile and q behind the
+// other SMs' prefetches when the previous kernel does not overlap).  L2 is coherent with every SM's stores, so a
 // line that the previous kernel writes later is simply updated there; the
 // copies into shared memory all come after the wait.
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
-  uint32_t budget = kStages * kStageBytes;
+  uint32_t budget = kPrefetchBytes;
   walk_chunk(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
     if (budget == 0) return;
     tile_sources<false>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
