@@ -7,9 +7,9 @@
 // heads keep their visual K and V in bf16.
 //
 // One warp per (b, h, 8 consecutive positions): 4 lanes per D = 128 row,
-// each lane owning 32 consecutive elements (a whole group for G = 32; for
-// G = 64 / 128 the 2 / 4 lanes of a group combine min and max with
-// shuffles).  The arithmetic is the fp32 spec the
+// each lane owning the 32 elements of its slice of the stored row (group
+// min and max combine over the row's 4 lanes with shuffles).  The
+// arithmetic is the fp32 spec the
 // oracle restates: r = max - min (RN), s = fp16(r / (2^b - 1)) (IEEE div),
 // z = fp16(min + 0), code = clamp(rint((x - z) / s), 0, 2^b - 1) using the
 // stored s and z, code 0 if s == 0.  Intrinsics pin every rounding so that
@@ -30,177 +30,141 @@ struct AppendArgs {
   int32_t t0, n_tok;
 };
 
-constexpr int kLaneElems = 32;                      // consecutive elements of a row per lane
-constexpr int kLanesPerRow = kD / kLaneElems;       // 4
+constexpr int kLanesPerRow = 4;                     // lanes per D = 128 row
+
 constexpr int kRowsPerWarp = 32 / kLanesPerRow;     // 8
 
 // The correctly rounded quotient, kept out of line: it is needed only for
 // near-ties.
 __device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
 
-// Value of blk[sel] for a runtime sel in [0, 4) without local memory.
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&blk)[4], int sel) {
-  const uint32_t lo = (sel & 1) ? blk[1] : blk[0];
-  const uint32_t hi = (sel & 1) ? blk[3] : blk[2];
-  return (sel & 2) ? hi : lo;
+// The row's 4 lanes each own one slice of the stored row (kvq.h storage
+// order): K slice t = elements d = 32P + 8t + j (P = 0..3, j = 0..7); V
+// slices 2l, 2l + 1 = elements d = 16m + 8r + 2l + n' (m = 0..7, r, n' =
+// 0, 1).  A lane loads exactly those elements, as 4 chunks of 8 (chunk k =
+// 32-element block k of the row for K; m in {2k, 2k+1} for V, so chunk k
+// lies in quantisation group k / (G/32) either way), quantises them and
+// packs its slice words without any exchange.  w[k][q] holds elements
+// j = 2q, 2q + 1 of chunk k (K: d = 32k + 8t + j; V: q = 2m' + r, m = 2k + m',
+// n' = j mod 2).
+//
+// Destination of element j = 4e + i (K) / j = 2q + n' (V) of chunk k:
+//   K b = 2: word floor(i/2), bit 16e + 2 c(k, i mod 2), c = {4,7},{3,6},{2,5},{0,1}
+//   K b = 4: word i,          bit 16e + 4k
+//   K b = 8: word 2k + floor(i/2), bit 16e + 8 (i mod 2)
+//   V b = 2: word n',              bit 8k + 2q
+//   V b = 4: word 2n' + floor(k/2), bit 16 (k mod 2) + 4q
+//   V b = 8: word 4n' + k,          bit 8q
+template <int BITS, bool kV>
+__device__ __forceinline__ int dst_word(int k, int j) {
+  if constexpr (!kV) {
+    const int i = j & 3;
+    return BITS == 2 ? (i >> 1) : (BITS == 4 ? i : 2 * k + (i >> 1));
+  } else {
+    const int n = j & 1;
+    return BITS == 2 ? n : (BITS == 4 ? 2 * n + (k >> 1) : 4 * n + k);
+  }
+}
+template <int BITS, bool kV>
+__device__ __forceinline__ int dst_bit(int k, int j) {
+  if constexpr (!kV) {
+    const int e = j >> 2, i = j & 3;
+    if constexpr (BITS == 2) {
+      const int c = k == 0 ? ((i & 1) ? 7 : 4) : k == 1 ? ((i & 1) ? 6 : 3) : k == 2 ? ((i & 1) ? 5 : 2) : (i & 1);
+      return 16 * e + 2 * c;
+    }
+    return BITS == 4 ? 16 * e + 4 * k : 16 * e + 8 * (i & 1);
+  } else {
+    const int q = j >> 1;
+    return BITS == 2 ? 8 * k + 2 * q : (BITS == 4 ? 16 * (k & 1) + 4 * q : 8 * q);
+  }
 }
 
-// Quantise the lane's 32 elements (16 bf16 pairs in w[]) of one row and
-// store them in the cache's storage order (slot sigma(d) of the row, see
-// kvq.h).  The lane (part) owns elements d = 32 part + e, e in [0, 32).  Its
-// codes land in every lane's slice of the row, so each lane first builds,
-// for each of the row's 4 lanes, the words of that lane's slice with its own
-// codes already in place (zeros elsewhere); a 4-lane exchange (3 xor-shuffle
-// rounds) then gives every lane the pieces of its own slice, which it ORs
-// and stores.
-//   K, d = 32P + 8t + 4e' + i (P = part): slice t (slots 32t ..) belongs to
-//     lane t.  Code (t, e', i) goes to slice word / bit
-//       b = 2: word floor(i/2), bit 16e' + 2c(P, i mod 2)
-//       b = 4: word i,          bit 16e' + 4P
-//       b = 8: word 2P + floor(i/2), bit 16e' + 8 (i mod 2)
-//   V, d = 16m + 8r + n (m = 2 part + m'): slices 2l, 2l+1 (slots 16n ..)
-//     belong to lane l = floor(n/2).  Code (m', r, n) goes to bit
-//       b = 2: 8 part + 2c'            of the slice's word
-//       b = 4: 16 (part mod 2) + 4c'   of the slice's word floor(part/2)
-//       b = 8: 8c'                     of the slice's word part
-//     with c' = 2m' + r.
+// Quantise the lane's 32 elements (4 chunks of 8, see above) and store its
+// slice words and, for the groups this lane is responsible for, z and s.
 // `gmask` = the 4 lanes of this row (shuffle partners).
-template <int BITS, bool kV>
-__device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, int part, uint32_t gmask,
+template <int BITS, bool kV, int G>
+__device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int part, uint32_t gmask,
                                               uint8_t* codes_row, uint8_t* sz_row) {
-  // group min / max over the lane's elements (packed bf16 pairs), then over
-  // the lanes of the group
-  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
-  __nv_bfloat162 mx2 = mn2;
-#pragma unroll
-  for (int i = 1; i < 16; ++i) {
-    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    mn2 = __hmin2(mn2, v);
-    mx2 = __hmax2(mx2, v);
-  }
-  float mn = fminf(__low2float(mn2), __high2float(mn2));
-  float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-  for (int off = 1; off < G / kLaneElems; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(gmask, mn, off, kLanesPerRow));
-    mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, off, kLanesPerRow));
-  }
-  mn = __fadd_rn(mn, 0.0f);  // -0 -> +0: signed zeros compare equal
+  constexpr int NG = kD / G;        // groups per row
+  constexpr int CPG = G / 32;       // chunks per group
   constexpr uint32_t cmax = (1u << BITS) - 1u;
-  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(cmax));
-  const __half sh = __float2half_rn(s32);
-  const __half zh = __float2half_rn(mn);
-  const float sf = __half2float(sh);
-  const float zf = __half2float(zh);
-  // Store the group's z and s once (first lane of the group): fp16 row
-  // [z_0 .. z_{ng-1}, s_0 .. s_{ng-1}].
-  if ((part & (G / kLaneElems - 1)) == 0) {
-    const int ng = kD / G, g = (part * kLaneElems) / G;
-    reinterpret_cast<__half*>(sz_row)[g] = zh;
-    reinterpret_cast<__half*>(sz_row)[ng + g] = sh;
+  // group min / max: the lane's chunks, then the row's 4 lanes
+  float mn[NG], mx[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w[g * CPG][0]);
+    __nv_bfloat162 bb = a;
+#pragma unroll
+    for (int k = g * CPG; k < (g + 1) * CPG; ++k)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k][q]);
+        a = __hmin2(a, v);
+        bb = __hmax2(bb, v);
+      }
+    mn[g] = fminf(__low2float(a), __high2float(a));
+    mx[g] = fmaxf(__low2float(bb), __high2float(bb));
   }
-  // blk[x][l]: word x of what this lane sends to row lane l
-  constexpr int kSend = (!kV && BITS == 4) ? 4 : 2;
-  uint32_t blk[kSend][4];
 #pragma unroll
-  for (int x = 0; x < kSend; ++x)
+  for (int off = 1; off < kLanesPerRow; off <<= 1)
 #pragma unroll
-    for (int l = 0; l < 4; ++l) blk[x][l] = 0u;
-  // crumb table of 2-bit K registers: c(P, 0), c(P, 1)
-  const uint32_t c0 = (0x0234u >> (4 * part)) & 0xFu;  // P = 0..3 -> 4, 3, 2, 0
-  const uint32_t c1 = (0x1567u >> (4 * part)) & 0xFu;  // P = 0..3 -> 7, 6, 5, 1
+    for (int g = 0; g < NG; ++g) {
+      mn[g] = fminf(mn[g], __shfl_xor_sync(gmask, mn[g], off, kLanesPerRow));
+      mx[g] = fmaxf(mx[g], __shfl_xor_sync(gmask, mx[g], off, kLanesPerRow));
+    }
+  float zf[NG], sf[NG], rs[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const float m0 = __fadd_rn(mn[g], 0.0f);  // -0 -> +0: signed zeros compare equal
+    const float s32 = __fdiv_rn(__fsub_rn(mx[g], m0), static_cast<float>(cmax));
+    const __half sh = __float2half_rn(s32);
+    const __half zh = __float2half_rn(m0);
+    sf[g] = __half2float(sh);
+    zf[g] = __half2float(zh);
+    // A group whose stored scale is 0 gets code 0 everywhere: with rs = 0
+    // every quotient is 0 (or NaN for an infinite input, which also converts
+    // to 0) and no near-tie is flagged.
+    rs[g] = sf[g] != 0.0f ? __frcp_rn(sf[g]) : 0.0f;
+    if (g == part) {  // lane g stores group g: fp16 [z_0 .., s_0 ..]
+      reinterpret_cast<__half*>(sz_row)[g] = zh;
+      reinterpret_cast<__half*>(sz_row)[NG + g] = sh;
+    }
+  }
   // code = clamp(rint(fl(fl(x - z) / s))).  The quotient is first formed as
   // fl(d * fl(1/s)), within 3 * 2^-24 |u| of the correctly rounded one; rint
   // is constant between half-integers, so both give the same code unless the
   // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
   // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
-  // it; only then is the IEEE division evaluated (out of line, rare).
-  // A group whose stored scale is 0 gets code 0 everywhere: with rs = 0 every
-  // quotient is 0 (or NaN for an infinite input, which also converts to 0)
-  // and no near-tie is flagged.  Every lane runs the same code so that the
-  // row's shuffles and votes stay converged.
-  {
-    const float rs = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
-    const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
-#pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {  // 8 elements at a time: e = 8 c8 + k
-      float d[8], u[8];
-      uint32_t need = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t pw = w[c8 * 4 + (k >> 1)];
-        const float x = (k & 1) ? bf16_hi(pw) : bf16_lo(pw);
-        d[k] = __fsub_rn(x, zf);
-        u[k] = __fmul_rn(d[k], rs);
-        const float fr = __fsub_rn(__fsub_rn(u[k], floorf(u[k])), 0.5f);  // exact for |u| < 2^23
-        if (fabsf(fr) <= win) need |= 1u << k;
-      }
-      if (__any_sync(gmask, need != 0)) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (need & (1u << k)) u[k] = exact_quotient(d[k], sf);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t code = min(__float2uint_rn(u[k]), cmax);  // round half to even; < 0 -> 0
-        if constexpr (!kV) {
-          // K: destination lane t = c8, e' = k / 4, i = k % 4
-          const int ep = k >> 2, i = k & 3;
-          if constexpr (BITS == 2) {
-            blk[i >> 1][c8] |= code << (16 * ep + 2 * ((i & 1) ? c1 : c0));
-          } else if constexpr (BITS == 4) {
-            blk[i][c8] |= code << (16 * ep + 4 * part);
-          } else {
-            blk[i >> 1][c8] |= code << (16 * ep + 8 * (i & 1));
-          }
-        } else {
-          // V: c' = c8 (= 2m' + r), n = k -> destination lane k / 2, slice k % 2
-          if constexpr (BITS == 2) {
-            blk[k & 1][k >> 1] |= code << (8 * part + 2 * c8);
-          } else if constexpr (BITS == 4) {
-            blk[k & 1][k >> 1] |= code << (16 * (part & 1) + 4 * c8);
-          } else {
-            blk[k & 1][k >> 1] |= code << (8 * c8);
-          }
-        }
-      }
-    }
-  }
-  // 4-lane exchange: in round r each lane swaps with lane part ^ r.
-  uint32_t piece[kSend][4];  // piece[x][src]: word x received from row lane src
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int peer = part ^ r;
-#pragma unroll
-    for (int x = 0; x < kSend; ++x) {
-      const uint32_t mine = pick4(blk[x], peer);
-      const uint32_t got = r ? __shfl_xor_sync(gmask, mine, r, kLanesPerRow) : mine;
-#pragma unroll
-      for (int src = 0; src < 4; ++src)
-        if (peer == src) piece[x][src] = got;  // selects: stays in registers
-    }
-  }
-  // This lane's BITS words: its K slice, or its two V slices (2 part, 2 part + 1).
+  // it; only then is the IEEE division evaluated (out of line, rare).  Every
+  // lane runs the same instructions so the row's votes stay converged.
+  const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
   uint32_t out[BITS];
 #pragma unroll
   for (int q = 0; q < BITS; ++q) out[q] = 0u;
 #pragma unroll
-  for (int src = 0; src < 4; ++src) {
-    if constexpr (!kV) {
-      if constexpr (BITS == 8) {
-        out[2 * src] = piece[0][src];
-        out[2 * src + 1] = piece[1][src];
-      } else {
+  for (int k = 0; k < 4; ++k) {
+    const int g = k / CPG;
+    float d[8], u[8];
+    uint32_t need = 0;
 #pragma unroll
-        for (int x = 0; x < kSend; ++x) out[x] |= piece[x][src];
-      }
-    } else {
-      constexpr int kSliceWords = BITS / 2;
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t pw = w[k][j >> 1];
+      const float x = (j & 1) ? bf16_hi(pw) : bf16_lo(pw);
+      d[j] = __fsub_rn(x, zf[g]);
+      u[j] = __fmul_rn(d[j], rs[g]);
+      const float fr = __fsub_rn(__fsub_rn(u[j], floorf(u[j])), 0.5f);  // exact for |u| < 2^23
+      if (fabsf(fr) <= win) need |= 1u << j;
+    }
+    if (__any_sync(gmask, need != 0)) {
 #pragma unroll
-      for (int sl = 0; sl < 2; ++sl) {
-        if constexpr (BITS == 2) out[sl] |= piece[sl][src];
-        else if constexpr (BITS == 4) out[kSliceWords * sl + src / 2] |= piece[sl][src];
-        else out[kSliceWords * sl + src] = piece[sl][src];
-      }
+      for (int j = 0; j < 8; ++j)
+        if (need & (1u << j)) u[j] = exact_quotient(d[j], sf[g]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t code = min(__float2uint_rn(u[j]), cmax);  // round half to even; < 0 -> 0
+      out[dst_word<BITS, kV>(k, j)] |= code << dst_bit<BITS, kV>(k, j);
     }
   }
   uint8_t* dst = codes_row + part * 4 * BITS;
@@ -214,9 +178,24 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[16], int G, in
   }
 }
 
+template <int BITS, bool kV>
+__device__ __forceinline__ void quantize_lane_g(int G, const uint32_t (&w)[4][4], int part, uint32_t gmask,
+                                                uint8_t* codes_row, uint8_t* sz_row) {
+  if (G == 32) quantize_lane<BITS, kV, 32>(w, part, gmask, codes_row, sz_row);
+  else if (G == 64) quantize_lane<BITS, kV, 64>(w, part, gmask, codes_row, sz_row);
+  else quantize_lane<BITS, kV, 128>(w, part, gmask, codes_row, sz_row);
+}
+
+// Element offsets (in bf16) of the lane's words: K chunk k word q -> 32k +
+// 8 part + 2q; V chunk k word q (= 2m' + r) -> 16 (2k + m') + 8r + 2 part.
+__device__ __forceinline__ int k_elem(int k, int q, int part) { return 32 * k + 8 * part + 2 * q; }
+__device__ __forceinline__ int v_elem(int k, int q, int part) {
+  return 16 * (2 * k + (q >> 1)) + 8 * (q & 1) + 2 * part;
+}
+
 // One warp per (b, h, 8 consecutive positions); 4 lanes per row, each lane
-// 32 consecutive elements (four 16-byte loads of K and of V, all in flight
-// before any use).
+// the elements of its slice of the stored row (K: four 16-byte loads; V:
+// sixteen 4-byte loads, all in flight before any use).
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
   pdl_wait();  // the previous kernel in the stream may still read the cache
   pdl_launch_dependents();
@@ -237,18 +216,18 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   const bool visual = t >= p.vs && t < p.ve;
   const bool prot = p.prot[h] != 0;
 
-  const int64_t src = b * a.sb + h * a.sh + i * a.st + part * kLaneElems;
-  uint32_t kw[16], vw[16];
+  const int64_t src = b * a.sb + h * a.sh + i * a.st;
+  uint32_t kw[4][4], vw[4][4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.kin + src) + q);
-    const uint4 y = __ldg(reinterpret_cast<const uint4*>(a.vin + src) + q);
-    kw[4 * q] = x.x; kw[4 * q + 1] = x.y; kw[4 * q + 2] = x.z; kw[4 * q + 3] = x.w;
-    vw[4 * q] = y.x; vw[4 * q + 1] = y.y; vw[4 * q + 2] = y.z; vw[4 * q + 3] = y.w;
+  for (int k = 0; k < 4; ++k) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.kin + src + k_elem(k, 0, part)));
+    kw[k][0] = x.x; kw[k][1] = x.y; kw[k][2] = x.z; kw[k][3] = x.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) vw[k][q] = __ldg(reinterpret_cast<const uint32_t*>(a.vin + src + v_elem(k, q, part)));
   }
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
-    const uint32_t (&w)[16] = which ? vw : kw;
+    const uint32_t (&w)[4][4] = which ? vw : kw;
     uint8_t* dst;
     if (!visual) {
       const int64_t tr = t < p.vs ? t : t - p.Tv;
@@ -266,21 +245,29 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
         uint8_t* sz = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_V_SZ : KVQ_SEG_K_SZ]) +
                       row * (which ? p.vszrow : p.kszrow);
         if (which) {
-          if (bits == 2) quantize_lane<2, true>(w, p.G, part, gmask, codes, sz);
-          else if (bits == 4) quantize_lane<4, true>(w, p.G, part, gmask, codes, sz);
-          else quantize_lane<8, true>(w, p.G, part, gmask, codes, sz);
+          if (bits == 2) quantize_lane_g<2, true>(p.G, w, part, gmask, codes, sz);
+          else if (bits == 4) quantize_lane_g<4, true>(p.G, w, part, gmask, codes, sz);
+          else quantize_lane_g<8, true>(p.G, w, part, gmask, codes, sz);
         } else {
-          if (bits == 2) quantize_lane<2, false>(w, p.G, part, gmask, codes, sz);
-          else if (bits == 4) quantize_lane<4, false>(w, p.G, part, gmask, codes, sz);
-          else quantize_lane<8, false>(w, p.G, part, gmask, codes, sz);
+          if (bits == 2) quantize_lane_g<2, false>(p.G, w, part, gmask, codes, sz);
+          else if (bits == 4) quantize_lane_g<4, false>(p.G, w, part, gmask, codes, sz);
+          else quantize_lane_g<8, false>(p.G, w, part, gmask, codes, sz);
         }
         continue;
       }
       dst = codes;
     }
-    uint4* o = reinterpret_cast<uint4*>(dst + part * kLaneElems * 2);
+    // bf16 row: the lane's elements go back to where they came from
+    uint16_t* o = reinterpret_cast<uint16_t*>(dst);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int k = 0; k < 4; ++k) {
+      if (which) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint32_t*>(o + v_elem(k, q, part)) = w[k][q];
+      } else {
+        *reinterpret_cast<uint4*>(o + k_elem(k, 0, part)) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+      }
+    }
   }
 }
 
