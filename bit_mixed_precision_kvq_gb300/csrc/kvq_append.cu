@@ -136,8 +136,9 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
   // is constant between half-integers, so both give the same code unless the
   // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
   // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
-  // it; only then is the IEEE division evaluated (out of line, rare).  Every
-  // lane runs the same instructions so the row's votes stay converged.
+  // it (0.5 - win is exact); only then is the IEEE division evaluated (out of
+  // line, rare).  Every lane runs the same instructions so the row's votes
+  // stay converged.
   const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
   uint32_t out[BITS];
 #pragma unroll
@@ -153,8 +154,8 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
       const float x = (j & 1) ? bf16_hi(pw) : bf16_lo(pw);
       d[j] = __fsub_rn(x, zf[g]);
       u[j] = __fmul_rn(d[j], rs[g]);
-      const float fr = __fsub_rn(__fsub_rn(u[j], floorf(u[j])), 0.5f);  // exact for |u| < 2^23
-      if (fabsf(fr) <= win) need |= 1u << j;
+      // |u - rint(u)| is exact for |u| < 2^23; a near-tie lies within win of 1/2
+      if (fabsf(__fsub_rn(u[j], rintf(u[j]))) >= 0.5f - win) need |= 1u << j;
     }
     if (__any_sync(gmask, need != 0)) {
 #pragma unroll
@@ -164,7 +165,7 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t code = min(__float2uint_rn(u[j]), cmax);  // round half to even; < 0 -> 0
-      out[dst_word<BITS, kV>(k, j)] |= code << dst_bit<BITS, kV>(k, j);
+      out[dst_word<BITS, kV>(k, j)] += code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
     }
   }
   uint8_t* dst = codes_row + part * 4 * BITS;

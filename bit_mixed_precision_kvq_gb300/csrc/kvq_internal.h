@@ -41,6 +41,23 @@ constexpr int kD = 128;          // head dimension supported by the kernels
 constexpr int kNH = KVQ_HEADS_PER_UNIT;  // query heads per unit (MMA N = 8)
 constexpr int kBf16PosBytes = 4 * kD;    // K + V bf16 rows of one position
 constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
+// Stage size of the split kernel's shared-memory ring, and the staging of
+// packed tiles: positions per tile (a multiple of the block size, <= 512)
+// and the largest block size of the kernel for (k_bits, v_bits, G) -- 64
+// positions (4 MMA row-tiles per softmax update) when a tile holds >= 256
+// positions, else 32; a call uses 64 only when its chunks are long enough to
+// keep the consumer warps busy with it.
+constexpr int kStageBytes = 32 * 1024;
+KVQ_HD constexpr int packed_row_bytes(int kb, int vb, int G) {
+  return 16 * kb + 16 * vb + (kb < 16 ? 4 * (kD / G) : 0) + (vb < 16 ? 4 * (kD / G) : 0);
+}
+KVQ_HD constexpr int packed_tile_rows32(int w) {
+  return ((kStageBytes - 4 * 128) / w) / 32 * 32 > 512 ? 512 : ((kStageBytes - 4 * 128) / w) / 32 * 32;
+}
+KVQ_HD constexpr int packed_block_halves(int kb, int vb, int G) {
+  return packed_tile_rows32(packed_row_bytes(kb, vb, G)) >= 256 ? 4 : 2;
+}
+
 // Work balance: a position costs its cache bytes plus this many byte
 // equivalents of unpack / tensor-core / softmax work, so that chunks of
 // cheap packed rows do not get several times more positions to compute.
@@ -132,7 +149,8 @@ struct Params {
   int32_t kb, vb, G;
   int32_t n_prot, n_packed;
   int32_t krow, kszrow, vrow, vszrow;  // bytes per row of the packed segments
-  int32_t tt_pk;                       // positions per packed tile (multiple of 16)
+  int32_t tt_pk;                       // positions per packed tile (multiple of the block)
+  int32_t pk_halves;                   // 16-row MMA halves per packed block: 2 or 4
   int32_t pk_off_vc, pk_off_ksz, pk_off_vsz;  // packed-tile offsets in a stage
   // cache segments
   const uint8_t* seg[KVQ_NSEG];

@@ -40,7 +40,6 @@ namespace kvq {
 constexpr int kConsumerWarps = 11;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 5;
-constexpr int kStageBytes = 32 * 1024;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kPrefetchBytes = kStageBytes;  // L2 prefetch before the dependency wait
@@ -642,34 +641,38 @@ __device__ __forceinline__ void acc_to_true(Acc& acc, int tig) {
 enum KPath { kKBf16 = 0, kKPacked = 1 };
 enum VPath { kVBf16Lane = 0, kVBf16D = 1, kVPacked = 2 };
 
-// One 32-position block [r0, r0 + 32) of a staged tile (n valid positions):
-// two 16-row MMA halves sharing one online-softmax update.
-template <int KP, int VP, int KB, int VB, int G>
-__device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
-                                         const uint8_t* vsz, int r0, int n, float sl2,
-                                         const uint32_t (&qb)[8][2], const uint32_t (&zb)[2],
-                                         int gid, int tig, int lane, Acc& acc) {
-  const bool two = r0 + 16 < n;  // the second half holds valid positions
-  float S[2][4];
-  if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0, sl2, qb, zb, gid, tig, S[0]);
-  else qk_bf16(kc, r0, sl2, qb, gid, tig, S[0]);
-  if (two) {
-    if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0 + 16, sl2, qb, zb, gid, tig, S[1]);
-    else qk_bf16(kc, r0 + 16, sl2, qb, gid, tig, S[1]);
-  } else {
-    S[1][0] = S[1][1] = S[1][2] = S[1][3] = -INFINITY;
-  }
-  if (r0 + 32 > n) {  // ragged block: mask rows past n
+// One block [r0, r0 + 16 NH) of a staged tile (n valid positions): NH
+// 16-row MMA halves sharing one online-softmax update.
+template <int NH, int KP, int VP, int KB, int VB, int G>
+__device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
+                                       const uint8_t* vsz, int r0, int n, float sl2,
+                                       const uint32_t (&qb)[8][2], const uint32_t (&zb)[2], int gid,
+                                       int tig, int lane, Acc& acc) {
+  float S[NH][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
+    if (h == 0 || r0 + 16 * h < n) {
+      if constexpr (KP == kKPacked) qk_packed<KB, G>(kc, ksz, r0 + 16 * h, sl2, qb, zb, gid, tig, S[h]);
+      else qk_bf16(kc, r0 + 16 * h, sl2, qb, gid, tig, S[h]);
+    } else {
+      S[h][0] = S[h][1] = S[h][2] = S[h][3] = -INFINITY;
+    }
+  }
+  if (r0 + 16 * NH > n) {  // ragged block: mask rows past n
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
       if (r0 + 16 * h + gid >= n) S[h][0] = S[h][1] = -INFINITY;
       if (r0 + 16 * h + gid + 8 >= n) S[h][2] = S[h][3] = -INFINITY;
     }
   }
 
-  // ---- online softmax over the 32 positions (columns = heads 2tig, 2tig+1) ----
-  float mx0 = fmaxf(fmaxf(S[0][0], S[0][2]), fmaxf(S[1][0], S[1][2]));
-  float mx1 = fmaxf(fmaxf(S[0][1], S[0][3]), fmaxf(S[1][1], S[1][3]));
+  // ---- online softmax over the block (columns = heads 2tig, 2tig+1) ----
+  float mx0 = fmaxf(S[0][0], S[0][2]), mx1 = fmaxf(S[0][1], S[0][3]);
+#pragma unroll
+  for (int h = 1; h < NH; ++h) {
+    mx0 = fmaxf(mx0, fmaxf(S[h][0], S[h][2]));
+    mx1 = fmaxf(mx1, fmaxf(S[h][1], S[h][3]));
+  }
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -678,18 +681,21 @@ __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, 
   const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
   const float b0s = mn0 == -INFINITY ? 0.f : mn0, b1s = mn1 == -INFINITY ? 0.f : mn1;
   const float c0 = ex2(acc.m[0] - b0s), c1 = ex2(acc.m[1] - b1s);
-  float P[2][4];
+  float P[NH][4];
+  float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     P[h][0] = ex2(S[h][0] - b0s);
     P[h][1] = ex2(S[h][1] - b1s);
     P[h][2] = ex2(S[h][2] - b0s);
     P[h][3] = ex2(S[h][3] - b1s);
+    l0 += P[h][0] + P[h][2];
+    l1 += P[h][1] + P[h][3];
   }
   acc.m[0] = mn0;
   acc.m[1] = mn1;
-  acc.l[0] = fmaf(acc.l[0], c0, (P[0][0] + P[0][2]) + (P[1][0] + P[1][2]));
-  acc.l[1] = fmaf(acc.l[1], c1, (P[0][1] + P[0][3]) + (P[1][1] + P[1][3]));
+  acc.l[0] = fmaf(acc.l[0], c0, l0);
+  acc.l[1] = fmaf(acc.l[1], c1, l1);
   if (!__all_sync(0xffffffffu, c0 == 1.f && c1 == 1.f)) {  // some running max moved
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -706,13 +712,15 @@ __device__ __forceinline__ void kblock32(const uint8_t* kc, const uint8_t* ksz, 
     }
   }
   // P^T as the B operand of PV: transpose the 8x8 quarters.
-  auto pv = [&](int h, uint32_t pa0, uint32_t pa1) {
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    if (h > 0 && r0 + 16 * h >= n) break;
+    const uint32_t pa0 = movmatrix_trans(pack_f16x2(P[h][0], P[h][1]));
+    const uint32_t pa1 = movmatrix_trans(pack_f16x2(P[h][2], P[h][3]));
     if constexpr (VP == kVPacked) pv_packed<VB, G>(vc, vsz, r0 + 16 * h, n, pa0, pa1, gid, tig, acc);
     else if constexpr (VP == kVBf16D) pv_bf16_dcols(vc, r0 + 16 * h, n, pa0, pa1, tig, lane, acc);
     else pv_bf16_lanecols(vc, r0 + 16 * h, n, pa0, pa1, gid, tig, acc);
-  };
-  pv(0, movmatrix_trans(pack_f16x2(P[0][0], P[0][1])), movmatrix_trans(pack_f16x2(P[0][2], P[0][3])));
-  if (two) pv(1, movmatrix_trans(pack_f16x2(P[1][0], P[1][1])), movmatrix_trans(pack_f16x2(P[1][2], P[1][3])));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -815,7 +823,7 @@ __device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt) {
   return false;
 }
 
-template <int KB, int VB, int G, bool kStep>
+template <int KB, int VB, int G, bool kStep, int NHP>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
@@ -917,9 +925,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       if (lane == 0) mbar_arrive(&sm.empty[it % kStages]);
       ++it;
     };
-    // This warp's 32-position blocks of a tile of n rows: first, first + 11, ...
-    auto deal = [&](int n, int& first) {
-      const int nb = (n + 31) >> 5;
+    // This warp's blocks (bs rows each) of a tile of n rows: first, first + 11, ...
+    auto deal = [&](int n, int bs, int& first) {
+      const int nb = (n + bs - 1) / bs;
       first = (warp + kConsumerWarps - static_cast<int>(gblk % kConsumerWarps)) % kConsumerWarps;
       gblk += nb;
       return nb;
@@ -928,18 +936,18 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       walk_piece(p, true, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
-        const int nb = deal(n, first);
+        const int nb = deal(n, 32, first);
         for (int kb = first; kb < nb; kb += kConsumerWarps)
-          kblock32<kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
-                                                 qb, zb, gid, tig, lane, acc);
+          kblock<2, kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
+                                                  qb, zb, gid, tig, lane, acc);
         end_tile();
       });
     } else {
       walk_piece(p, false, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
-        const int nb = deal(n, first);
         if (kind == kTilePacked) {
+          const int nb = deal(n, 16 * NHP, first);
           if constexpr (VB < 16) {
             if (first < nb && !packed_acc) {
               acc_to_packed<VB>(acc);
@@ -947,10 +955,11 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
             }
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
-            kblock32<(KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
-                base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 32, n, sl2, qb,
-                zb, gid, tig, lane, acc);
+            kblock<NHP, (KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
+                base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16 * NHP, n, sl2,
+                qb, zb, gid, tig, lane, acc);
         } else {  // text rows of a packed unit
+          const int nb = deal(n, 32, first);
           if constexpr (VB < 16) {
             if (first < nb && packed_acc) {
               acc_to_true<VB, G>(acc, tig);
@@ -958,8 +967,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
             }
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
-            kblock32<kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
-                                                qb, zb, gid, tig, lane, acc);
+            kblock<2, kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
+                                                 qb, zb, gid, tig, lane, acc);
         }
         end_tile();
       });
@@ -1070,7 +1079,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   }
 }
 
-template <int KB, int VB, int G, bool kStep>
+// NHP: 16-row MMA halves per packed block (2 or 4; the launch's pk_halves).
+template <int KB, int VB, int G, bool kStep, int NHP>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -1094,7 +1104,7 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
     }
     return;
   }
-  consumer_loop<KB, VB, G, kStep>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G, kStep, NHP>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq
