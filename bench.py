@@ -41,6 +41,12 @@ import torch  # noqa: E402
 
 import synth  # noqa: E402
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# roofline kernel, from one ncu capture of the same launch configuration with
+# the current kernels: (workload, layers, fused) -> bytes.  Other workloads:
+# not captured (null).
+NCU_TRAFFIC = {("llava_ov_7b", 28, True): 5450496}
+
 METRIC = ("decode-attention µs/step and achieved HBM GB/s (compressed bytes) vs 8 TB/s peak")
 UNIT = "GB/s"
 
@@ -422,10 +428,11 @@ def run_ours(args, rank, world, local):
                    "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
                    "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
+                     "traffic": NCU_TRAFFIC.get((w.name, n_layers, model.fused)),
                      "kernel": ("split_mma_kernel<..., step> (kvq_decode_step, one launch)" if model.fused
                                 else "kvq_quantize_append + kvq_decode_attention (3 launches)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
                      "per_launch_bytes": int(layer_bytes), "per_launch_us": round(launch_ms * 1e3, 3),
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if peaks else
                                     "fallback 6800 GB/s"},
