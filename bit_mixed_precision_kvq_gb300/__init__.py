@@ -71,7 +71,8 @@ class Layout(ctypes.Structure):
                 ("row_bytes", ctypes.c_int64 * KVQ_NSEG), ("off", ctypes.c_int64 * KVQ_NSEG),
                 ("bytes", ctypes.c_int64 * KVQ_NSEG), ("total_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("eff_bits_k", ctypes.c_double),
-                ("eff_bits_v", ctypes.c_double)]
+                ("eff_bits_v", ctypes.c_double), ("n_konly", ctypes.c_int32),
+                ("konly_head", ctypes.c_uint8 * KVQ_MAX_HEADS)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -126,14 +127,16 @@ def _stream(stream) -> int:
 
 def cache_layout(B: int, H_q: int, H_kv: int, D: int, T_cap: int, vis_start: int, vis_end: int,
                  k_bits: int, v_bits: int, group_size: int,
-                 protected: Sequence[int] = ()) -> Layout:
+                 protected: Sequence[int] = (), k_only: Sequence[int] = ()) -> Layout:
     """kvq_cache_layout: validate the per-layer description and derive the layout.
-    ``protected`` lists the protected KV heads."""
+    ``protected`` lists the KV heads whose visual K and V stay bf16, ``k_only``
+    those whose visual K alone stays bf16 (V quantised)."""
     d = LayoutDesc(B, H_q, H_kv, D, T_cap, vis_start, vis_end, k_bits, v_bits, group_size)
-    for h in protected:
-        if not 0 <= int(h) < KVQ_MAX_HEADS:
-            raise KvqError(1, "kvq_cache_layout")
-        d.protected_heads[int(h)] = 1
+    for mode, heads in ((1, protected), (2, k_only)):
+        for h in heads:
+            if not 0 <= int(h) < KVQ_MAX_HEADS or d.protected_heads[int(h)] != 0:
+                raise KvqError(1, "kvq_cache_layout")
+            d.protected_heads[int(h)] = mode
     out = Layout()
     st = load().kvq_cache_layout(ctypes.byref(d), ctypes.byref(out))
     if st != 0:

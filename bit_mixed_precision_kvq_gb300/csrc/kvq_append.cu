@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
   const int32_t b = static_cast<int32_t>(bh / p.Hkv);
   const int32_t t = a.t0 + i;
   const bool visual = t >= p.vs && t < p.ve;
-  const bool prot = p.prot[h] != 0;
+  const int mode = p.prot[h];  // 0 quantised, 1 K and V protected, 2 K protected
 
   const int64_t src = b * a.sb + h * a.sh + i * a.st;
   uint32_t kw[4][4], vw[4][4];
@@ -234,12 +234,17 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
       const int64_t tr = t < p.vs ? t : t - p.Tv;
       const int64_t row = (static_cast<int64_t>(b) * p.Hkv + h) * p.T_text + tr;
       dst = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_TEXT_V : KVQ_SEG_TEXT_K]) + row * (2 * kD);
-    } else if (prot) {
+    } else if (which == 0 && mode != 0) {  // protected or K-only head: bf16 K
+      const int64_t row = prot_k_row(p, b, mode == 1 ? kClsProt : kClsKonly, p.slot[h]) * p.Tv + (t - p.vs);
+      dst = const_cast<uint8_t*>(p.seg[KVQ_SEG_PROT_K]) + row * (2 * kD);
+    } else if (which == 1 && mode == 1) {  // protected head: bf16 V
       const int64_t row = (static_cast<int64_t>(b) * p.n_prot + p.slot[h]) * p.Tv + (t - p.vs);
-      dst = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_PROT_V : KVQ_SEG_PROT_K]) + row * (2 * kD);
+      dst = const_cast<uint8_t*>(p.seg[KVQ_SEG_PROT_V]) + row * (2 * kD);
     } else {
       const int bits = which ? p.vb : p.kb;
-      const int64_t row = (static_cast<int64_t>(b) * p.n_packed + p.slot[h]) * p.Tv_pad + (t - p.vs);
+      const int64_t row =
+          (which ? packed_v_row(p, b, mode == 2 ? kClsKonly : kClsPacked, p.slot[h])
+                 : static_cast<int64_t>(b) * p.n_packed + p.slot[h]) * p.Tv_pad + (t - p.vs);
       uint8_t* codes = const_cast<uint8_t*>(p.seg[which ? KVQ_SEG_V_CODES : KVQ_SEG_K_CODES]) +
                        row * (which ? p.vrow : p.krow);
       if (bits < 16) {

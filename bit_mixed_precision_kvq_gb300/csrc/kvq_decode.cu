@@ -22,10 +22,10 @@
 
 namespace kvq {
 
-const void* split_kernel_k2(int vb, int G, bool step, int halves);
-const void* split_kernel_k4(int vb, int G, bool step, int halves);
-const void* split_kernel_k8(int vb, int G, bool step, int halves);
-const void* split_kernel_k16(int vb, int G, bool step, int halves);
+const void* split_kernel_k2(int vb, int G, bool step, int halves, bool konly);
+const void* split_kernel_k4(int vb, int G, bool step, int halves, bool konly);
+const void* split_kernel_k8(int vb, int G, bool step, int halves, bool konly);
+const void* split_kernel_k16(int vb, int G, bool step, int halves, bool konly);
 
 constexpr int kCombineWarps = 16;
 
@@ -55,9 +55,20 @@ namespace {
 // 64-position packed blocks only when packed chunks are long (>= 1024
 // positions: enough blocks for every consumer warp); else 32.
 int packed_halves(const kvq::Plan& P, const kvq_layout* L) {
+  if (L->n_konly > 0) return 2;  // K-only layouts: 32-position blocks only
   if (kvq::packed_block_halves(L->d.k_bits, L->d.v_bits, L->d.group_size) < 4) return 2;
   const int64_t per_chunk = P.aligned ? P.T / (P.n_q > 0 ? P.n_q : 1) : P.T;
   return per_chunk >= 1024 ? 4 : 2;
+}
+
+// K-only tiles: bf16 K rows, then the packed V rows and their scale/zero.
+void konly_tile_geometry(kvq::Params* p) {
+  const int w = 2 * kvq::kD + p->vrow + p->vszrow;
+  const int tt = kvq::packed_tile_rows32(w);
+  auto r128 = [](int x) { return (x + 127) / 128 * 128; };
+  p->tt_ko = tt;
+  p->ko_off_vc = r128(tt * 2 * kvq::kD);
+  p->ko_off_vsz = p->ko_off_vc + r128(tt * p->vrow);
 }
 
 void packed_tile_geometry(kvq::Params* p) {
@@ -72,12 +83,12 @@ void packed_tile_geometry(kvq::Params* p) {
   p->pk_off_vsz = p->pk_off_ksz + r128(tt * p->kszrow);
 }
 
-const void* split_kernel_for(int kb, int vb, int G, bool step, int halves) {
+const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool konly) {
   switch (kb) {
-    case 2: return kvq::split_kernel_k2(vb, G, step, halves);
-    case 4: return kvq::split_kernel_k4(vb, G, step, halves);
-    case 8: return kvq::split_kernel_k8(vb, G, step, halves);
-    case 16: return kvq::split_kernel_k16(vb, G, step, halves);
+    case 2: return kvq::split_kernel_k2(vb, G, step, halves, konly);
+    case 4: return kvq::split_kernel_k4(vb, G, step, halves, konly);
+    case 8: return kvq::split_kernel_k8(vb, G, step, halves, konly);
+    case 16: return kvq::split_kernel_k16(vb, G, step, halves, konly);
   }
   return nullptr;
 }
@@ -137,6 +148,7 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   kvq_plan_cuts(&p->plan, p->cuts);
   p->pk_halves = packed_halves(p->plan, L);
   packed_tile_geometry(p);
+  konly_tile_geometry(p);
   return KVQ_OK;
 }
 
@@ -155,7 +167,8 @@ extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cach
   std::lock_guard<std::mutex> call_lock(call_mu);
   kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace, ws_bytes, &p);
   if (st != KVQ_OK) return st;
-  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p.pk_halves);
+  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p.pk_halves,
+                                       L->n_konly > 0);
   if (!split) return KVQ_ERR_UNSUPPORTED;
   if ((st = prepare_split(split, kSplitSmemBytes)) != KVQ_OK) return st;
   if (kvq_launch_pdl(split, p.plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, &p) != 0)
@@ -184,7 +197,8 @@ extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const vo
   p.k_new = static_cast<const uint16_t*>(k_new_bf16);
   p.v_new = static_cast<const uint16_t*>(v_new_bf16);
   p.t_new = t_new;
-  const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p.pk_halves);
+  const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p.pk_halves,
+                                    L->n_konly > 0);
   if (!fn) return KVQ_ERR_UNSUPPORTED;
   if ((st = prepare_split(fn, kSplitSmemBytes)) != KVQ_OK) return st;
   // Cooperative launch: a combining CTA may wait for other CTAs of its unit,

@@ -64,6 +64,10 @@ KVQ_HD constexpr int packed_block_halves(int kb, int vb, int G) {
 constexpr int kPosCost = 256;
 constexpr int kBf16PosCost = kBf16PosBytes + kPosCost;
 
+// Unit classes, in unit order: protected heads (K and V bf16), K-only
+// protected heads (K bf16, V packed), packed heads.
+enum UnitClass { kClsProt = 0, kClsKonly = 1, kClsPacked = 2 };
+
 struct Plan {
   int32_t U_p;        // protected units
   int32_t U;          // all units
@@ -75,9 +79,14 @@ struct Plan {
   int64_t ub_p, ub_u; // cost of a protected / packed unit
   int64_t P_bytes;    // U_p * ub_p
   int64_t total;      // cost of all units
-  // per-unit chunks (aligned != 0, when C >= U): n_p per protected and n_q
-  // per packed unit, plus one for each of the first R units
+  // per-unit chunks (aligned != 0, when C >= U): n_p per protected, n_k per
+  // K-only and n_q per packed unit, plus one for each of the first R units
   int32_t aligned, n_p, n_q, R;
+  // K-only protected units (after the protected ones)
+  int32_t U_k, n_k;
+  int32_t w_kvis;     // cost of one K-only visual position
+  int64_t ub_k;       // cost of a K-only unit
+  int64_t K_bytes;    // U_k * ub_k
 };
 
 struct Cut {
@@ -85,18 +94,25 @@ struct Cut {
   int32_t p;  // position inside the unit
 };
 
-// Position inside a unit at cost offset `rem` (0 <= rem < unit cost).
-KVQ_HD int32_t unit_cut_pos(const Plan& P, bool prot, int64_t rem) {
-  if (prot) return static_cast<int32_t>(rem / kBf16PosCost);
+// Position inside a unit of class cls at cost offset `rem` (0 <= rem < unit
+// cost).  Visual cuts of units with packed rows are 16-row aligned.
+KVQ_HD int32_t unit_cut_pos(const Plan& P, int cls, int64_t rem) {
+  if (cls == kClsProt) return static_cast<int32_t>(rem / kBf16PosCost);
+  const int64_t w = cls == kClsKonly ? P.w_kvis : P.w_vis;
   const int64_t pre = static_cast<int64_t>(P.vsa) * kBf16PosCost;
-  const int64_t vis = static_cast<int64_t>(P.vea - P.vsa) * P.w_vis;
+  const int64_t vis = static_cast<int64_t>(P.vea - P.vsa) * w;
   if (rem < pre) return static_cast<int32_t>(rem / kBf16PosCost);
   if (rem < pre + vis) {
-    int64_t row = (rem - pre) / P.w_vis;
+    int64_t row = (rem - pre) / w;
     row -= row % kVisAlign;
     return P.vsa + static_cast<int32_t>(row);
   }
   return P.vea + static_cast<int32_t>((rem - pre - vis) / kBf16PosCost);
+}
+
+// Class of unit u.
+KVQ_HD int unit_class(const Plan& P, int32_t u) {
+  return u < P.U_p ? kClsProt : (u < P.U_p + P.U_k ? kClsKonly : kClsPacked);
 }
 
 // Last unit of chunk c: a chunk that ends exactly at the start of a unit
@@ -114,9 +130,12 @@ KVQ_HD int32_t chunk_last_unit(const Cut* cuts, int32_t c, int32_t U) {
 KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t* c_first,
                              int32_t* c_last) {
   if (P.aligned) {  // closed form of the per-unit allocation
-    const int32_t base = u <= P.U_p ? u * P.n_p : P.U_p * P.n_p + (u - P.U_p) * P.n_q;
+    const int32_t Uk_end = P.U_p + P.U_k;
+    const int32_t base = u <= P.U_p ? u * P.n_p
+                         : u <= Uk_end ? P.U_p * P.n_p + (u - P.U_p) * P.n_k
+                                       : P.U_p * P.n_p + P.U_k * P.n_k + (u - Uk_end) * P.n_q;
     const int32_t c0 = base + (u < P.R ? u : P.R);
-    const int32_t n = (u < P.U_p ? P.n_p : P.n_q) + (u < P.R ? 1 : 0);
+    const int32_t n = (u < P.U_p ? P.n_p : (u < Uk_end ? P.n_k : P.n_q)) + (u < P.R ? 1 : 0);
     *c_first = c0;
     *c_last = c0 + n - 1;
     return;
@@ -168,37 +187,69 @@ struct Params {
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
   Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host
-  uint8_t prot[KVQ_MAX_HEADS];        // head -> protected?
+  uint8_t prot[KVQ_MAX_HEADS];        // head -> protection mode (0, 1 both, 2 K only)
   int32_t slot[KVQ_MAX_HEADS];        // head -> slot
   uint8_t prot_head[KVQ_MAX_HEADS];   // protected slot -> head
   uint8_t packed_head[KVQ_MAX_HEADS]; // packed slot -> head
+  // K-only protected heads (layouts that have them)
+  uint8_t konly_head[KVQ_MAX_HEADS];  // K-only slot -> head
+  int32_t n_konly;
+  int32_t tt_ko;                       // positions per K-only tile (bf16 K + packed V rows)
+  int32_t ko_off_vc, ko_off_vsz;       // K-only-tile offsets in a stage
 };
 
-// unit -> (b, head, hc, protected?)
+// unit -> (b, head, hc, slot, class).  kKO: the layout may have K-only
+// protected heads (three unit classes); else only protected and packed.
 struct UnitInfo {
   int32_t b, h, hc, slot;
-  bool prot;
+  int32_t cls;
+  bool prot;  // cls == kClsProt
 };
 
+template <bool kKO>
 KVQ_HD UnitInfo unit_info(const Params& p, int32_t u) {
   UnitInfo r;
-  const bool prot = u < p.plan.U_p;
-  const int32_t v = prot ? u : u - p.plan.U_p;
-  const int32_t nslots = prot ? p.n_prot : p.n_packed;
+  int cls;
+  int32_t v, nslots;
+  if constexpr (kKO) {
+    cls = unit_class(p.plan, u);
+    v = cls == kClsProt ? u : (cls == kClsKonly ? u - p.plan.U_p : u - p.plan.U_p - p.plan.U_k);
+    nslots = cls == kClsProt ? p.n_prot : (cls == kClsKonly ? p.n_konly : p.n_packed);
+  } else {
+    cls = u < p.plan.U_p ? kClsProt : kClsPacked;
+    v = cls == kClsProt ? u : u - p.plan.U_p;
+    nslots = cls == kClsProt ? p.n_prot : p.n_packed;
+  }
   r.b = v / (nslots * p.NHC);
   const int32_t rem = v - r.b * nslots * p.NHC;
   r.slot = rem / p.NHC;
   r.hc = rem - r.slot * p.NHC;
-  r.h = prot ? p.prot_head[r.slot] : p.packed_head[r.slot];
-  r.prot = prot;
+  if constexpr (kKO) {
+    r.h = cls == kClsProt ? p.prot_head[r.slot] : (cls == kClsKonly ? p.konly_head[r.slot] : p.packed_head[r.slot]);
+  } else {
+    r.h = cls == kClsProt ? p.prot_head[r.slot] : p.packed_head[r.slot];
+  }
+  r.cls = cls;
+  r.prot = cls == kClsProt;
   return r;
 }
 
 // (b, head, hc) -> unit
 KVQ_HD int32_t unit_of(const Params& p, int32_t b, int32_t h, int32_t hc) {
   const int32_t s = p.slot[h];
-  if (p.prot[h]) return (b * p.n_prot + s) * p.NHC + hc;
-  return p.plan.U_p + (b * p.n_packed + s) * p.NHC + hc;
+  if (p.prot[h] == 1) return (b * p.n_prot + s) * p.NHC + hc;
+  if (p.prot[h] == 2) return p.plan.U_p + (b * p.n_konly + s) * p.NHC + hc;
+  return p.plan.U_p + p.plan.U_k + (b * p.n_packed + s) * p.NHC + hc;
+}
+
+// Rows of the visual segments.  Protected K rows hold the protected heads
+// then the K-only heads; packed V rows hold the packed heads then the
+// K-only heads.
+KVQ_HD int64_t prot_k_row(const Params& p, int32_t b, int cls, int32_t slot) {
+  return static_cast<int64_t>(b) * (p.n_prot + p.n_konly) + (cls == kClsKonly ? p.n_prot : 0) + slot;
+}
+KVQ_HD int64_t packed_v_row(const Params& p, int32_t b, int cls, int32_t slot) {
+  return static_cast<int64_t>(b) * (p.n_packed + p.n_konly) + (cls == kClsKonly ? p.n_packed : 0) + slot;
 }
 
 }  // namespace kvq

@@ -36,7 +36,7 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   if (!(d.group_size == 32 || d.group_size == 64 || d.group_size == 128)) return KVQ_ERR_INVALID_ARG;
   if (d.D % d.group_size != 0) return KVQ_ERR_INVALID_ARG;
   for (int h = 0; h < KVQ_MAX_HEADS; ++h)
-    if (d.protected_heads[h] > 1 || (h >= d.H_kv && d.protected_heads[h] != 0))
+    if (d.protected_heads[h] > 2 || (h >= d.H_kv && d.protected_heads[h] != 0))
       return KVQ_ERR_INVALID_ARG;
   if (d.D != kvq::kD) return KVQ_ERR_UNSUPPORTED;
 
@@ -51,9 +51,12 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   L.Tv_pad = (L.Tv + 15) / 16 * 16;
   L.T_text = d.T_cap - L.Tv;
   for (int h = 0; h < d.H_kv; ++h) {
-    if (d.protected_heads[h]) {
+    if (d.protected_heads[h] == 1) {
       L.slot[h] = L.n_prot;
       L.prot_head[L.n_prot++] = static_cast<uint8_t>(h);
+    } else if (d.protected_heads[h] == 2) {
+      L.slot[h] = L.n_konly;
+      L.konly_head[L.n_konly++] = static_cast<uint8_t>(h);
     } else {
       L.slot[h] = L.n_packed;
       L.packed_head[L.n_packed++] = static_cast<uint8_t>(h);
@@ -71,11 +74,15 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
   L.row_bytes[KVQ_SEG_PROT_V] = 2 * D;
   L.row_bytes[KVQ_SEG_TEXT_K] = 2 * D;
   L.row_bytes[KVQ_SEG_TEXT_V] = 2 * D;
-  const int64_t packed_rows = static_cast<int64_t>(d.B) * L.n_packed * L.Tv_pad;
-  const int64_t prot_rows = static_cast<int64_t>(d.B) * L.n_prot * L.Tv;
+  // K-only heads (mode 2) keep their K with the protected heads' K and their
+  // V with the packed heads' V (after them).
+  const int64_t packed_k_rows = static_cast<int64_t>(d.B) * L.n_packed * L.Tv_pad;
+  const int64_t packed_v_rows = static_cast<int64_t>(d.B) * (L.n_packed + L.n_konly) * L.Tv_pad;
+  const int64_t prot_k_rows = static_cast<int64_t>(d.B) * (L.n_prot + L.n_konly) * L.Tv;
+  const int64_t prot_v_rows = static_cast<int64_t>(d.B) * L.n_prot * L.Tv;
   const int64_t text_rows = static_cast<int64_t>(d.B) * d.H_kv * L.T_text;
-  const int64_t rows[KVQ_NSEG] = {packed_rows, packed_rows, packed_rows, packed_rows,
-                                  prot_rows,   prot_rows,   text_rows,   text_rows};
+  const int64_t rows[KVQ_NSEG] = {packed_k_rows, packed_k_rows, packed_v_rows, packed_v_rows,
+                                  prot_k_rows,   prot_v_rows,   text_rows,     text_rows};
   int64_t off = 0;
   for (int s = 0; s < KVQ_NSEG; ++s) {
     L.off[s] = off;
@@ -141,6 +148,7 @@ void kvq_fill_params(const kvq_layout* L, kvq::Params* p) {
   p->G = d.group_size;
   p->n_prot = L->n_prot;
   p->n_packed = L->n_packed;
+  p->n_konly = L->n_konly;
   p->krow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES]);
   p->kszrow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_SZ]);
   p->vrow = static_cast<int32_t>(L->row_bytes[KVQ_SEG_V_CODES]);
@@ -150,6 +158,7 @@ void kvq_fill_params(const kvq_layout* L, kvq::Params* p) {
     p->slot[h] = L->slot[h];
     p->prot_head[h] = L->prot_head[h];
     p->packed_head[h] = L->packed_head[h];
+    p->konly_head[h] = L->konly_head[h];
   }
 }
 
@@ -161,16 +170,20 @@ kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target)
   P.NHC = (L->g + kvq::kNH - 1) / kvq::kNH;
   P.vsa = d.vis_start < T ? d.vis_start : T;
   P.vea = d.vis_end < T ? d.vis_end : T;
-  P.w_vis = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES] + L->row_bytes[KVQ_SEG_K_SZ] +
-                                 L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ]) +
+  const int64_t vrow = L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ];
+  P.w_vis = static_cast<int32_t>(L->row_bytes[KVQ_SEG_K_CODES] + L->row_bytes[KVQ_SEG_K_SZ] + vrow) +
             kvq::kPosCost;
+  P.w_kvis = static_cast<int32_t>(2 * kvq::kD + vrow) + kvq::kPosCost;
   P.U_p = d.B * L->n_prot * P.NHC;
+  P.U_k = d.B * L->n_konly * P.NHC;
   P.U = d.B * d.H_kv * P.NHC;
   P.ub_p = static_cast<int64_t>(T) * kvq::kBf16PosCost;
   const int64_t n_vis = P.vea - P.vsa;
+  P.ub_k = (static_cast<int64_t>(T) - n_vis) * kvq::kBf16PosCost + n_vis * P.w_kvis;
   P.ub_u = (static_cast<int64_t>(T) - n_vis) * kvq::kBf16PosCost + n_vis * P.w_vis;
   P.P_bytes = static_cast<int64_t>(P.U_p) * P.ub_p;
-  P.total = P.P_bytes + static_cast<int64_t>(P.U - P.U_p) * P.ub_u;
+  P.K_bytes = static_cast<int64_t>(P.U_k) * P.ub_k;
+  P.total = P.P_bytes + P.K_bytes + static_cast<int64_t>(P.U - P.U_p - P.U_k) * P.ub_u;
   // Chunks: the target (a whole number of CTAs per SM), but no chunk below
   // 8 Ki cost units and never more than KVQ_MAX_CTAS.
   int64_t C = n_chunks_target;
@@ -187,41 +200,51 @@ void kvq_plan_cuts(kvq::Plan* Pp, kvq::Cut* cuts) {
   kvq::Plan& P = *Pp;
   cuts[P.C] = Cut{P.U, 0};
   P.aligned = P.C >= P.U ? 1 : 0;
-  P.n_p = P.n_q = P.R = 0;
+  P.n_p = P.n_k = P.n_q = P.R = 0;
+  const int64_t U_q = P.U - P.U_p - P.U_k;
   if (!P.aligned) {
     // Equal-cost cuts of the concatenated stream of units.
     for (int32_t c = 0; c < P.C; ++c) {
       const int64_t X = (P.total * static_cast<int64_t>(c)) / P.C;
       if (X < P.P_bytes) {
         const int64_t u = X / P.ub_p;
-        cuts[c] = Cut{static_cast<int32_t>(u), kvq::unit_cut_pos(P, true, X - u * P.ub_p)};
-      } else {
-        const int64_t u = (X - P.P_bytes) / P.ub_u;
+        cuts[c] = Cut{static_cast<int32_t>(u), kvq::unit_cut_pos(P, kvq::kClsProt, X - u * P.ub_p)};
+      } else if (X < P.P_bytes + P.K_bytes) {
+        const int64_t u = (X - P.P_bytes) / P.ub_k;
         cuts[c] = Cut{P.U_p + static_cast<int32_t>(u),
-                      kvq::unit_cut_pos(P, false, X - P.P_bytes - u * P.ub_u)};
+                      kvq::unit_cut_pos(P, kvq::kClsKonly, X - P.P_bytes - u * P.ub_k)};
+      } else {
+        const int64_t Xu = X - P.P_bytes - P.K_bytes;
+        const int64_t u = Xu / P.ub_u;
+        cuts[c] = Cut{P.U_p + P.U_k + static_cast<int32_t>(u),
+                      kvq::unit_cut_pos(P, kvq::kClsPacked, Xu - u * P.ub_u)};
       }
     }
     return;
   }
-  // Per-unit chunks, n_p for each protected and n_q for each packed unit in
-  // proportion to their costs (at least one each); the R chunks left over
-  // go one each to the first R units.
-  const int64_t U_q = P.U - P.U_p;
-  int64_t n_p = P.U_p ? std::max<int64_t>(1, P.C * P.ub_p / P.total) : 0;
-  int64_t n_q = U_q ? std::max<int64_t>(1, P.C * P.ub_u / P.total) : 0;
-  while (n_p * P.U_p + n_q * U_q > P.C) {  // only when a share was raised to 1
-    if (n_p > 1 && (n_q <= 1 || n_p * P.ub_u >= n_q * P.ub_p)) --n_p; else --n_q;
+  // Per-unit chunks: n per unit of each class in proportion to its cost (at
+  // least one each); the R chunks left over go one each to the first R
+  // units.
+  const int64_t Uc[3] = {P.U_p, P.U_k, U_q};
+  const int64_t uc[3] = {P.ub_p, P.ub_k, P.ub_u};
+  int64_t n[3];
+  for (int k = 0; k < 3; ++k) n[k] = Uc[k] ? std::max<int64_t>(1, P.C * uc[k] / P.total) : 0;
+  while (n[0] * Uc[0] + n[1] * Uc[1] + n[2] * Uc[2] > P.C) {  // only when a share was raised to 1
+    int pick = -1;  // the class with the most chunks per unit of cost
+    for (int k = 0; k < 3; ++k)
+      if (Uc[k] && n[k] > 1 && (pick < 0 || n[k] * uc[pick] > n[pick] * uc[k])) pick = k;
+    --n[pick];  // exists: with every n at 1 the sum is U <= C
   }
-  const int64_t R = P.C - n_p * P.U_p - n_q * U_q;
-  P.n_p = static_cast<int32_t>(n_p);
-  P.n_q = static_cast<int32_t>(n_q);
+  const int64_t R = P.C - n[0] * Uc[0] - n[1] * Uc[1] - n[2] * Uc[2];
+  P.n_p = static_cast<int32_t>(n[0]);
+  P.n_k = static_cast<int32_t>(n[1]);
+  P.n_q = static_cast<int32_t>(n[2]);
   P.R = static_cast<int32_t>(R);
   int32_t c = 0;
   for (int32_t u = 0; u < P.U; ++u) {
-    const bool prot = u < P.U_p;
-    const int64_t n = (prot ? n_p : n_q) + (u < R ? 1 : 0);
-    const int64_t cost = prot ? P.ub_p : P.ub_u;
-    for (int64_t k = 0; k < n; ++k) cuts[c++] = Cut{u, kvq::unit_cut_pos(P, prot, cost * k / n)};
+    const int cls = kvq::unit_class(P, u);
+    const int64_t nu = n[cls] + (u < R ? 1 : 0);
+    for (int64_t k = 0; k < nu; ++k) cuts[c++] = Cut{u, kvq::unit_cut_pos(P, cls, uc[cls] * k / nu)};
   }
 }
 

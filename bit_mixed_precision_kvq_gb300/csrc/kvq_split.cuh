@@ -58,19 +58,27 @@ struct SplitSmem {
   int ncomb;  // fused step: CTAs combining the current unit
 };
 
-enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2 };
+// Tile kinds: bf16 text rows, bf16 protected visual rows, packed visual
+// rows, K-only visual rows (bf16 K + packed V).
+enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2, kTileKonly = 3 };
 
-// Walk the tiles of one piece [ps, pe) of a unit: text prefix, visual block,
-// text suffix, each cut into tiles.  f(kind, t0, n).
-template <typename F>
-__device__ __forceinline__ void walk_piece(const Params& p, bool prot, int ps, int pe, F&& f) {
+// Walk the tiles of one piece [ps, pe) of a unit of class cls: text prefix,
+// visual block, text suffix, each cut into tiles.  f(kind, t0, n).
+template <bool kKO, typename F>
+__device__ __forceinline__ void walk_piece(const Params& p, int cls, int ps, int pe, F&& f) {
   const int b1 = max(ps, min(pe, p.vs)), b2 = max(ps, min(pe, p.ve));
 #pragma unroll 1
   for (int seg = 0; seg < 3; ++seg) {  // selects, not an array: no local memory
     const int s0 = seg == 0 ? ps : (seg == 1 ? b1 : b2);
     const int s1 = seg == 0 ? b1 : (seg == 1 ? b2 : pe);
-    const int kind = seg == 1 ? (prot ? kTileProt : kTilePacked) : kTileText;
-    const int tt = kind == kTilePacked ? p.tt_pk : kTileBf16;
+    int kind, tt;
+    if constexpr (kKO) {
+      kind = seg == 1 ? (cls == kClsProt ? kTileProt : (cls == kClsKonly ? kTileKonly : kTilePacked)) : kTileText;
+      tt = kind == kTilePacked ? p.tt_pk : (kind == kTileKonly ? p.tt_ko : kTileBf16);
+    } else {
+      kind = seg == 1 ? (cls == kClsProt ? kTileProt : kTilePacked) : kTileText;
+      tt = kind == kTilePacked ? p.tt_pk : kTileBf16;
+    }
     for (int t0 = s0; t0 < s1; t0 += tt) f(kind, t0, min(tt, s1 - t0));
   }
 }
@@ -84,19 +92,30 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // 4 of them).  In the fused step the step's own row (position T - 1, the
 // last row of the last text tile) comes from the k_new / v_new inputs rather
 // than from the cache row that the launch itself writes.
-template <bool kStep, typename F>
+template <bool kStep, bool kKO, typename F>
 __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int kind, int t0,
                                              int n, F&& f) {
-  if (kind != kTilePacked) {
+  if (kKO && kind == kTileKonly) {
+    // bf16 K rows (protected K segment) + packed V rows and their scale/zero
+    const int64_t krow = prot_k_row(p, ui.b, kClsKonly, ui.slot) * p.Tv + (t0 - p.vs);
+    const int64_t vrow = packed_v_row(p, ui.b, kClsKonly, ui.slot) * p.Tv_pad + (t0 - p.vs);
+    const uint32_t bv = round16(n * p.vrow), bvs = round16(n * p.vszrow);
+    f(0u, p.seg[KVQ_SEG_PROT_K] + krow * (2 * kD), static_cast<uint32_t>(n) * (2 * kD));
+    f(static_cast<uint32_t>(p.ko_off_vc), p.seg[KVQ_SEG_V_CODES] + vrow * p.vrow, bv);
+    if (bvs) f(static_cast<uint32_t>(p.ko_off_vsz), p.seg[KVQ_SEG_V_SZ] + vrow * p.vszrow, bvs);
+  } else if (kind != kTilePacked) {
     int64_t row;
     const uint8_t *ks, *vs;
+    int64_t vrow_p = 0;
     if (kind == kTileText) {
       const int tr = t0 < p.vs ? t0 : t0 - p.Tv;
       row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
+      vrow_p = row;
       ks = p.seg[KVQ_SEG_TEXT_K];
       vs = p.seg[KVQ_SEG_TEXT_V];
     } else {
-      row = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
+      vrow_p = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
+      row = kKO ? prot_k_row(p, ui.b, kClsProt, ui.slot) * p.Tv + (t0 - p.vs) : vrow_p;
       ks = p.seg[KVQ_SEG_PROT_K];
       vs = p.seg[KVQ_SEG_PROT_V];
     }
@@ -106,27 +125,28 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
       const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
       if (head) {
         f(0u, ks + row * (2 * kD), head);
-        f(static_cast<uint32_t>(kBf16VOff), vs + row * (2 * kD), head);
+        f(static_cast<uint32_t>(kBf16VOff), vs + vrow_p * (2 * kD), head);
       }
       f(head, reinterpret_cast<const uint8_t*>(p.k_new + nrow), static_cast<uint32_t>(2 * kD));
       f(kBf16VOff + head, reinterpret_cast<const uint8_t*>(p.v_new + nrow), static_cast<uint32_t>(2 * kD));
     } else {
       f(0u, ks + row * (2 * kD), bytes);
-      f(static_cast<uint32_t>(kBf16VOff), vs + row * (2 * kD), bytes);
+      f(static_cast<uint32_t>(kBf16VOff), vs + vrow_p * (2 * kD), bytes);
     }
   } else {
     const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
+    const int64_t vrow = kKO ? packed_v_row(p, ui.b, kClsPacked, ui.slot) * p.Tv_pad + (t0 - p.vs) : row;
     const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
     const uint32_t bks = round16(n * p.kszrow), bvs = round16(n * p.vszrow);
     f(0u, p.seg[KVQ_SEG_K_CODES] + row * p.krow, bk);
-    f(static_cast<uint32_t>(p.pk_off_vc), p.seg[KVQ_SEG_V_CODES] + row * p.vrow, bv);
+    f(static_cast<uint32_t>(p.pk_off_vc), p.seg[KVQ_SEG_V_CODES] + vrow * p.vrow, bv);
     if (bks) f(static_cast<uint32_t>(p.pk_off_ksz), p.seg[KVQ_SEG_K_SZ] + row * p.kszrow, bks);
-    if (bvs) f(static_cast<uint32_t>(p.pk_off_vsz), p.seg[KVQ_SEG_V_SZ] + row * p.vszrow, bvs);
+    if (bvs) f(static_cast<uint32_t>(p.pk_off_vsz), p.seg[KVQ_SEG_V_SZ] + vrow * p.vszrow, bvs);
   }
 }
 
 // Walk the CTA's tiles: f(unit info, kind, t0, n).
-template <typename F>
+template <bool kKO, typename F>
 __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
@@ -134,8 +154,8 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   for (int u = a.u; u <= u_last; ++u) {
     const int ps = (u == a.u) ? a.p : 0;
     const int pe = (u == e.u) ? e.p : p.plan.T;
-    const UnitInfo ui = unit_info(p, u);
-    walk_piece(p, ui.prot, ps, pe, [&](int kind, int t0, int n) { f(ui, kind, t0, n); });
+    const UnitInfo ui = unit_info<kKO>(p, u);
+    walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) { f(ui, kind, t0, n); });
   }
 }
 
@@ -144,11 +164,12 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
 // other SMs' prefetches when the previous kernel does not overlap).  L2 is coherent with every SM's stores, so a
 // line that the previous kernel writes later is simply updated there; the
 // copies into shared memory all come after the wait.
+template <bool kKO>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   uint32_t budget = kPrefetchBytes;
-  walk_chunk(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+  walk_chunk<kKO>(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
     if (budget == 0) return;
-    tile_sources<false>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
+    tile_sources<false, kKO>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
       const uint32_t b = min(bytes, budget);
       if (b) prefetch_l2(src, b);
       budget -= b;
@@ -156,18 +177,18 @@ __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   });
 }
 
-template <bool kStep>
+template <bool kStep, bool kKO>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
   uint32_t it = 0;
-  walk_chunk(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+  walk_chunk<kKO>(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
     const int st = it % kStages;
     const uint32_t round = it / kStages;
     if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
     uint8_t* dst = sm.stage[st];
     uint32_t total = 0;
-    tile_sources<kStep>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
+    tile_sources<kStep, kKO>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
     mbar_arrive_expect_tx(&sm.full[st], total);
-    tile_sources<kStep>(p, ui, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
+    tile_sources<kStep, kKO>(p, ui, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
       bulk_g2s(dst + off, src, bytes, &sm.full[st]);
     });
     ++it;
@@ -823,7 +844,7 @@ __device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt) {
   return false;
 }
 
-template <int KB, int VB, int G, bool kStep, int NHP>
+template <int KB, int VB, int G, bool kStep, int NHP, bool kKO>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
@@ -837,7 +858,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   for (int u = a.u; u <= u_last; ++u) {
     const int ps = (u == a.u) ? a.p : 0;
     const int pe = (u == e.u) ? e.p : p.plan.T;
-    const UnitInfo ui = unit_info(p, u);
+    const UnitInfo ui = unit_info<kKO>(p, u);
     const int hq0 = ui.h * p.g + ui.hc * kNH;
     const int nh = min(kNH, p.g - ui.hc * kNH);
     if (u == a.u) pdl_wait();  // q (and the cache) may come from the previous kernel
@@ -933,7 +954,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       return nb;
     };
     if (ui.prot) {  // protected unit: bf16 rows only
-      walk_piece(p, true, ps, pe, [&](int kind, int t0, int n) {
+      walk_piece<kKO>(p, kClsProt, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
         const int nb = deal(n, 32, first);
@@ -943,7 +964,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         end_tile();
       });
     } else {
-      walk_piece(p, false, ps, pe, [&](int kind, int t0, int n) {
+      walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
         if (kind == kTilePacked) {
@@ -958,7 +979,19 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
             kblock<NHP, (KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
                 base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16 * NHP, n, sl2,
                 qb, zb, gid, tig, lane, acc);
-        } else {  // text rows of a packed unit
+        } else if (kKO && kind == kTileKonly) {  // bf16 K + packed V
+          const int nb = deal(n, 32, first);
+          if constexpr (VB < 16) {
+            if (first < nb && !packed_acc) {
+              acc_to_packed<VB>(acc);
+              packed_acc = true;
+            }
+          }
+          for (int kb = first; kb < nb; kb += kConsumerWarps)
+            kblock<2, kKBf16, (VB < 16 ? kVPacked : kVBf16D), 16, VB, G>(
+                base, nullptr, base + p.ko_off_vc, base + p.ko_off_vsz, kb * 32, n, sl2, qb, zb, gid, tig,
+                lane, acc);
+        } else {  // text rows of a packed or K-only unit
           const int nb = deal(n, 32, first);
           if constexpr (VB < 16) {
             if (first < nb && packed_acc) {
@@ -1080,7 +1113,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
 }
 
 // NHP: 16-row MMA halves per packed block (2 or 4; the launch's pk_halves).
-template <int KB, int VB, int G, bool kStep, int NHP>
+// kKO: the layout has K-only protected heads (a third unit class).
+template <int KB, int VB, int G, bool kStep, int NHP, bool kKO>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -1098,13 +1132,13 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
   __syncthreads();
   if (warp == kConsumerWarps) {
     if (lane == 0) {
-      producer_prefetch(p, blockIdx.x);
+      producer_prefetch<kKO>(p, blockIdx.x);
       pdl_wait();  // the previous kernel in the stream may have written the cache
-      producer_loop<kStep>(p, sm, blockIdx.x);
+      producer_loop<kStep, kKO>(p, sm, blockIdx.x);
     }
     return;
   }
-  consumer_loop<KB, VB, G, kStep, NHP>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G, kStep, NHP, kKO>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq

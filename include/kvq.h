@@ -78,10 +78,10 @@ typedef enum kvq_status {
 enum kvq_segment {
   KVQ_SEG_K_CODES = 0, /* uint32 [B][n_packed][Tv_pad][D*k_bits/32] (storage order above); bf16 rows if k_bits == 16 */
   KVQ_SEG_K_SZ = 1,    /* fp16 [B][n_packed][Tv_pad][2*D/G] = [z.., s..]; empty if k_bits == 16 */
-  KVQ_SEG_V_CODES = 2, /* as K_CODES with v_bits */
-  KVQ_SEG_V_SZ = 3,    /* as K_SZ with v_bits */
-  KVQ_SEG_PROT_K = 4,  /* bf16 [B][n_prot][Tv][D]: visual K of protected heads */
-  KVQ_SEG_PROT_V = 5,  /* bf16 [B][n_prot][Tv][D] */
+  KVQ_SEG_V_CODES = 2, /* as K_CODES with v_bits, [B][n_packed + n_konly][..]: packed heads, then K-only ones */
+  KVQ_SEG_V_SZ = 3,    /* as K_SZ with v_bits, [B][n_packed + n_konly][..] */
+  KVQ_SEG_PROT_K = 4,  /* bf16 [B][n_prot + n_konly][Tv][D]: visual K of protected, then K-only heads */
+  KVQ_SEG_PROT_V = 5,  /* bf16 [B][n_prot][Tv][D]: visual V of protected heads */
   KVQ_SEG_TEXT_K = 6,  /* bf16 [B][H_kv][T_cap - Tv][D]: every non-visual position */
   KVQ_SEG_TEXT_V = 7   /* bf16 [B][H_kv][T_cap - Tv][D] */
 };
@@ -98,22 +98,24 @@ typedef struct kvq_layout_desc {
   int32_t k_bits;     /* 2, 4, 8, or 16 (= bf16, unquantised) */
   int32_t v_bits;     /* 2, 4, 8, or 16 */
   int32_t group_size; /* G in {32, 64, 128}, groups of G consecutive elements along D */
-  uint8_t protected_heads[KVQ_MAX_HEADS]; /* 1 = visual K and V of that KV head stay bf16 */
+  uint8_t protected_heads[KVQ_MAX_HEADS]; /* 0 = quantised; 1 = visual K and V of that KV head
+                                             stay bf16; 2 = only its visual K stays bf16
+                                             (HeadGuard's "K, and V as needed") */
 } kvq_layout_desc;
 
 /* Derived layout (plain value; filled by kvq_cache_layout, read-only after). */
 typedef struct kvq_layout {
   kvq_layout_desc d;
   int32_t g;          /* H_q / H_kv */
-  int32_t n_prot;     /* protected KV heads */
+  int32_t n_prot;     /* KV heads with K and V protected (mode 1) */
   int32_t n_packed;   /* unprotected KV heads */
   int32_t Tv;         /* vis_end - vis_start: visual rows per (b, head) */
   int32_t Tv_pad;     /* Tv rounded up to a multiple of 16: row stride of the packed segments */
   int32_t T_text;     /* T_cap - Tv: text rows per (b, head) */
   int32_t units;      /* B * H_kv * ceil(g / KVQ_HEADS_PER_UNIT) */
-  int32_t slot[KVQ_MAX_HEADS];        /* head -> index among its kind (protected / packed) */
+  int32_t slot[KVQ_MAX_HEADS];        /* head -> index among its kind (protected / K-only / packed) */
   uint8_t prot_head[KVQ_MAX_HEADS];   /* protected slot -> head */
-  uint8_t packed_head[KVQ_MAX_HEADS]; /* packed slot -> head */
+  uint8_t packed_head[KVQ_MAX_HEADS]; /* packed slot -> head (mode 0) */
   int64_t row_bytes[KVQ_NSEG];        /* bytes of one row of each segment */
   int64_t off[KVQ_NSEG];              /* byte offset of each segment (256-byte aligned) */
   int64_t bytes[KVQ_NSEG];            /* payload bytes of each segment */
@@ -121,6 +123,8 @@ typedef struct kvq_layout {
   int64_t workspace_bytes;            /* decode workspace needed for any T <= T_cap */
   double eff_bits_k;                  /* stored bits per visual K value, scale/zero included */
   double eff_bits_v;
+  int32_t n_konly;                    /* KV heads with only K protected (mode 2) */
+  uint8_t konly_head[KVQ_MAX_HEADS];  /* K-only slot -> head */
 } kvq_layout;
 
 /*

@@ -229,8 +229,16 @@ def attention_weights(q_bf16: np.ndarray, khat: np.ndarray, hq: int, scale: floa
 def decode_reference(q_bf16, k_bf16, v_bf16, vis_start: int, vis_end: int, prot, k_bits: int,
                      v_bits: int, G: int, scale: float, threads: int = 0, plant: int = 0):
     """Whole decode step for one layer: reconstruct K and V under the policy,
-    then exact fp64 attention.  Returns (out, lse, khat, vhat)."""
-    khat, _ = reconstruct(k_bf16, vis_start, vis_end, prot, k_bits, G, plant)
-    vhat, _ = reconstruct(v_bf16, vis_start, vis_end, prot, v_bits, G, plant)
+    then exact fp64 attention.  Returns (out, lse, khat, vhat).  prot[h]: 0 =
+    quantised, 1 = K and V of the head's visual rows kept bf16, 2 = only its
+    K kept bf16 (HeadGuard brief: image Key, and Value as needed)."""
+    pm = [int(m) for m in np.asarray(prot).reshape(-1)]
+    k_prot = [1 if m in (1, 2) else 0 for m in pm]
+    if plant == 11:  # planted: a K-only head keeps its V in bf16 too
+        v_prot = [1 if m in (1, 2) else 0 for m in pm]
+    else:
+        v_prot = [1 if m == 1 else 0 for m in pm]
+    khat, _ = reconstruct(k_bf16, vis_start, vis_end, k_prot, k_bits, G, plant)
+    vhat, _ = reconstruct(v_bf16, vis_start, vis_end, v_prot, v_bits, G, plant)
     out, lse = attention(q_bf16, khat, vhat, scale, threads, plant)
     return out, lse, khat, vhat

@@ -3,7 +3,7 @@ its segments back, and compare them with the CPU oracle."""
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 from typing import List, Optional, Sequence
 
 import numpy as np
@@ -29,13 +29,15 @@ class Case:
     G: int
     prot: List[int]
     D: int = 128
+    konly: List[int] = field(default_factory=list)  # K-only protected heads
 
     def layout(self):
         return kvq.cache_layout(self.B, self.H_q, self.H_kv, self.D, self.T_cap, self.vs, self.ve,
-                                self.kb, self.vb, self.G, self.prot)
+                                self.kb, self.vb, self.G, self.prot, self.konly)
 
     def mask(self):
-        return [1 if h in self.prot else 0 for h in range(self.H_kv)]
+        """Protection mode per KV head: 1 K and V, 2 K only, 0 none."""
+        return [1 if h in self.prot else (2 if h in self.konly else 0) for h in range(self.H_kv)]
 
 
 def case_of(w: synth.Workload, layer: int, extra: int = 0) -> Case:
@@ -86,7 +88,8 @@ def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.nda
     Tvp = int(L.Tv_pad)
     b_sel = list(range(B)) if b_sel is None else list(b_sel)
     prot = [h for h in range(H) if h in c.prot]
-    pack = [h for h in range(H) if h not in c.prot]
+    konly = [h for h in range(H) if h in c.konly]
+    pack = [h for h in range(H) if h not in c.prot and h not in c.konly]
     nvis = max(0, min(t_hi, c.ve) - c.vs)
     n_rows = 0
     for which, x_np, nbits, sc, ssz, sp, stx in (
@@ -102,24 +105,28 @@ def check_append(L, c: Case, cache: torch.Tensor, k_np: np.ndarray, v_np: np.nda
                     f"{which} text suffix b={b}"
         if nvis == 0:
             continue
-        if prot:
-            pr = seg(L, cn, sp, np.uint16).reshape(B, len(prot), Tv, D)
+        # bf16 visual rows: K of protected then K-only heads; V of protected heads
+        bf = prot + konly if which == "k" else prot
+        # packed visual rows: K of packed heads; V of packed then K-only heads
+        pk = pack if which == "k" else pack + konly
+        if bf:
+            pr = seg(L, cn, sp, np.uint16).reshape(B, len(bf), Tv, D)
             for i, b in enumerate(b_sel):
-                assert np.array_equal(pr[b, :, :nvis], x_np[i][prot][:, c.vs:c.vs + nvis]), \
+                assert np.array_equal(pr[b, :, :nvis], x_np[i][bf][:, c.vs:c.vs + nvis]), \
                     f"{which} protected rows b={b}"
-        if not pack:
+        if not pk:
             continue
         if nbits == 16:
-            raw = seg(L, cn, sc, np.uint16).reshape(B, len(pack), Tvp, D)
+            raw = seg(L, cn, sc, np.uint16).reshape(B, len(pk), Tvp, D)
             for i, b in enumerate(b_sel):
-                assert np.array_equal(raw[b, :, :nvis], x_np[i][pack][:, c.vs:c.vs + nvis])
+                assert np.array_equal(raw[b, :, :nvis], x_np[i][pk][:, c.vs:c.vs + nvis])
             continue
         W = D * nbits // 32
         ng = D // c.G
-        words = seg(L, cn, sc, np.uint32).reshape(B, len(pack), Tvp, W)
-        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pack), Tvp, 2 * ng)
+        words = seg(L, cn, sc, np.uint32).reshape(B, len(pk), Tvp, W)
+        sz = seg(L, cn, ssz, np.uint16).reshape(B, len(pk), Tvp, 2 * ng)
         for i, b in enumerate(b_sel):
-            xin = np.ascontiguousarray(x_np[i][pack][:, c.vs:c.vs + nvis])
+            xin = np.ascontiguousarray(x_np[i][pk][:, c.vs:c.vs + nvis])
             w_ref, sz_ref = oracle.quantize_pack_rows_stored(xin, c.G, nbits, which)
             got_w = words[b, :, :nvis].reshape(-1, W)
             got_sz = sz[b, :, :nvis].reshape(-1, 2 * ng)

@@ -374,6 +374,28 @@ def pin_gqa_grouping(plant: int = 0):
         assert np.allclose(out[0, hq], hq // 2 + 1.0, atol=1e-13), hq
 
 
+def pin_konly_policy(plant: int = 0):
+    """A K-only protected head (HeadGuard brief: image Key kept, Value as
+    needed) keeps its visual K rows exactly and quantises its visual V rows
+    like an unprotected head; other heads are unaffected."""
+    rng = np.random.default_rng(11)
+    B, H, T, D, vs, ve = 1, 3, 24, 128, 4, 20
+    k = _bf16_bits_from_float(rng.standard_normal((B, H, T, D)))
+    v = _bf16_bits_from_float(rng.standard_normal((B, H, T, D)))
+    q = _bf16_bits_from_float(rng.standard_normal((B, H, D)))
+    _, _, kh, vh = oracle.decode_reference(q, k, v, vs, ve, [2, 1, 0], 4, 4, 32, 0.1, plant=plant)
+    kraw = _bf16_value(k).astype(np.float64)
+    vraw = _bf16_value(v).astype(np.float64)
+    assert np.array_equal(kh[:, 0], kraw[:, 0]) and np.array_equal(kh[:, 1], kraw[:, 1])
+    assert np.array_equal(vh[:, 1], vraw[:, 1])
+    # the K-only head's V and the packed head's K and V are quantised
+    for x, xr in ((vh[:, 0], vraw[:, 0]), (kh[:, 2], kraw[:, 2]), (vh[:, 2], vraw[:, 2])):
+        assert not np.array_equal(x[:, vs:ve], xr[:, vs:ve])
+        assert np.array_equal(x[:, :vs], xr[:, :vs]) and np.array_equal(x[:, ve:], xr[:, ve:])
+    vq, _ = oracle.reconstruct(v[:, :1], vs, ve, [0], 4, 32, plant)
+    assert np.array_equal(vh[:, 0], vq[:, 0])
+
+
 ALL_PINS = [
     pin_f16_conversion,
     pin_quantiser_bruteforce,
@@ -394,4 +416,5 @@ ALL_PINS = [
     pin_text_rows_untouched,
     pin_packed_row_count,
     pin_gqa_grouping,
+    pin_konly_policy,
 ]

@@ -50,7 +50,10 @@ int main(int argc, char** argv) {
     d.k_bits = bits[next(4)];
     d.v_bits = bits[next(4)];
     d.group_size = groups[next(3)];
-    for (int h = 0; h < d.H_kv; ++h) d.protected_heads[h] = next(5) == 0;
+    for (int h = 0; h < d.H_kv; ++h) {
+      const uint32_t r = next(8);
+      d.protected_heads[h] = r == 0 ? 1 : (r == 1 ? 2 : 0);  // some protected, some K-only
+    }
     kvq_layout L;
     if (kvq_cache_layout(&d, &L) != KVQ_OK) FAIL("layout rejected at case %d", it);
     const int T = 1 + static_cast<int>(next(static_cast<uint32_t>(d.T_cap)));
@@ -75,8 +78,8 @@ int main(int argc, char** argv) {
         covered[u] = pe;
         if (pe > ps) ++work_units;
         if (!slots.insert(static_cast<long>(u) + c).second) FAIL("case %d: slot %d reused", it, u + c);
-        const bool prot = u < P.U_p;
-        if (!prot && ps > P.vsa && ps < P.vea && (ps - P.vsa) % kvq::kVisAlign)
+        const bool bf16_only = kvq::unit_class(P, u) == kvq::kClsProt;
+        if (!bf16_only && ps > P.vsa && ps < P.vea && (ps - P.vsa) % kvq::kVisAlign)
           FAIL("case %d: unaligned visual cut %d", it, ps);
       }
       if (P.aligned && work_units > 1) FAIL("case %d: chunk %d spans %d units", it, c, work_units);

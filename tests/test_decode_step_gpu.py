@@ -64,6 +64,7 @@ CASES = [
     Case(2, 32, 2, 400, 5, 300, 8, 4, 32, [1]),         # g = 16: two head chunks per KV head
     Case(3, 8, 8, 300, 30, 250, 2, 8, 128, []),         # g = 1, B = 3
     Case(1, 40, 40, 320, 10, 290, 16, 16, 32, [3, 7]),  # MHA, bf16 "packed" segments
+    Case(2, 28, 4, 700, 14, 690, 4, 2, 64, [2], konly=[0]),  # K-only protected head
 ]
 
 

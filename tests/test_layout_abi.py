@@ -34,15 +34,18 @@ def _align(x, a):
     return (x + a - 1) // a * a
 
 
-def _expected(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot):
+def _expected(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot, konly):
     """Independent restatement of the documented segment shapes."""
     Tv = ve - vs
     Tvp = -(-Tv // 16) * 16
     npr = len(prot)
-    npk = Hkv - npr
+    nko = len(konly)
+    npk = Hkv - npr - nko
     rb = [D * kb // 8, 4 * D // G if kb < 16 else 0, D * vb // 8, 4 * D // G if vb < 16 else 0,
           2 * D, 2 * D, 2 * D, 2 * D]
-    rows = [B * npk * Tvp] * 4 + [B * npr * Tv] * 2 + [B * Hkv * (Tcap - Tv)] * 2
+    # K-only heads: K with the protected heads' K, V with the packed heads' V
+    rows = ([B * npk * Tvp] * 2 + [B * (npk + nko) * Tvp] * 2 + [B * (npr + nko) * Tv, B * npr * Tv]
+            + [B * Hkv * (Tcap - Tv)] * 2)
     off, offs = 0, []
     for r, n in zip(rb, rows):
         offs.append(off)
@@ -51,35 +54,41 @@ def _expected(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot):
 
 
 CASES = [
-    (1, 4, 1, 128, 257, 14, 256, 4, 4, 32, []),
-    (1, 28, 4, 128, 6288, 14, 6287, 4, 2, 64, [0]),
-    (16, 32, 32, 128, 617, 40, 616, 8, 4, 32, [1, 5, 9, 30]),
-    (8, 32, 8, 128, 32769, 32, 32768, 2, 2, 32, [3]),
-    (32, 40, 40, 128, 2941, 60, 2940, 8, 8, 64, [0, 1, 2, 3, 39]),
-    (3, 12, 4, 128, 100, 0, 100, 16, 2, 128, [0, 1, 2, 3]),
-    (2, 2, 2, 128, 50, 10, 10, 4, 16, 32, []),
+    (1, 4, 1, 128, 257, 14, 256, 4, 4, 32, [], []),
+    (1, 28, 4, 128, 6288, 14, 6287, 4, 2, 64, [0], []),
+    (16, 32, 32, 128, 617, 40, 616, 8, 4, 32, [1, 5, 9, 30], []),
+    (8, 32, 8, 128, 32769, 32, 32768, 2, 2, 32, [3], []),
+    (32, 40, 40, 128, 2941, 60, 2940, 8, 8, 64, [0, 1, 2, 3, 39], []),
+    (3, 12, 4, 128, 100, 0, 100, 16, 2, 128, [0, 1, 2, 3], []),
+    (2, 2, 2, 128, 50, 10, 10, 4, 16, 32, [], []),
+    (1, 28, 4, 128, 6288, 14, 6287, 4, 2, 64, [], [0]),          # K-only protection
+    (4, 32, 8, 128, 1000, 8, 990, 2, 4, 32, [5], [1, 6, 7]),     # both kinds
 ]
 
 
 @pytest.mark.parametrize("case", CASES)
 def test_layout_matches_formula(lib, case):
-    B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot = case
-    L = kvq.cache_layout(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot)
+    B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot, konly = case
+    L = kvq.cache_layout(B, Hq, Hkv, D, Tcap, vs, ve, kb, vb, G, prot, konly)
     rb, rows, offs, total = _expected(*case)
     assert list(L.row_bytes) == rb
     assert list(L.bytes) == [r * n for r, n in zip(rb, rows)]
     assert list(L.off) == offs and L.total_bytes == total
     assert all(o % 256 == 0 for o in L.off)
-    assert L.g == Hq // Hkv and L.n_prot == len(prot) and L.n_packed == Hkv - len(prot)
+    assert L.g == Hq // Hkv and L.n_prot == len(prot) and L.n_konly == len(konly)
+    assert L.n_packed == Hkv - len(prot) - len(konly)
     assert L.Tv == ve - vs and L.T_text == Tcap - (ve - vs) and L.Tv_pad == -(-(ve - vs) // 16) * 16
     nhc = -(-(Hq // Hkv) // 8)
     assert L.units == B * Hkv * nhc
     # head -> slot -> head round trip
-    ps = pk = 0
+    ps = pk = ko = 0
     for h in range(Hkv):
         if h in prot:
             assert L.slot[h] == ps and L.prot_head[ps] == h
             ps += 1
+        elif h in konly:
+            assert L.slot[h] == ko and L.konly_head[ko] == h
+            ko += 1
         else:
             assert L.slot[h] == pk and L.packed_head[pk] == h
             pk += 1
@@ -120,6 +129,15 @@ def test_layout_unsupported_head_dim(lib):
 def test_layout_rejects_mask_beyond_heads(lib):
     with pytest.raises(kvq.KvqError):
         kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [5])
+    with pytest.raises(kvq.KvqError):
+        kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [], [4])
+
+
+def test_layout_rejects_unknown_protection_mode(lib):
+    d = kvq.LayoutDesc(1, 8, 4, 128, 256, 10, 200, 4, 4, 32)
+    d.protected_heads[1] = 3
+    out = kvq.Layout()
+    assert lib.kvq_cache_layout(ctypes.byref(d), ctypes.byref(out)) == 1
 
 
 # Fake, never-dereferenced device addresses: every case below must be rejected

@@ -23,6 +23,7 @@ PLANTS = {
     8: "softmax scale dropped",
     9: "scale uses 2^b steps instead of 2^b - 1",
     10: "2-bit K storage slots of a register pair swapped",
+    11: "K-only protected head keeps its V in bf16 too",
 }
 
 

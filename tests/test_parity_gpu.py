@@ -140,7 +140,9 @@ def _fuzz_cases(n=40, seed=99):
             vs = min(T, int(rng.integers(0, 20)))
             ve = vs + int(rng.integers(0, T - vs + 1))
         prot = [h for h in range(H_kv) if rng.random() < 0.3]
-        out.append((i, Case(B, g * H_kv, H_kv, T, vs, ve, kb, vb, G, prot)))
+        # every other case also has K-only protected heads
+        konly = [h for h in range(H_kv) if h not in prot and (h + i) % 3 == 1] if i % 2 == 0 else []
+        out.append((i, Case(B, g * H_kv, H_kv, T, vs, ve, kb, vb, G, prot, konly=konly)))
     return out
 
 
@@ -149,6 +151,27 @@ def test_fuzz(cuda_dev, kvq, i, c):
     q, k, v = synth.random_case(1000 + i, c.B, c.H_q, c.H_kv, c.D, c.T_cap, cuda_dev,
                                 scale_k=float(1 + (i % 3)))
     _run_full(c, q, k, v, c.T_cap)
+
+
+KONLY_CASES = [
+    # B, H_q, H_kv, T_cap, vs, ve, kb, vb, G, protected, K-only
+    Case(1, 28, 4, 6288, 14, 6287, 4, 2, 64, [], konly=[0]),        # LLaVA-OV shape, head 0 K-only
+    Case(2, 32, 8, 1500, 32, 1500, 2, 2, 32, [3], konly=[0, 5]),    # both kinds, long visual tail
+    Case(3, 16, 16, 300, 10, 290, 8, 4, 32, [1], konly=[2, 3, 9]),  # MHA
+    Case(1, 8, 2, 500, 0, 500, 4, 16, 128, [], konly=[1]),          # bf16 V segment
+]
+
+
+@pytest.mark.parametrize("ci", range(len(KONLY_CASES)))
+def test_konly_heads(cuda_dev, kvq, ci):
+    """HeadGuard's "K, and V as needed": K-only protected heads keep their
+    visual K in bf16 and quantise their V; storage bit-exact, attention
+    within the bar."""
+    c = KONLY_CASES[ci]
+    q, k, v = synth.random_case(1200 + ci, c.B, c.H_q, c.H_kv, c.D, c.T_cap, cuda_dev)
+    n, worst = _run_full(c, q, k, v, c.T_cap)
+    assert n > 0
+    print(f"konly {ci}: worst err/max|V| = {worst:.2e}")
 
 
 def test_chunked_appends_equal_one_append(cuda_dev, kvq):
