@@ -18,7 +18,8 @@ __all__ = [
     "KvqError", "load", "lib_path", "cache_layout", "quantize_append", "decode_attention",
     "kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention", "KVQ_MAX_HEADS",
     "decode_attention_static_ws", "kvq_decode_attention_static_ws", "STATIC_WS_BYTES",
-    "decode_step", "kvq_decode_step",
+    "decode_step", "kvq_decode_step", "decode_attention_ragged", "kvq_decode_attention_ragged",
+    "decode_step_ragged", "kvq_decode_step_ragged",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
@@ -30,7 +31,7 @@ KVQ_NSEG = 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
 EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
-                    "kvq_decode_step",
+                    "kvq_decode_step", "kvq_decode_attention_ragged", "kvq_decode_step_ragged",
                     "kvq_decode_attention_static_ws", "kvq_last_cuda_error", "kvq_status_string"]
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
@@ -98,6 +99,11 @@ def load() -> ctypes.CDLL:
     lib.kvq_decode_attention.restype = ctypes.c_int
     lib.kvq_decode_step.argtypes = [ctypes.POINTER(Layout), P, P, P, P, i32, f32, P, P, P, sz, P]
     lib.kvq_decode_step.restype = ctypes.c_int
+    lib.kvq_decode_attention_ragged.argtypes = [ctypes.POINTER(Layout), P, P, P, i32, f32, P, P, P, sz, P]
+    lib.kvq_decode_attention_ragged.restype = ctypes.c_int
+    lib.kvq_decode_step_ragged.argtypes = [ctypes.POINTER(Layout), P, P, P, P, P, i32, f32, P, P, P, sz,
+                                           P]
+    lib.kvq_decode_step_ragged.restype = ctypes.c_int
     lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
     lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
     lib.kvq_last_cuda_error.argtypes = []
@@ -195,6 +201,42 @@ def decode_step(L: Layout, cache, q, k_new, v_new, t_new: int, out,
         raise KvqError(st, "kvq_decode_step")
 
 
+def decode_attention_ragged(L: Layout, cache, q, seq_len, T_max: int, out,
+                            softmax_scale: Optional[float] = None, lse=None, workspace=None,
+                            ws_bytes: Optional[int] = None, stream=None) -> None:
+    """kvq_decode_attention_ragged: sequence b attends positions
+    [0, seq_len[b]) (seq_len: device int32 [B]; an entry outside [1, T_max]
+    marks an inactive sequence, whose outputs are zero and lse -inf)."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kvq_decode_attention_ragged(ctypes.byref(L), _addr(cache), _addr(q), _addr(seq_len),
+                                            int(T_max), float(softmax_scale), _addr(out), _addr(lse),
+                                            _addr(workspace), int(ws_bytes), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_attention_ragged")
+
+
+def decode_step_ragged(L: Layout, cache, q, k_new, v_new, t_new, T_max: int, out,
+                       softmax_scale: Optional[float] = None, lse=None, workspace=None,
+                       ws_bytes: Optional[int] = None, stream=None) -> None:
+    """kvq_decode_step_ragged: sequence b stores its row at t_new[b] (device
+    int32 [B]) and attends [0, t_new[b]]; an entry outside [0, T_max) or
+    inside the visual range marks an inactive sequence (nothing stored,
+    outputs zero, lse -inf).  Workspace rules as for decode_step."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kvq_decode_step_ragged(ctypes.byref(L), _addr(cache), _addr(q), _addr(k_new),
+                                       _addr(v_new), _addr(t_new), int(T_max), float(softmax_scale),
+                                       _addr(out), _addr(lse), _addr(workspace), int(ws_bytes),
+                                       _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_step_ragged")
+
+
 def decode_attention_static_ws(L: Layout, cache, q, T: int, out,
                                softmax_scale: Optional[float] = None, lse=None,
                                stream=None) -> None:
@@ -216,3 +258,6 @@ kvq_cache_layout = cache_layout
 kvq_quantize_append = quantize_append
 kvq_decode_attention = decode_attention
 kvq_decode_attention_static_ws = decode_attention_static_ws
+kvq_decode_step = decode_step
+kvq_decode_attention_ragged = decode_attention_ragged
+kvq_decode_step_ragged = decode_step_ragged

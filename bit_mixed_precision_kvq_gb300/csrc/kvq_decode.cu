@@ -144,6 +144,7 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   const int64_t o_bytes = (slots * kvq::kNH * kvq::kD * 4 + 255) / 256 * 256;
   p->ws_ml = reinterpret_cast<float*>(ws + cnt_bytes + o_bytes);
   p->scale_log2 = softmax_scale * 1.4426950408889634f;
+  p->seq_len = nullptr;  // uniform call; the ragged entry points set it
   p->plan = kvq_make_plan(L, T, n_sm);  // one CTA per SM
   kvq_plan_cuts(&p->plan, p->cuts);
   p->pk_halves = packed_halves(p->plan, L);
@@ -157,56 +158,43 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
 constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
 static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
 
-}  // namespace
 
-extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
-                                           int32_t T, float softmax_scale, void* out_bf16, float* lse,
-                                           void* workspace, size_t ws_bytes, void* stream) {
-  static kvq::Params p;  // large (cut table): keep it off the host stack
-  static std::mutex call_mu;
-  std::lock_guard<std::mutex> call_lock(call_mu);
-  kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace, ws_bytes, &p);
-  if (st != KVQ_OK) return st;
-  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p.pk_halves,
+// The split kernel and the combine of one decode call (p prepared).
+kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
+  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p->pk_halves,
                                        L->n_konly > 0);
   if (!split) return KVQ_ERR_UNSUPPORTED;
-  if ((st = prepare_split(split, kSplitSmemBytes)) != KVQ_OK) return st;
-  if (kvq_launch_pdl(split, p.plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, &p) != 0)
+  kvq_status st = prepare_split(split, kSplitSmemBytes);
+  if (st != KVQ_OK) return st;
+  if (kvq_launch_pdl(split, p->plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, p) != 0)
     return KVQ_ERR_CUDA;
   if (kvq_launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), L->d.B * L->d.H_q,
-                     kvq::kCombineWarps * 32, 0, stream, &p) != 0)
+                     kvq::kCombineWarps * 32, 0, stream, p) != 0)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 
-extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
-                                      const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,
-                                      float softmax_scale, void* out_bf16, float* lse, void* workspace,
-                                      size_t ws_bytes, void* stream) {
-  static kvq::Params p;
-  static std::mutex call_mu;
-  std::lock_guard<std::mutex> call_lock(call_mu);
+// Checks of the fused step's new rows.
+kvq_status step_rows_ok(const kvq_layout* L, const void* k_new_bf16, const void* v_new_bf16) {
   if (!L || !k_new_bf16 || !v_new_bf16) return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(k_new_bf16) % 16 || reinterpret_cast<uintptr_t>(v_new_bf16) % 16)
     return KVQ_ERR_INVALID_ARG;
-  if (t_new < 0 || t_new >= L->d.T_cap) return KVQ_ERR_INVALID_ARG;
-  if (t_new >= L->d.vis_start && t_new < L->d.vis_end) return KVQ_ERR_INVALID_ARG;
-  kvq_status st = decode_params(L, cache, q_bf16, t_new + 1, softmax_scale, out_bf16, lse, workspace,
-                                ws_bytes, &p);
-  if (st != KVQ_OK) return st;
-  p.k_new = static_cast<const uint16_t*>(k_new_bf16);
-  p.v_new = static_cast<const uint16_t*>(v_new_bf16);
-  p.t_new = t_new;
-  const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p.pk_halves,
+  return KVQ_OK;
+}
+
+// The fused step's single launch (p prepared).  Cooperative: a combining CTA
+// may wait for other CTAs of its unit, so all CTAs must be resident together
+// (one per SM, C <= SM count).  Programmatic serialisation is added while
+// the runtime accepts both.
+kvq_status launch_step(const kvq_layout* L, kvq::Params* p, void* stream) {
+  const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p->pk_halves,
                                     L->n_konly > 0);
   if (!fn) return KVQ_ERR_UNSUPPORTED;
-  if ((st = prepare_split(fn, kSplitSmemBytes)) != KVQ_OK) return st;
-  // Cooperative launch: a combining CTA may wait for other CTAs of its unit,
-  // so all CTAs must be resident together (one per SM, C <= SM count).
-  // Programmatic serialisation is added while the runtime accepts both.
+  const kvq_status st = prepare_split(fn, kSplitSmemBytes);
+  if (st != KVQ_OK) return st;
   static int pdl_ok = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.plan.C);
+  cfg.gridDim = dim3(p->plan.C);
   cfg.blockDim = dim3(kvq::kSplitThreads);
   cfg.dynamicSmemBytes = kSplitSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -216,7 +204,7 @@ extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const vo
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  void* args[1] = {&p};
+  void* args[1] = {p};
   cudaError_t e = cudaErrorUnknown;
   if (pdl_ok) {
     cfg.numAttrs = 2;
@@ -232,4 +220,74 @@ extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const vo
   }
   if (e != cudaSuccess) return kvq_cuda_fail(e);
   return KVQ_OK;
+}
+
+// One parameter block for every decode entry point: it is large (the cut
+// table), so it stays off the host stack, and calls are serialised on it.
+std::mutex g_call_mu;
+kvq::Params g_params;
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                           int32_t T, float softmax_scale, void* out_bf16, float* lse,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+  std::lock_guard<std::mutex> lock(g_call_mu);
+  kvq::Params* p = &g_params;
+  const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
+                                      ws_bytes, p);
+  if (st != KVQ_OK) return st;
+  return launch_decode(L, p, stream);
+}
+
+extern "C" kvq_status kvq_decode_attention_ragged(const kvq_layout* L, const void* cache,
+                                                  const void* q_bf16, const int32_t* seq_len,
+                                                  int32_t T_max, float softmax_scale, void* out_bf16,
+                                                  float* lse, void* workspace, size_t ws_bytes,
+                                                  void* stream) {
+  std::lock_guard<std::mutex> lock(g_call_mu);
+  if (!seq_len || reinterpret_cast<uintptr_t>(seq_len) % 4) return KVQ_ERR_INVALID_ARG;
+  kvq::Params* p = &g_params;
+  const kvq_status st = decode_params(L, cache, q_bf16, T_max, softmax_scale, out_bf16, lse, workspace,
+                                      ws_bytes, p);
+  if (st != KVQ_OK) return st;
+  p->seq_len = seq_len;
+  return launch_decode(L, p, stream);
+}
+
+extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
+                                      const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,
+                                      float softmax_scale, void* out_bf16, float* lse, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  std::lock_guard<std::mutex> lock(g_call_mu);
+  kvq_status st = step_rows_ok(L, k_new_bf16, v_new_bf16);
+  if (st != KVQ_OK) return st;
+  if (t_new < 0 || t_new >= L->d.T_cap) return KVQ_ERR_INVALID_ARG;
+  if (t_new >= L->d.vis_start && t_new < L->d.vis_end) return KVQ_ERR_INVALID_ARG;
+  kvq::Params* p = &g_params;
+  st = decode_params(L, cache, q_bf16, t_new + 1, softmax_scale, out_bf16, lse, workspace, ws_bytes, p);
+  if (st != KVQ_OK) return st;
+  p->k_new = static_cast<const uint16_t*>(k_new_bf16);
+  p->v_new = static_cast<const uint16_t*>(v_new_bf16);
+  p->t_new = t_new;
+  return launch_step(L, p, stream);
+}
+
+extern "C" kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, const void* q_bf16,
+                                             const void* k_new_bf16, const void* v_new_bf16,
+                                             const int32_t* t_new, int32_t T_max, float softmax_scale,
+                                             void* out_bf16, float* lse, void* workspace, size_t ws_bytes,
+                                             void* stream) {
+  std::lock_guard<std::mutex> lock(g_call_mu);
+  kvq_status st = step_rows_ok(L, k_new_bf16, v_new_bf16);
+  if (st != KVQ_OK) return st;
+  if (!t_new || reinterpret_cast<uintptr_t>(t_new) % 4) return KVQ_ERR_INVALID_ARG;
+  kvq::Params* p = &g_params;
+  st = decode_params(L, cache, q_bf16, T_max, softmax_scale, out_bf16, lse, workspace, ws_bytes, p);
+  if (st != KVQ_OK) return st;
+  p->k_new = static_cast<const uint16_t*>(k_new_bf16);
+  p->v_new = static_cast<const uint16_t*>(v_new_bf16);
+  p->t_new = T_max - 1;  // the largest step position a sequence may have
+  p->seq_len = t_new;
+  return launch_step(L, p, stream);
 }

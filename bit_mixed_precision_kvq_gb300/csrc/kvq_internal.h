@@ -196,6 +196,9 @@ struct Params {
   int32_t n_konly;
   int32_t tt_ko;                       // positions per K-only tile (bf16 K + packed V rows)
   int32_t ko_off_vc, ko_off_vsz;       // K-only-tile offsets in a stage
+  // ragged calls: device int32 [B] of attended positions (decode) or step
+  // positions (fused step) per sequence; null for uniform calls
+  const int32_t* seq_len;
 };
 
 // unit -> (b, head, hc, slot, class).  kKO: the layout may have K-only

@@ -89,12 +89,13 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // Producer
 // ---------------------------------------------------------------------------
 // The bulk copies of one tile, as f(stage offset, source, bytes) calls (2 to
-// 4 of them).  In the fused step the step's own row (position T - 1, the
-// last row of the last text tile) comes from the k_new / v_new inputs rather
-// than from the cache row that the launch itself writes.
+// 4 of them).  In the fused step the step's own row (position Tu - 1 of a
+// unit whose sequence attends [0, Tu): the last row of its last text tile)
+// comes from the k_new / v_new inputs rather than from the cache row that
+// the launch itself writes.
 template <bool kStep, bool kKO, typename F>
-__device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int kind, int t0,
-                                             int n, F&& f) {
+__device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int Tu, int kind,
+                                             int t0, int n, F&& f) {
   if (kKO && kind == kTileKonly) {
     // bf16 K rows (protected K segment) + packed V rows and their scale/zero
     const int64_t krow = prot_k_row(p, ui.b, kClsKonly, ui.slot) * p.Tv + (t0 - p.vs);
@@ -120,7 +121,7 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
       vs = p.seg[KVQ_SEG_PROT_V];
     }
     const uint32_t bytes = static_cast<uint32_t>(n) * (2 * kD);
-    if (kStep && kind == kTileText && t0 + n == p.plan.T) {
+    if (kStep && kind == kTileText && t0 + n == Tu) {
       const uint32_t head = bytes - 2 * kD;
       const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
       if (head) {
@@ -145,17 +146,36 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
   }
 }
 
-// Walk the CTA's tiles: f(unit info, kind, t0, n).
-template <bool kKO, typename F>
+// Positions attended by sequence b: the plan's T for uniform calls; for
+// ragged calls seq_len[b] (decode) or t_new[b] + 1 (fused step, where the
+// step position must be a text position), and 0 -- an inactive sequence --
+// for an entry outside that range.  Read only after the dependency wait.
+template <bool kStep>
+__device__ __forceinline__ int seq_end(const Params& p, int b) {
+  if (p.seq_len == nullptr) return p.plan.T;
+  const int t = p.seq_len[b];
+  if constexpr (kStep) {
+    const bool ok = t >= 0 && t < p.plan.T && (t < p.vs || t >= p.ve);
+    return ok ? t + 1 : 0;
+  } else {
+    return (t >= 1 && t <= p.plan.T) ? t : 0;
+  }
+}
+
+// Walk the CTA's tiles: f(unit info, unit end Tu, kind, t0, n).  kEnds:
+// clip every unit at its sequence's end (seq_end); the L2 prefetch, issued
+// before the dependency wait, walks the unclipped pieces instead.
+template <bool kKO, bool kStep, bool kEnds, typename F>
 __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
   const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
   for (int u = a.u; u <= u_last; ++u) {
-    const int ps = (u == a.u) ? a.p : 0;
-    const int pe = (u == e.u) ? e.p : p.plan.T;
     const UnitInfo ui = unit_info<kKO>(p, u);
-    walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) { f(ui, kind, t0, n); });
+    const int Tu = kEnds ? seq_end<kStep>(p, ui.b) : p.plan.T;
+    const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
+    const int ps = min((u == a.u) ? a.p : 0, pe);
+    walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) { f(ui, Tu, kind, t0, n); });
   }
 }
 
@@ -167,9 +187,9 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
 template <bool kKO>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   uint32_t budget = kPrefetchBytes;
-  walk_chunk<kKO>(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+  walk_chunk<kKO, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     if (budget == 0) return;
-    tile_sources<false, kKO>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
+    tile_sources<false, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
       const uint32_t b = min(bytes, budget);
       if (b) prefetch_l2(src, b);
       budget -= b;
@@ -180,15 +200,15 @@ __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
 template <bool kStep, bool kKO>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
   uint32_t it = 0;
-  walk_chunk<kKO>(p, c, [&](const UnitInfo& ui, int kind, int t0, int n) {
+  walk_chunk<kKO, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     const int st = it % kStages;
     const uint32_t round = it / kStages;
     if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
     uint8_t* dst = sm.stage[st];
     uint32_t total = 0;
-    tile_sources<kStep, kKO>(p, ui, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
+    tile_sources<kStep, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
     mbar_arrive_expect_tx(&sm.full[st], total);
-    tile_sources<kStep, kKO>(p, ui, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
+    tile_sources<kStep, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
       bulk_g2s(dst + off, src, bytes, &sm.full[st]);
     });
     ++it;
@@ -821,7 +841,7 @@ __device__ __forceinline__ void combine_row(const Params& p, int u, int j, int c
       Ot.z = fmaf(o.z, sc, Ot.z);
       Ot.w = fmaf(o.w, sc, Ot.w);
     }
-    float inv = 1.0f / Lt;
+    float inv = Lt > 0.f ? 1.0f / Lt : 0.f;  // Lt = 0: an inactive sequence (out 0, lse -inf)
     if (nan) inv = __int_as_float(0x7fffffff);
     uint2 packed;
     packed.x = static_cast<uint32_t>(f32_to_bf16_bits(Ot.x * inv)) |
@@ -856,12 +876,13 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   uint32_t it = 0;    // tiles seen (stage ring position)
   uint32_t gblk = 0;  // 32-position blocks dealt so far (round-robin over warps)
   for (int u = a.u; u <= u_last; ++u) {
-    const int ps = (u == a.u) ? a.p : 0;
-    const int pe = (u == e.u) ? e.p : p.plan.T;
     const UnitInfo ui = unit_info<kKO>(p, u);
     const int hq0 = ui.h * p.g + ui.hc * kNH;
     const int nh = min(kNH, p.g - ui.hc * kNH);
     if (u == a.u) pdl_wait();  // q (and the cache) may come from the previous kernel
+    const int Tu = seq_end<kStep>(p, ui.b);
+    const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
+    const int ps = min((u == a.u) ? a.p : 0, pe);
 
     // q of head column gid as the B operand, in the permuted d order; group sums.
     uint32_t qb[8][2];
@@ -927,9 +948,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
       const uint8_t* base = sm.stage[st];
-      if (kStep && kind == kTileText && t0 + n == p.plan.T && ui.hc == 0 && warp == 0) {
-        // lanes 0-15 the K row, lanes 16-31 the V row
-        const int tr = p.t_new < p.vs ? p.t_new : p.t_new - p.Tv;
+      if (kStep && kind == kTileText && t0 + n == Tu && ui.hc == 0 && warp == 0) {
+        // lanes 0-15 the K row, lanes 16-31 the V row (position Tu - 1)
+        const int tr = Tu - 1 < p.vs ? Tu - 1 : Tu - 1 - p.Tv;
         const int64_t row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
         const int half = lane >> 4, q = lane & 15;
         const uint4 w = *reinterpret_cast<const uint4*>(base + (half ? kBf16VOff : 0) +
@@ -1060,7 +1081,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       }
       if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
       if (sole) {
-        const float inv = (M != M) ? M : 1.0f / L;
+        const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
         p.out[(row0 + j) * kD + d] = f32_to_bf16_bits(O * inv);
         if (d == 0 && p.lse) p.lse[row0 + j] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
       } else {

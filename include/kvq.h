@@ -208,6 +208,47 @@ kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
                            float softmax_scale, void* out_bf16, float* lse, void* workspace,
                            size_t ws_bytes, void* stream);
 
+/*
+ * Ragged batches: every sequence of the batch has its own length, held in a
+ * device array that the caller's decode loop updates on the GPU (so the
+ * calls can be captured once in a CUDA graph and replayed as lengths grow).
+ * The layout (visual range, protected heads) is shared by the batch; a
+ * sequence attends only to its own positions.  Work is split over T_max
+ * positions per sequence, so the cost is that of a uniform call of length
+ * T_max whatever the lengths are.
+ *
+ * kvq_decode_attention_ragged -- kvq_decode_attention with sequence b
+ * attending positions [0, seq_len[b]).
+ *   seq_len   device int32 [B], 4-byte aligned, read by the kernels (after
+ *             the previous kernel of the stream has finished)
+ *   T_max     1 <= T_max <= T_cap; entries are meant to lie in [1, T_max]
+ * An entry outside [1, T_max] marks an inactive sequence: its outputs are
+ * zero and its lse is -inf (no error is returned; the host never sees the
+ * array).  The other arguments are those of kvq_decode_attention.
+ */
+kvq_status kvq_decode_attention_ragged(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                       const int32_t* seq_len, int32_t T_max, float softmax_scale,
+                                       void* out_bf16, float* lse, void* workspace, size_t ws_bytes,
+                                       void* stream);
+
+/*
+ * kvq_decode_step_ragged -- kvq_decode_step with one step position per
+ * sequence: sequence b stores its K/V row at t_new[b] and attends positions
+ * [0, t_new[b]].
+ *   t_new     device int32 [B], 4-byte aligned
+ *   T_max     1 <= T_max <= T_cap; entries are meant to lie in [0, T_max)
+ *             and outside [vis_start, vis_end)
+ * An entry outside that set marks an inactive sequence: nothing is stored
+ * for it, its outputs are zero and its lse is -inf.  The workspace rules
+ * are those of kvq_decode_step (the arrival counters are shared by both
+ * step entry points).
+ */
+kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, const void* q_bf16,
+                                  const void* k_new_bf16, const void* v_new_bf16,
+                                  const int32_t* t_new, int32_t T_max, float softmax_scale,
+                                  void* out_bf16, float* lse, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
 /* Size in bytes of the device scratch array used by
  * kvq_decode_attention_static_ws (16 MiB: enough for layouts with up to
  * 3008 units, i.e. B * H_kv * ceil(g/8) <= 3008). */

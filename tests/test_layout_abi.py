@@ -198,6 +198,32 @@ def test_decode_step_argument_checks(lib):
         kvq.decode_step(L, FAKE, FAKE, FAKE, FAKE, 220, FAKE, float("inf"), 0, FAKE, ws, stream=0)
 
 
+def test_ragged_argument_checks(lib):
+    """The ragged entry points check what the host sees (the length array's
+    pointer, T_max, the rest as for the uniform calls); the lengths
+    themselves live on the device and are checked by the kernels."""
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ws = L.workspace_bytes
+    ok = dict(cache=FAKE, q=FAKE, sl=FAKE, T=256, out=FAKE, lse=0, ws=FAKE, ws_bytes=ws)
+    for bad, code in ((dict(sl=0), 1), (dict(sl=FAKE + 2), 1), (dict(T=0), 1), (dict(T=257), 1),
+                      (dict(cache=0), 1), (dict(q=FAKE + 8), 1), (dict(ws=0), 1),
+                      (dict(ws_bytes=ws - 1), 3)):
+        a = dict(ok)
+        a.update(bad)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_attention_ragged(L, a["cache"], a["q"], a["sl"], a["T"], a["out"], 0.1,
+                                        a["lse"], a["ws"], a["ws_bytes"], stream=0)
+        assert e.value.status == code, bad
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_step_ragged(L, a["cache"], a["q"], FAKE, FAKE, a["sl"], a["T"], a["out"], 0.1,
+                                   a["lse"], a["ws"], a["ws_bytes"], stream=0)
+        assert e.value.status == code, bad
+    for kn, vn in ((0, FAKE), (FAKE, 0), (FAKE + 8, FAKE)):
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.decode_step_ragged(L, FAKE, FAKE, kn, vn, FAKE, 256, FAKE, 0.1, 0, FAKE, ws, stream=0)
+        assert e.value.status == 1
+
+
 def test_corrupted_layout_rejected(lib):
     L = kvq.cache_layout(1, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
     for field, val in (("total_bytes", 1), ("n_prot", 2), ("Tv", 5)):
