@@ -242,3 +242,53 @@ def decode_reference(q_bf16, k_bf16, v_bf16, vis_start: int, vis_end: int, prot,
     vhat, _ = reconstruct(v_bf16, vis_start, vis_end, v_prot, v_bits, G, plant)
     out, lse = attention(q_bf16, khat, vhat, scale, threads, plant)
     return out, lse, khat, vhat
+
+
+def sensitivity_reference(q_bf16, k_bf16, v_bf16, vis_start: int, vis_end: int, prot, k_bits: int,
+                          v_bits: int, G: int, scale: float, readout, plant: int = 0):
+    """K-vs-V sensitivity of one layer's compressed cache, in fp64.
+
+    "VLM_KV_Quantization" sections 3-4 measure quantisation damage as the
+    KL divergence D_KL(P_fp || P_q) of the model's output distribution from
+    the unquantised one, quantising visual K or visual V alone with the same
+    tokens, bits and group size.  Without a model, per (b, hq):
+      kl_attn = D_KL(p || p_hat): softmax weights over positions with the raw
+                bf16 K (p) and with K as the decode reads it (p_hat);
+      kl_out  = D_KL(P || P_hat): P = softmax(readout @ o) with o the
+                attention output over the raw cache, P_hat the same over the
+                cache as the decode reads it (readout [n_out, D] fp32 stands
+                for the layers after attention);
+      err     = ||o_hat - o||_2.
+    The cache as read is decode_reference's policy (prot, k_bits, v_bits,
+    G); the raw cache is the same inputs with nothing quantised.  Returns
+    fp64 [B, Hq, 3] = (kl_attn, kl_out, err)."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    B, Hq, D = q.shape
+    Hkv = k_bf16.shape[1]
+    kb, vb = (v_bits, k_bits) if plant == 13 else (k_bits, v_bits)  # planted: K and V swapped
+    o, _, kx, _ = decode_reference(q, k_bf16, v_bf16, vis_start, vis_end, [0] * Hkv, 16, 16, G, scale,
+                                   plant=plant)
+    oh, _, kh, _ = decode_reference(q, k_bf16, v_bf16, vis_start, vis_end, prot, kb, vb, G, scale,
+                                    plant=plant)
+    W = np.asarray(readout, dtype=np.float32).astype(np.float64)
+    res = np.empty((B, Hq, 3), np.float64)
+
+    def kl(a, b, log_a, log_b):
+        if plant == 12:  # planted: divergence taken in the other direction
+            a, b, log_a, log_b = b, a, log_b, log_a
+        return float(np.sum(a * (log_a - log_b)))
+
+    def log_softmax(z):
+        m = np.max(z)
+        return z - (m + np.log(np.sum(np.exp(z - m))))
+
+    for b in range(B):
+        for hq in range(Hq):
+            p = attention_weights(q[b:b + 1], kx[b:b + 1], hq, scale, plant)
+            ph = attention_weights(q[b:b + 1], kh[b:b + 1], hq, scale, plant)
+            res[b, hq, 0] = kl(p, ph, np.log(p), np.log(ph))
+            lz = log_softmax(W @ o[b, hq])
+            lzh = log_softmax(W @ oh[b, hq])
+            res[b, hq, 1] = kl(np.exp(lz), np.exp(lzh), lz, lzh)
+            res[b, hq, 2] = float(np.sqrt(np.sum((oh[b, hq] - o[b, hq]) ** 2)))
+    return res

@@ -396,6 +396,87 @@ def pin_konly_policy(plant: int = 0):
     assert np.array_equal(vh[:, 0], vq[:, 0])
 
 
+# ---------------------------------------------------------------------------
+# K-vs-V sensitivity probe ("VLM_KV_Quantization" sections 3-4: KL of the
+# distribution after quantising K or V alone, against the unquantised one)
+# ---------------------------------------------------------------------------
+
+def _readout(seed, n_out, D):
+    return np.random.default_rng(seed).standard_normal((n_out, D)).astype(np.float32)
+
+
+def pin_probe_nothing_quantised(plant: int = 0):
+    """With nothing quantised (bits 16, or every head protected) the cache
+    as read is the raw cache: every divergence and the error are exactly 0."""
+    q, k, v = _small_case(41, 1, 4, 2, 60, 128)
+    W = _readout(1, 16, 128)
+    for prot, kb, vb in (([0, 0], 16, 16), ([1, 1], 2, 2)):
+        r = oracle.sensitivity_reference(q, k, v, 5, 50, prot, kb, vb, 32, 0.1, W, plant=plant)
+        assert np.array_equal(r, np.zeros_like(r)), (prot, kb, vb)
+
+
+def pin_probe_v_only_leaves_weights(plant: int = 0):
+    """Quantising V alone cannot move the softmax weights (kl_attn = 0
+    exactly) but does move the output; quantising K alone moves both."""
+    q, k, v = _small_case(42, 1, 4, 2, 60, 128)
+    W = _readout(2, 16, 128)
+    r = oracle.sensitivity_reference(q, k, v, 5, 50, [0, 0], 16, 2, 32, 0.1, W, plant=plant)
+    assert np.all(r[..., 0] == 0.0)
+    assert np.all(r[..., 1] > 0) and np.all(r[..., 2] > 0)
+    r = oracle.sensitivity_reference(q, k, v, 5, 50, [0, 0], 2, 16, 32, 0.1, W, plant=plant)
+    assert np.all(r[..., 0] > 0) and np.all(r[..., 1] > 0) and np.all(r[..., 2] > 0)
+
+
+def pin_probe_two_positions_closed_form(plant: int = 0):
+    """Two positions, q = e_0, scale 1.  Position 0 is text with k = e_0;
+    position 1 is visual with k = (0.5, 3, 0, ...), whose 2-bit group has
+    s = 1, z = 0 and sends 0.5 to code 0 (half to even): scores (1, 0.5)
+    exact, (1, 0) as read.  v_0 = e_0, v_1 = 0 (V unquantised), readout rows
+    (4 e_0, 0).  Every value below is a two-term formula."""
+    D = 32
+    k = np.zeros((1, 1, 2, D))
+    k[0, 0, 0, 0] = 1.0
+    k[0, 0, 1, 0], k[0, 0, 1, 1] = 0.5, 3.0
+    v = np.zeros((1, 1, 2, D))
+    v[0, 0, 0, 0] = 1.0
+    q = np.zeros((1, 1, D))
+    q[0, 0, 0] = 1.0
+    W = np.zeros((2, D), np.float32)
+    W[0, 0] = 4.0
+    r = oracle.sensitivity_reference(_bf16_bits_from_float(q), _bf16_bits_from_float(k),
+                                     _bf16_bits_from_float(v), 1, 2, [0], 2, 16, 32, 1.0, W,
+                                     plant=plant)
+
+    def two(x0, x1):  # softmax of two scores
+        e0, e1 = math.exp(x0), math.exp(x1)
+        return e0 / (e0 + e1), e1 / (e0 + e1)
+
+    p0, p1 = two(1.0, 0.5)
+    h0, h1 = two(1.0, 0.0)
+    kl_attn = p0 * math.log(p0 / h0) + p1 * math.log(p1 / h1)
+    P0, P1 = two(4.0 * p0, 0.0)
+    Q0, Q1 = two(4.0 * h0, 0.0)
+    kl_out = P0 * math.log(P0 / Q0) + P1 * math.log(P1 / Q1)
+    assert abs(r[0, 0, 0] - kl_attn) < 1e-14, (r[0, 0, 0], kl_attn)
+    assert abs(r[0, 0, 1] - kl_out) < 1e-14, (r[0, 0, 1], kl_out)
+    assert abs(r[0, 0, 2] - abs(p0 - h0)) < 1e-15
+
+
+def pin_probe_nonnegative_and_ordered(plant: int = 0):
+    """Divergences are >= 0 (Gibbs), and fewer bits do more damage: mean
+    INT2 > mean INT4 > mean INT8 for each of K and V."""
+    q, k, v = _small_case(43, 2, 4, 2, 120, 128)
+    W = _readout(3, 32, 128)
+    for which in ("k", "v"):
+        means = []
+        for bits in (2, 4, 8):
+            kb, vb = (bits, 16) if which == "k" else (16, bits)
+            r = oracle.sensitivity_reference(q, k, v, 8, 110, [0, 0], kb, vb, 32, 0.09, W, plant=plant)
+            assert np.all(r >= 0), (which, bits)
+            means.append(r[..., 1].mean())
+        assert means[0] > means[1] > means[2] > 0, (which, means)
+
+
 ALL_PINS = [
     pin_f16_conversion,
     pin_quantiser_bruteforce,
@@ -417,4 +498,8 @@ ALL_PINS = [
     pin_packed_row_count,
     pin_gqa_grouping,
     pin_konly_policy,
+    pin_probe_nothing_quantised,
+    pin_probe_v_only_leaves_weights,
+    pin_probe_two_positions_closed_form,
+    pin_probe_nonnegative_and_ordered,
 ]

@@ -24,6 +24,8 @@ PLANTS = {
     9: "scale uses 2^b steps instead of 2^b - 1",
     10: "2-bit K storage slots of a register pair swapped",
     11: "K-only protected head keeps its V in bf16 too",
+    12: "sensitivity divergence taken in the other direction",
+    13: "sensitivity probe quantises V where it should quantise K",
 }
 
 
