@@ -66,6 +66,12 @@ def parse_args():
     ap.add_argument("--prefill-in-step", choices=["auto", "yes", "no"], default="auto",
                     help="include kvq_quantize_append of the whole bf16 history in every step "
                          "(auto: yes for llava_next_13b, whose step includes the prefill)")
+    ap.add_argument("--n-q", type=int, default=1,
+                    help="query tokens per sequence and step: > 1 appends n_q rows and runs "
+                         "kvq_decode_attention_mq (multi-query decode) per layer")
+    ap.add_argument("--probe", action="store_true",
+                    help="instead of the decode step: the K-vs-V sensitivity study "
+                         "(kvq_sensitivity_probe) on the workload's synthetic cache")
     return ap.parse_args()
 
 
@@ -170,18 +176,20 @@ class ClockSampler:
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
-def decode_bytes(L, T: int) -> int:
-    """Compressed cache bytes a decode over positions [0, T) must read, plus q
-    and out.  A packed visual row costs its codes plus its fp16 scale/zero."""
+def decode_bytes(L, T: int, n_q: int = 1) -> int:
+    """Compressed cache bytes a decode over positions [0, T) must read (once,
+    whatever the number n_q of query tokens), plus q and out.  A packed
+    visual row costs its codes plus its fp16 scale/zero."""
     d = L.d
     vsa, vea = min(d.vis_start, T), min(d.vis_end, T)
     n_vis = vea - vsa
     n_txt = T - n_vis
     bf16_row = 2 * d.D
     packed = sum(int(L.row_bytes[s]) for s in range(4))  # K codes, K s/z, V codes, V s/z
+    konly = bf16_row + int(L.row_bytes[2]) + int(L.row_bytes[3])  # bf16 K, packed V
     per_b = (d.H_kv * n_txt * 2 * bf16_row + L.n_prot * n_vis * 2 * bf16_row
-             + L.n_packed * n_vis * packed)
-    qo = 2 * d.B * d.H_q * d.D * 2
+             + L.n_packed * n_vis * packed + L.n_konly * n_vis * konly)
+    qo = 2 * d.B * n_q * d.H_q * d.D * 2
     return d.B * per_b + qo
 
 
@@ -213,13 +221,14 @@ class Model:
     """Per-layer caches (history quantised once), per-step inputs, outputs."""
 
     def __init__(self, w: synth.Workload, dev, n_layers: int, prefill_in_step: bool = False,
-                 fused: bool = True):
+                 fused: bool = True, n_q: int = 1):
         import bit_mixed_precision_kvq_gb300 as kvq
         self.kvq = kvq
-        self.fused = fused
+        self.n_q = n_q
+        self.fused = fused and n_q == 1  # multi-query: append the rows, then decode
         self.w = w
         self.T_hist = w.T
-        self.T = w.T + 1
+        self.T = w.T + n_q
         self.prefill_in_step = prefill_in_step
         self.layers = []
         self.ws = {}  # one workspace per unit count (its counter area is sized by it)
@@ -238,16 +247,25 @@ class Model:
                 del k, v
             self.layers.append(layer)
             n = int(L.units)
-            if n not in self.ws or self.ws[n].numel() < int(L.workspace_bytes):
-                self.ws[n] = torch.zeros(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
+            nb = kvq.decode_mq_workspace_bytes(L, n_q)
+            if n not in self.ws or self.ws[n].numel() < nb:
+                self.ws[n] = torch.zeros(nb, dtype=torch.uint8, device=dev)
             layer["ws"] = self.ws[n]
         nL = n_layers
         # per-step device inputs/outputs, packed per layer so that the e2e leg
         # moves them with one copy each way
-        self.q = torch.stack([synth.make_q(w, l, 0, dev) for l in range(nL)])
-        self.ks = torch.stack([synth.make_step_kv(w, l, "k", 0, dev) for l in range(nL)])
-        self.vs = torch.stack([synth.make_step_kv(w, l, "v", 0, dev) for l in range(nL)])
-        self.out = torch.empty((nL, w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        if n_q == 1:
+            self.q = torch.stack([synth.make_q(w, l, 0, dev) for l in range(nL)])
+            self.out = torch.empty((nL, w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        else:  # [layer][B][n_q][H_q][D]
+            self.q = torch.stack([torch.stack([synth.make_q(w, l, s, dev) for s in range(n_q)], 1)
+                                  for l in range(nL)])
+            self.out = torch.empty((nL, w.B, n_q, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
+        # the step's own K/V rows, [layer][B][H_kv][n_q][D]
+        self.ks = torch.stack([torch.cat([synth.make_step_kv(w, l, "k", s, dev) for s in range(n_q)], 2)
+                               for l in range(nL)])
+        self.vs = torch.stack([torch.cat([synth.make_step_kv(w, l, "v", s, dev) for s in range(n_q)], 2)
+                               for l in range(nL)])
         self.scale = 1.0 / math.sqrt(w.D)
         torch.cuda.synchronize()
 
@@ -266,6 +284,10 @@ class Model:
         if self.fused:
             kvq.decode_step(L, ly["cache"], self.q[l], self.ks[l], self.vs[l], self.T_hist,
                             self.out[l], self.scale, None, ly["ws"])
+        elif self.n_q > 1:
+            kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
+            kvq.decode_attention_mq(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
+                                    ly["ws"])
         else:
             kvq.quantize_append(L, ly["cache"], self.ks[l], self.vs[l], self.T_hist)
             kvq.decode_attention(L, ly["cache"], self.q[l], self.T, self.out[l], self.scale, None,
@@ -279,7 +301,8 @@ class Model:
         self.kvq.quantize_append(ly["L"], ly["cache"], ly["k"], ly["v"], 0)
 
     def step_bytes(self) -> int:
-        b = sum(decode_bytes(ly["L"], self.T) + append_bytes(ly["L"], 1) for ly in self.layers)
+        b = sum(decode_bytes(ly["L"], self.T, self.n_q) + append_bytes(ly["L"], self.n_q)
+                for ly in self.layers)
         if self.prefill_in_step:
             b += sum(prefill_bytes(ly["L"], self.T_hist) for ly in self.layers)
         return b
@@ -293,7 +316,7 @@ def run_ours(args, rank, world, local):
     n_layers = args.layers or w.n_layers
     prefill = (args.prefill_in_step == "yes" or
                (args.prefill_in_step == "auto" and args.workload == "llava_next_13b"))
-    model = Model(w, dev, n_layers, prefill_in_step=prefill, fused=(args.fused == "yes"))
+    model = Model(w, dev, n_layers, prefill_in_step=prefill, fused=(args.fused == "yes"), n_q=args.n_q)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -354,7 +377,7 @@ def run_ours(args, rank, world, local):
         rl_ev.append((a, b))
     torch.cuda.synchronize()
     launch_ms = float(np.median([a.elapsed_time(b) for a, b in rl_ev])) / n_layers
-    layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) + append_bytes(ly["L"], 1)
+    layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T, model.n_q) + append_bytes(ly["L"], model.n_q)
                                  for ly in model.layers]))
     peaks = {}
     try:
@@ -426,11 +449,14 @@ def run_ours(args, rank, world, local):
                                f"K{w.layers[0].k_bits}/V{w.layers[0].v_bits} G{w.group_size}, "
                                f"protected {w.layers[0].protected}",
                    "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
-                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
+                   "query_tokens": model.n_q},
         "roofline": {"bound": "hbm",
-                     "traffic": NCU_TRAFFIC.get((w.name, n_layers, model.fused)),
+                     "traffic": NCU_TRAFFIC.get((w.name, n_layers, model.fused)) if model.n_q == 1 else None,
                      "kernel": ("split_mma_kernel<..., step> (kvq_decode_step, one launch)" if model.fused
-                                else "kvq_quantize_append + kvq_decode_attention (3 launches)"),
+                                else ("kvq_quantize_append + kvq_decode_attention_mq (3 launches)"
+                                      if model.n_q > 1 else
+                                      "kvq_quantize_append + kvq_decode_attention (3 launches)")),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "per_launch_bytes": int(layer_bytes), "per_launch_us": round(launch_ms * 1e3, 3),
@@ -543,8 +569,90 @@ def run_reference(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# --probe: K-vs-V sensitivity study
+# ---------------------------------------------------------------------------
+
+PROBE_BITS = (8, 4, 2)
+PROBE_NOUT = 1024
+FP64_NOMINAL_TFLOPS = 1.25  # GB300 FP64, nominal
+
+
+def run_probe(args):
+    """The pages' K-vs-V comparison ("VLM_KV_Quantization", sections 3-4),
+    model-free: for every layer of the workload and every bit-width, the same
+    synthetic history is appended into a cache with only visual K quantised
+    (V bits 16) and one with only visual V quantised (K bits 16), same group
+    size, no protected head (the study removes every policy), and
+    kvq_sensitivity_probe measures the divergences on each.  The readout is a
+    fixed seeded N(0, 1) matrix of PROBE_NOUT rows.  Prints one JSON line with
+    the means over (layer, query head) and the probe's device time."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_mixed_precision_kvq_gb300 as kvq
+    dev = torch.device("cuda", 0)
+    w = synth.workload(args.workload, args.T)
+    n_layers = args.layers or w.n_layers
+    T = w.T
+    g = torch.Generator().manual_seed(20261203)
+    R = torch.randn((PROBE_NOUT, w.D), generator=g, dtype=torch.float32).to(dev)
+    scale = 1.0 / math.sqrt(w.D)
+    sums = {(b, side): np.zeros(3) for b in PROBE_BITS for side in "kv"}
+    n_rows = 0
+    times = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for l in range(n_layers):
+        k = synth.make_kv(w, l, "k", dev)
+        v = synth.make_kv(w, l, "v", dev)
+        q = synth.make_q(w, l, 0, dev)
+        for bits in PROBE_BITS:
+            for side in "kv":
+                kb, vb = (bits, 16) if side == "k" else (16, bits)
+                L = kvq.cache_layout(w.B, w.H_q, w.H_kv, w.D, T, w.vis_start, w.vis_end, kb, vb,
+                                     w.group_size, [])
+                cache = torch.empty(int(L.total_bytes), dtype=torch.uint8, device=dev)
+                kvq.quantize_append(L, cache, k, v, 0)
+                res = torch.empty((w.B, w.H_q, 3), dtype=torch.float64, device=dev)
+                ws = torch.empty(kvq.probe_workspace_bytes(L, T), dtype=torch.uint8, device=dev)
+                torch.cuda.synchronize()
+                ev0.record()
+                kvq.sensitivity_probe(L, cache, q, k, v, T, R, res, scale, ws)
+                ev1.record()
+                torch.cuda.synchronize()
+                times.append(ev0.elapsed_time(ev1) * 1e3)
+                sums[(bits, side)] += res.double().sum(dim=(0, 1)).cpu().numpy()
+        n_rows += w.B * w.H_q
+        del k, v
+    table = {}
+    for bits in PROBE_BITS:
+        mk, mv = sums[(bits, "k")] / n_rows, sums[(bits, "v")] / n_rows
+        table[str(bits)] = {"k_kl_attn": mk[0], "k_kl_out": mk[1], "v_kl_out": mv[1],
+                            "k_over_v_kl_out": mk[1] / mv[1] if mv[1] > 0 else None,
+                            "k_err": mk[2], "v_err": mv[2]}
+    us = float(np.median(times))
+    flops = 8.0 * w.D * w.B * w.H_q * T  # two score dots and two output sums per position, fp64
+    achieved = flops / (us * 1e-6) / 1e12
+    line = {
+        "metric": "K-vs-V sensitivity (model-free KL of attention weights and of a readout "
+                  "distribution, K or V quantised alone)",
+        "workload": w.name, "layers": n_layers, "group_size": w.group_size, "T": T,
+        "readout_rows": PROBE_NOUT, "bits": table,
+        "probe_us_per_layer": us,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP64_NOMINAL_TFLOPS,
+                     "unit": "TFLOP/s (fp64)", "frac": achieved / FP64_NOMINAL_TFLOPS,
+                     "peak_source": "nominal GB300 FP64"},
+        "data": "synthetic",
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.probe:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --probe needs a CUDA GPU")
+        run_probe(args)
+        return
     if args.impl == "reference":
         rank, world, local = dist_setup(use_cuda=False)
         run_reference(args, rank, world, local)

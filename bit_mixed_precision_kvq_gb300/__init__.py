@@ -19,12 +19,16 @@ __all__ = [
     "kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention", "KVQ_MAX_HEADS",
     "decode_attention_static_ws", "kvq_decode_attention_static_ws", "STATIC_WS_BYTES",
     "decode_step", "kvq_decode_step", "decode_attention_ragged", "kvq_decode_attention_ragged",
-    "decode_step_ragged", "kvq_decode_step_ragged",
+    "decode_step_ragged", "kvq_decode_step_ragged", "sensitivity_probe", "kvq_sensitivity_probe",
+    "probe_workspace_bytes", "kvq_probe_workspace_bytes", "decode_attention_mq",
+    "kvq_decode_attention_mq", "decode_mq_workspace_bytes", "kvq_decode_mq_workspace_bytes",
+    "KVQ_MAX_QUERY_TOKENS",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
 
 KVQ_MAX_HEADS = 128
+KVQ_MAX_QUERY_TOKENS = 64
 KVQ_NSEG = 8
 (SEG_K_CODES, SEG_K_SZ, SEG_V_CODES, SEG_V_SZ, SEG_PROT_K, SEG_PROT_V, SEG_TEXT_K,
  SEG_TEXT_V) = range(8)
@@ -32,6 +36,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_CAPACITY", 4: "KVQ_ERR_CUDA"}
 EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_attention",
                     "kvq_decode_step", "kvq_decode_attention_ragged", "kvq_decode_step_ragged",
+                    "kvq_sensitivity_probe", "kvq_probe_workspace_bytes", "kvq_decode_attention_mq",
+                    "kvq_decode_mq_workspace_bytes",
                     "kvq_decode_attention_static_ws", "kvq_last_cuda_error", "kvq_status_string"]
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
@@ -104,6 +110,15 @@ def load() -> ctypes.CDLL:
     lib.kvq_decode_step_ragged.argtypes = [ctypes.POINTER(Layout), P, P, P, P, P, i32, f32, P, P, P, sz,
                                            P]
     lib.kvq_decode_step_ragged.restype = ctypes.c_int
+    lib.kvq_decode_mq_workspace_bytes.argtypes = [ctypes.POINTER(Layout), i32]
+    lib.kvq_decode_mq_workspace_bytes.restype = sz
+    lib.kvq_decode_attention_mq.argtypes = [ctypes.POINTER(Layout), P, P, i32, i32, f32, P, P, P, sz, P]
+    lib.kvq_decode_attention_mq.restype = ctypes.c_int
+    lib.kvq_probe_workspace_bytes.argtypes = [ctypes.POINTER(Layout), i32]
+    lib.kvq_probe_workspace_bytes.restype = sz
+    lib.kvq_sensitivity_probe.argtypes = [ctypes.POINTER(Layout), P, P, P, P, i64, i64, i64, i32, f32, P,
+                                          i32, P, P, sz, P]
+    lib.kvq_sensitivity_probe.restype = ctypes.c_int
     lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
     lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
     lib.kvq_last_cuda_error.argtypes = []
@@ -237,6 +252,63 @@ def decode_step_ragged(L: Layout, cache, q, k_new, v_new, t_new, T_max: int, out
         raise KvqError(st, "kvq_decode_step_ragged")
 
 
+def decode_mq_workspace_bytes(L: Layout, n_q: int) -> int:
+    """kvq_decode_mq_workspace_bytes: workspace bytes of decode_attention_mq."""
+    return int(load().kvq_decode_mq_workspace_bytes(ctypes.byref(L), int(n_q)))
+
+
+def decode_attention_mq(L: Layout, cache, q, T: int, out, softmax_scale: Optional[float] = None,
+                        lse=None, workspace=None, ws_bytes: Optional[int] = None,
+                        stream=None) -> None:
+    """kvq_decode_attention_mq: q [B, n_q, H_q, D] bf16; token i attends
+    positions [0, T - n_q + 1 + i); out [B, n_q, H_q, D], lse [B, n_q, H_q]."""
+    n_q = int(q.shape[1])
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kvq_decode_attention_mq(ctypes.byref(L), _addr(cache), _addr(q), n_q, int(T),
+                                        float(softmax_scale), _addr(out), _addr(lse),
+                                        _addr(workspace), int(ws_bytes), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_decode_attention_mq")
+
+
+def probe_workspace_bytes(L: Layout, T: int) -> int:
+    """kvq_probe_workspace_bytes: scratch bytes of sensitivity_probe over T positions."""
+    return int(load().kvq_probe_workspace_bytes(ctypes.byref(L), int(T)))
+
+
+def sensitivity_probe(L: Layout, cache, q, k, v, T: int, readout, result,
+                      softmax_scale: Optional[float] = None, workspace=None,
+                      ws_bytes: Optional[int] = None, strides: Optional[Sequence[int]] = None,
+                      stream=None) -> None:
+    """kvq_sensitivity_probe: per (b, hq), fp64 (kl_attn, kl_out, err) of
+    the cache against the raw rows k, v ([B, H_kv, >= T, D] bf16 on the
+    device) into result ([B, H_q, 3] float64); readout [n_out, D] float32."""
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(L.d.D)
+    if strides is None:
+        if k.stride() != v.stride():
+            raise ValueError("k and v must share strides")
+        if k.stride(-1) != 1:
+            raise ValueError("last dim must be contiguous")
+        strides = k.stride()[:3]
+    n_out = readout.shape[0] if hasattr(readout, "shape") else 0
+    if workspace is None:
+        import torch
+        workspace = torch.empty(max(1, probe_workspace_bytes(L, T)), dtype=torch.uint8,
+                                device=result.device)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().kvq_sensitivity_probe(ctypes.byref(L), _addr(cache), _addr(q), _addr(k), _addr(v),
+                                      int(strides[0]), int(strides[1]), int(strides[2]), int(T),
+                                      float(softmax_scale), _addr(readout), int(n_out), _addr(result),
+                                      _addr(workspace), int(ws_bytes), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_sensitivity_probe")
+
+
 def decode_attention_static_ws(L: Layout, cache, q, T: int, out,
                                softmax_scale: Optional[float] = None, lse=None,
                                stream=None) -> None:
@@ -261,3 +333,7 @@ kvq_decode_attention_static_ws = decode_attention_static_ws
 kvq_decode_step = decode_step
 kvq_decode_attention_ragged = decode_attention_ragged
 kvq_decode_step_ragged = decode_step_ragged
+kvq_sensitivity_probe = sensitivity_probe
+kvq_decode_attention_mq = decode_attention_mq
+kvq_decode_mq_workspace_bytes = decode_mq_workspace_bytes
+kvq_probe_workspace_bytes = probe_workspace_bytes

@@ -22,28 +22,29 @@
 
 namespace kvq {
 
-const void* split_kernel_k2(int vb, int G, bool step, int halves, bool konly);
-const void* split_kernel_k4(int vb, int G, bool step, int halves, bool konly);
-const void* split_kernel_k8(int vb, int G, bool step, int halves, bool konly);
-const void* split_kernel_k16(int vb, int G, bool step, int halves, bool konly);
+const void* split_kernel_k2(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_k4(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_k8(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_k16(int vb, int G, bool step, int halves, bool general);
 
 constexpr int kCombineWarps = 16;
 
-// Combine: one CTA per output row (b, hq), 16 warps (combine_row).
+// Combine: one CTA per output row (b, token i, hq), 16 warps (combine_row).
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ Params p) {
   __shared__ float sm_ml[kCombineWarps][2];
   __shared__ float4 sm_o[kCombineWarps][32];
-  const int bq = blockIdx.x;
-  const int b = bq / p.Hq;
-  const int hq = bq - b * p.Hq;
+  const int bq = blockIdx.x;  // (b * n_q + i) * Hq + hq
+  const int bi = bq / p.Hq;
+  const int hq = bq - bi * p.Hq;
+  const int b = bi / p.n_q, i = bi - (bi / p.n_q) * p.n_q;
   const int h = hq / p.g;
-  const int r = hq - h * p.g;
-  const int hc = r / kNH;
+  const int c = (hq - h * p.g) * p.n_q + i;  // column among the KV head's g * n_q
+  const int hc = c / kNH;
   const int u = unit_of(p, b, h, hc);
   int cf, cl;
   plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
   pdl_wait();
-  combine_row<kCombineWarps>(p, u, r - hc * kNH, cf, cl, bq, threadIdx.x >> 5, threadIdx.x & 31, sm_ml,
+  combine_row<kCombineWarps>(p, u, c - hc * kNH, cf, cl, bq, threadIdx.x >> 5, threadIdx.x & 31, sm_ml,
                              sm_o, false, []() { __syncthreads(); });
 }
 
@@ -54,8 +55,8 @@ namespace {
 // Positions per packed tile and its sub-buffer offsets inside one stage.
 // 64-position packed blocks only when packed chunks are long (>= 1024
 // positions: enough blocks for every consumer warp); else 32.
-int packed_halves(const kvq::Plan& P, const kvq_layout* L) {
-  if (L->n_konly > 0) return 2;  // K-only layouts: 32-position blocks only
+int packed_halves(const kvq::Plan& P, const kvq_layout* L, int n_q) {
+  if (L->n_konly > 0 || n_q > 1) return 2;  // the general kernels: 32-position blocks only
   if (kvq::packed_block_halves(L->d.k_bits, L->d.v_bits, L->d.group_size) < 4) return 2;
   const int64_t per_chunk = P.aligned ? P.T / (P.n_q > 0 ? P.n_q : 1) : P.T;
   return per_chunk >= 1024 ? 4 : 2;
@@ -83,12 +84,13 @@ void packed_tile_geometry(kvq::Params* p) {
   p->pk_off_vsz = p->pk_off_ksz + r128(tt * p->kszrow);
 }
 
-const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool konly) {
+// general: the variant for layouts with K-only heads and multi-query calls.
+const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool general) {
   switch (kb) {
-    case 2: return kvq::split_kernel_k2(vb, G, step, halves, konly);
-    case 4: return kvq::split_kernel_k4(vb, G, step, halves, konly);
-    case 8: return kvq::split_kernel_k8(vb, G, step, halves, konly);
-    case 16: return kvq::split_kernel_k16(vb, G, step, halves, konly);
+    case 2: return kvq::split_kernel_k2(vb, G, step, halves, general);
+    case 4: return kvq::split_kernel_k4(vb, G, step, halves, general);
+    case 8: return kvq::split_kernel_k8(vb, G, step, halves, general);
+    case 16: return kvq::split_kernel_k16(vb, G, step, halves, general);
   }
   return nullptr;
 }
@@ -113,10 +115,16 @@ kvq_status prepare_split(const void* fn, size_t smem) {
   return KVQ_OK;
 }
 
-// Shared argument checks and parameter set-up of the decode entry points.
+// Units of a decode call with n_q query tokens per sequence.
+int64_t decode_units(const kvq_layout* L, int32_t n_q) {
+  return static_cast<int64_t>(L->d.B) * L->d.H_kv * ((static_cast<int64_t>(L->g) * n_q + kvq::kNH - 1) / kvq::kNH);
+}
+
+// Shared argument checks and parameter set-up of the decode entry points
+// (n_q query tokens per sequence).
 kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_bf16, int32_t T,
                          float softmax_scale, void* out_bf16, float* lse, void* workspace,
-                         size_t ws_bytes, kvq::Params* p) {
+                         size_t ws_bytes, kvq::Params* p, int32_t n_q = 1) {
   const kvq_status st = kvq_check_layout(L);
   if (st != KVQ_OK) return st;
   if (!cache || !q_bf16 || !out_bf16 || !workspace) return KVQ_ERR_INVALID_ARG;
@@ -126,7 +134,8 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
     return KVQ_ERR_INVALID_ARG;
   if (T < 1 || T > L->d.T_cap) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
-  if (ws_bytes < static_cast<size_t>(L->workspace_bytes)) return KVQ_ERR_CAPACITY;
+  const int64_t units = decode_units(L, n_q);
+  if (ws_bytes < static_cast<size_t>(kvq::ws_total_bytes(units))) return KVQ_ERR_CAPACITY;
   int n_sm = 0;
   if (kvq_device_sm_count(&n_sm) != 0) return KVQ_ERR_CUDA;
   kvq_fill_params(L, p);
@@ -136,18 +145,18 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   p->q = static_cast<const uint16_t*>(q_bf16);
   p->out = static_cast<uint16_t*>(out_bf16);
   p->lse = lse;
-  const int64_t slots = static_cast<int64_t>(L->units) + KVQ_MAX_CTAS - 1;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int64_t cnt_bytes = kvq::ws_counter_bytes(L->units);
+  const int64_t cnt_bytes = kvq::ws_counter_bytes(units);
   p->cnt = reinterpret_cast<uint32_t*>(ws);
   p->ws_o = reinterpret_cast<float*>(ws + cnt_bytes);
-  const int64_t o_bytes = (slots * kvq::kNH * kvq::kD * 4 + 255) / 256 * 256;
-  p->ws_ml = reinterpret_cast<float*>(ws + cnt_bytes + o_bytes);
+  p->ws_ml = reinterpret_cast<float*>(ws + cnt_bytes + kvq::ws_o_bytes(units));
   p->scale_log2 = softmax_scale * 1.4426950408889634f;
   p->seq_len = nullptr;  // uniform call; the ragged entry points set it
-  p->plan = kvq_make_plan(L, T, n_sm);  // one CTA per SM
+  p->n_q = n_q;
+  p->plan = kvq_make_plan(L, T, n_sm, n_q);  // one CTA per SM
+  p->NHC = p->plan.NHC;
   kvq_plan_cuts(&p->plan, p->cuts);
-  p->pk_halves = packed_halves(p->plan, L);
+  p->pk_halves = packed_halves(p->plan, L, n_q);
   packed_tile_geometry(p);
   konly_tile_geometry(p);
   return KVQ_OK;
@@ -162,13 +171,13 @@ static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one
 // The split kernel and the combine of one decode call (p prepared).
 kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p->pk_halves,
-                                       L->n_konly > 0);
+                                       L->n_konly > 0 || p->n_q > 1);
   if (!split) return KVQ_ERR_UNSUPPORTED;
   kvq_status st = prepare_split(split, kSplitSmemBytes);
   if (st != KVQ_OK) return st;
   if (kvq_launch_pdl(split, p->plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, p) != 0)
     return KVQ_ERR_CUDA;
-  if (kvq_launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), L->d.B * L->d.H_q,
+  if (kvq_launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), L->d.B * p->n_q * L->d.H_q,
                      kvq::kCombineWarps * 32, 0, stream, p) != 0)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
@@ -188,7 +197,7 @@ kvq_status step_rows_ok(const kvq_layout* L, const void* k_new_bf16, const void*
 // the runtime accepts both.
 kvq_status launch_step(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p->pk_halves,
-                                    L->n_konly > 0);
+                                    L->n_konly > 0);  // the fused step is single-query
   if (!fn) return KVQ_ERR_UNSUPPORTED;
   const kvq_status st = prepare_split(fn, kSplitSmemBytes);
   if (st != KVQ_OK) return st;
@@ -252,6 +261,26 @@ extern "C" kvq_status kvq_decode_attention_ragged(const kvq_layout* L, const voi
                                       ws_bytes, p);
   if (st != KVQ_OK) return st;
   p->seq_len = seq_len;
+  return launch_decode(L, p, stream);
+}
+
+extern "C" size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q) {
+  if (kvq_check_layout(L) != KVQ_OK || n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS) return 0;
+  return static_cast<size_t>(kvq::ws_total_bytes(decode_units(L, n_q)));
+}
+
+extern "C" kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                              int32_t n_q, int32_t T, float softmax_scale, void* out_bf16,
+                                              float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  std::lock_guard<std::mutex> lock(g_call_mu);
+  if (!L) return KVQ_ERR_INVALID_ARG;
+  if (n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS || T < n_q) return KVQ_ERR_INVALID_ARG;
+  // the positions some tokens do not attend, [T - n_q + 1, T), must be text
+  if (n_q > 1 && T - n_q + 1 < L->d.vis_end && T > L->d.vis_start) return KVQ_ERR_INVALID_ARG;
+  kvq::Params* p = &g_params;
+  const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
+                                      ws_bytes, p, n_q);
+  if (st != KVQ_OK) return st;
   return launch_decode(L, p, stream);
 }
 

@@ -155,8 +155,18 @@ KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t*
   *c_first = lo;
 }
 
-// Bytes of the per-unit counter area at the start of the workspace.
-KVQ_HD int64_t ws_counter_bytes(int32_t units) { return (4 * static_cast<int64_t>(units) + 255) / 256 * 256; }
+// Decode workspace: the per-unit arrival counters of the fused step, then one
+// partial (o[kNH][kD] fp32, then (m, l)[kNH] fp32 in a second array) per
+// slot, slots <= units + C - 1 <= units + KVQ_MAX_CTAS - 1; each part
+// 256-byte aligned.
+KVQ_HD int64_t ws_counter_bytes(int64_t units) { return (4 * units + 255) / 256 * 256; }
+KVQ_HD int64_t ws_o_bytes(int64_t units) {
+  return ((units + KVQ_MAX_CTAS - 1) * kNH * kD * 4 + 255) / 256 * 256;
+}
+KVQ_HD int64_t ws_ml_bytes(int64_t units) { return ((units + KVQ_MAX_CTAS - 1) * kNH * 8 + 255) / 256 * 256; }
+KVQ_HD int64_t ws_total_bytes(int64_t units) {
+  return ws_counter_bytes(units) + ws_o_bytes(units) + ws_ml_bytes(units);
+}
 
 // Everything a kernel needs about one layer and one call (passed by value).
 struct Params {
@@ -199,22 +209,27 @@ struct Params {
   // ragged calls: device int32 [B] of attended positions (decode) or step
   // positions (fused step) per sequence; null for uniform calls
   const int32_t* seq_len;
+  // multi-query decode: query tokens per sequence (1 otherwise).  A unit's
+  // columns are (head j, token i) pairs, column c = j * n_q + i; token i
+  // attends the unit's positions except the last n_q - 1 - i.
+  int32_t n_q;
 };
 
-// unit -> (b, head, hc, slot, class).  kKO: the layout may have K-only
-// protected heads (three unit classes); else only protected and packed.
+// unit -> (b, head, hc, slot, class).  kGen: the general kernels (layouts
+// with K-only protected heads -- three unit classes -- and multi-query
+// calls); else only protected and packed units.
 struct UnitInfo {
   int32_t b, h, hc, slot;
   int32_t cls;
   bool prot;  // cls == kClsProt
 };
 
-template <bool kKO>
+template <bool kGen>
 KVQ_HD UnitInfo unit_info(const Params& p, int32_t u) {
   UnitInfo r;
   int cls;
   int32_t v, nslots;
-  if constexpr (kKO) {
+  if constexpr (kGen) {
     cls = unit_class(p.plan, u);
     v = cls == kClsProt ? u : (cls == kClsKonly ? u - p.plan.U_p : u - p.plan.U_p - p.plan.U_k);
     nslots = cls == kClsProt ? p.n_prot : (cls == kClsKonly ? p.n_konly : p.n_packed);
@@ -227,7 +242,7 @@ KVQ_HD UnitInfo unit_info(const Params& p, int32_t u) {
   const int32_t rem = v - r.b * nslots * p.NHC;
   r.slot = rem / p.NHC;
   r.hc = rem - r.slot * p.NHC;
-  if constexpr (kKO) {
+  if constexpr (kGen) {
     r.h = cls == kClsProt ? p.prot_head[r.slot] : (cls == kClsKonly ? p.konly_head[r.slot] : p.packed_head[r.slot]);
   } else {
     r.h = cls == kClsProt ? p.prot_head[r.slot] : p.packed_head[r.slot];
@@ -235,6 +250,14 @@ KVQ_HD UnitInfo unit_info(const Params& p, int32_t u) {
   r.cls = cls;
   r.prot = cls == kClsProt;
   return r;
+}
+
+// Row of q / out / lse (in units of D elements, or of one lse value) of
+// column c of KV head h of sequence b: [B][n_q][H_q] row-major.
+KVQ_HD int64_t col_row(const Params& p, int32_t b, int32_t h, int32_t c) {
+  if (p.n_q == 1) return static_cast<int64_t>(b) * p.Hq + h * p.g + c;
+  const int32_t j = c / p.n_q, i = c - (c / p.n_q) * p.n_q;
+  return (static_cast<int64_t>(b) * p.n_q + i) * p.Hq + h * p.g + j;
 }
 
 // (b, head, hc) -> unit
@@ -260,7 +283,8 @@ KVQ_HD int64_t packed_v_row(const Params& p, int32_t b, int cls, int32_t slot) {
 // Host helpers implemented in kvq_layout.cpp.
 kvq_status kvq_check_layout(const kvq_layout* L);
 void kvq_fill_params(const kvq_layout* L, kvq::Params* p);
-kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target);
+// n_q: query tokens per sequence (multi-query decode; 1 otherwise).
+kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target, int32_t n_q = 1);
 // The cut table cuts[0..P->C] of a plan (see the decomposition above); sets
 // the plan's per-unit chunk fields.
 void kvq_plan_cuts(kvq::Plan* P, kvq::Cut* cuts);

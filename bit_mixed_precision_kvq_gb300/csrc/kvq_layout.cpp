@@ -90,11 +90,7 @@ kvq_status build_layout(const kvq_layout_desc* desc, kvq_layout* out) {
     off = align_up(off + L.bytes[s] + kPad, kAlign);
   }
   L.total_bytes = off;
-  // Workspace: one partial (o[8][D] fp32, (m, l)[8]) per slot, slots <= units + C - 1,
-  // after a 256-byte header (grid-barrier words of the fused decode step).
-  const int64_t slots = static_cast<int64_t>(L.units) + KVQ_MAX_CTAS - 1;
-  L.workspace_bytes = kvq::ws_counter_bytes(L.units) + align_up(slots * kvq::kNH * D * 4, kAlign) +
-                      align_up(slots * kvq::kNH * 8, kAlign);
+  L.workspace_bytes = kvq::ws_total_bytes(L.units);
   L.eff_bits_k = d.k_bits < 16 ? d.k_bits + 32.0 / d.group_size : 16.0;
   L.eff_bits_v = d.v_bits < 16 ? d.v_bits + 32.0 / d.group_size : 16.0;
   *out = L;
@@ -162,12 +158,12 @@ void kvq_fill_params(const kvq_layout* L, kvq::Params* p) {
   }
 }
 
-kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target) {
+kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target, int32_t n_q) {
   kvq::Plan P;
   std::memset(&P, 0, sizeof(P));
   const kvq_layout_desc& d = L->d;
   P.T = T;
-  P.NHC = (L->g + kvq::kNH - 1) / kvq::kNH;
+  P.NHC = (L->g * n_q + kvq::kNH - 1) / kvq::kNH;
   P.vsa = d.vis_start < T ? d.vis_start : T;
   P.vea = d.vis_end < T ? d.vis_end : T;
   const int64_t vrow = L->row_bytes[KVQ_SEG_V_CODES] + L->row_bytes[KVQ_SEG_V_SZ];

@@ -45,6 +45,7 @@ constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16
 constexpr uint32_t kPrefetchBytes = kStageBytes;  // L2 prefetch before the dependency wait
 constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
 constexpr uint32_t kSpinPolls = 1u << 21;      // bounded inter-CTA wait (fused step)
+constexpr int kNoLimit = 1 << 30;              // kblock: no multi-query column limit
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
@@ -64,7 +65,7 @@ enum TileKind { kTileText = 0, kTileProt = 1, kTilePacked = 2, kTileKonly = 3 };
 
 // Walk the tiles of one piece [ps, pe) of a unit of class cls: text prefix,
 // visual block, text suffix, each cut into tiles.  f(kind, t0, n).
-template <bool kKO, typename F>
+template <bool kGen, typename F>
 __device__ __forceinline__ void walk_piece(const Params& p, int cls, int ps, int pe, F&& f) {
   const int b1 = max(ps, min(pe, p.vs)), b2 = max(ps, min(pe, p.ve));
 #pragma unroll 1
@@ -72,7 +73,7 @@ __device__ __forceinline__ void walk_piece(const Params& p, int cls, int ps, int
     const int s0 = seg == 0 ? ps : (seg == 1 ? b1 : b2);
     const int s1 = seg == 0 ? b1 : (seg == 1 ? b2 : pe);
     int kind, tt;
-    if constexpr (kKO) {
+    if constexpr (kGen) {
       kind = seg == 1 ? (cls == kClsProt ? kTileProt : (cls == kClsKonly ? kTileKonly : kTilePacked)) : kTileText;
       tt = kind == kTilePacked ? p.tt_pk : (kind == kTileKonly ? p.tt_ko : kTileBf16);
     } else {
@@ -93,10 +94,10 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // unit whose sequence attends [0, Tu): the last row of its last text tile)
 // comes from the k_new / v_new inputs rather than from the cache row that
 // the launch itself writes.
-template <bool kStep, bool kKO, typename F>
+template <bool kStep, bool kGen, typename F>
 __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int Tu, int kind,
                                              int t0, int n, F&& f) {
-  if (kKO && kind == kTileKonly) {
+  if (kGen && kind == kTileKonly) {
     // bf16 K rows (protected K segment) + packed V rows and their scale/zero
     const int64_t krow = prot_k_row(p, ui.b, kClsKonly, ui.slot) * p.Tv + (t0 - p.vs);
     const int64_t vrow = packed_v_row(p, ui.b, kClsKonly, ui.slot) * p.Tv_pad + (t0 - p.vs);
@@ -116,7 +117,7 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
       vs = p.seg[KVQ_SEG_TEXT_V];
     } else {
       vrow_p = (static_cast<int64_t>(ui.b) * p.n_prot + ui.slot) * p.Tv + (t0 - p.vs);
-      row = kKO ? prot_k_row(p, ui.b, kClsProt, ui.slot) * p.Tv + (t0 - p.vs) : vrow_p;
+      row = kGen ? prot_k_row(p, ui.b, kClsProt, ui.slot) * p.Tv + (t0 - p.vs) : vrow_p;
       ks = p.seg[KVQ_SEG_PROT_K];
       vs = p.seg[KVQ_SEG_PROT_V];
     }
@@ -136,7 +137,7 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
     }
   } else {
     const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
-    const int64_t vrow = kKO ? packed_v_row(p, ui.b, kClsPacked, ui.slot) * p.Tv_pad + (t0 - p.vs) : row;
+    const int64_t vrow = kGen ? packed_v_row(p, ui.b, kClsPacked, ui.slot) * p.Tv_pad + (t0 - p.vs) : row;
     const uint32_t bk = round16(n * p.krow), bv = round16(n * p.vrow);
     const uint32_t bks = round16(n * p.kszrow), bvs = round16(n * p.vszrow);
     f(0u, p.seg[KVQ_SEG_K_CODES] + row * p.krow, bk);
@@ -165,17 +166,17 @@ __device__ __forceinline__ int seq_end(const Params& p, int b) {
 // Walk the CTA's tiles: f(unit info, unit end Tu, kind, t0, n).  kEnds:
 // clip every unit at its sequence's end (seq_end); the L2 prefetch, issued
 // before the dependency wait, walks the unclipped pieces instead.
-template <bool kKO, bool kStep, bool kEnds, typename F>
+template <bool kGen, bool kStep, bool kEnds, typename F>
 __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
   const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
   for (int u = a.u; u <= u_last; ++u) {
-    const UnitInfo ui = unit_info<kKO>(p, u);
+    const UnitInfo ui = unit_info<kGen>(p, u);
     const int Tu = kEnds ? seq_end<kStep>(p, ui.b) : p.plan.T;
     const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
     const int ps = min((u == a.u) ? a.p : 0, pe);
-    walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) { f(ui, Tu, kind, t0, n); });
+    walk_piece<kGen>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) { f(ui, Tu, kind, t0, n); });
   }
 }
 
@@ -184,12 +185,12 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
 // other SMs' prefetches when the previous kernel does not overlap).  L2 is coherent with every SM's stores, so a
 // line that the previous kernel writes later is simply updated there; the
 // copies into shared memory all come after the wait.
-template <bool kKO>
+template <bool kGen>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   uint32_t budget = kPrefetchBytes;
-  walk_chunk<kKO, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
+  walk_chunk<kGen, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     if (budget == 0) return;
-    tile_sources<false, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
+    tile_sources<false, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
       const uint32_t b = min(bytes, budget);
       if (b) prefetch_l2(src, b);
       budget -= b;
@@ -197,18 +198,18 @@ __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   });
 }
 
-template <bool kStep, bool kKO>
+template <bool kStep, bool kGen>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
   uint32_t it = 0;
-  walk_chunk<kKO, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
+  walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     const int st = it % kStages;
     const uint32_t round = it / kStages;
     if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
     uint8_t* dst = sm.stage[st];
     uint32_t total = 0;
-    tile_sources<kStep, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
+    tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
     mbar_arrive_expect_tx(&sm.full[st], total);
-    tile_sources<kStep, kKO>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
+    tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
       bulk_g2s(dst + off, src, bytes, &sm.full[st]);
     });
     ++it;
@@ -686,7 +687,7 @@ enum VPath { kVBf16Lane = 0, kVBf16D = 1, kVPacked = 2 };
 // 16-row MMA halves sharing one online-softmax update.
 template <int NH, int KP, int VP, int KB, int VB, int G>
 __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, const uint8_t* vc,
-                                       const uint8_t* vsz, int r0, int n, float sl2,
+                                       const uint8_t* vsz, int r0, int n, int lim0, int lim1, float sl2,
                                        const uint32_t (&qb)[8][2], const uint32_t (&zb)[2], int gid,
                                        int tig, int lane, Acc& acc) {
   float S[NH][4];
@@ -704,6 +705,19 @@ __device__ __forceinline__ void kblock(const uint8_t* kc, const uint8_t* ksz, co
     for (int h = 0; h < NH; ++h) {
       if (r0 + 16 * h + gid >= n) S[h][0] = S[h][1] = -INFINITY;
       if (r0 + 16 * h + gid + 8 >= n) S[h][2] = S[h][3] = -INFINITY;
+    }
+  }
+  // Multi-query (general kernels): column 2tig (2tig + 1) sees the rows
+  // below lim0 (lim1); the other callers pass the constant kNoLimit, which
+  // removes this code from their instantiations.
+  if ((lim0 != kNoLimit || lim1 != kNoLimit) && min(lim0, lim1) < r0 + 16 * NH) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const int ra = r0 + 16 * h + gid;
+      if (ra >= lim0) S[h][0] = -INFINITY;
+      if (ra >= lim1) S[h][1] = -INFINITY;
+      if (ra + 8 >= lim0) S[h][2] = -INFINITY;
+      if (ra + 8 >= lim1) S[h][3] = -INFINITY;
     }
   }
 
@@ -864,7 +878,7 @@ __device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt) {
   return false;
 }
 
-template <int KB, int VB, int G, bool kStep, int NHP, bool kKO>
+template <int KB, int VB, int G, bool kStep, int NHP, bool kGen>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
@@ -876,13 +890,24 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   uint32_t it = 0;    // tiles seen (stage ring position)
   uint32_t gblk = 0;  // 32-position blocks dealt so far (round-robin over warps)
   for (int u = a.u; u <= u_last; ++u) {
-    const UnitInfo ui = unit_info<kKO>(p, u);
-    const int hq0 = ui.h * p.g + ui.hc * kNH;
-    const int nh = min(kNH, p.g - ui.hc * kNH);
+    const UnitInfo ui = unit_info<kGen>(p, u);
+    // The unit's columns: query heads h*g + hc*kNH + j; in the general
+    // kernels (head, token) pairs of a multi-query call, rows via col_row.
+    const int c0 = ui.hc * kNH;
+    const int hq0 = ui.h * p.g + c0;
+    const int nh = kGen ? min(kNH, p.g * p.n_q - c0) : min(kNH, p.g - c0);
+    auto out_row = [&](int j) -> int64_t {
+      if constexpr (kGen) return col_row(p, ui.b, ui.h, c0 + j);
+      else return static_cast<int64_t>(ui.b) * p.Hq + hq0 + j;
+    };
     if (u == a.u) pdl_wait();  // q (and the cache) may come from the previous kernel
     const int Tu = seq_end<kStep>(p, ui.b);
     const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
     const int ps = min((u == a.u) ? a.p : 0, pe);
+    // Multi-query (general kernels): the ends of the lane's two columns
+    // (token i does not see the unit's last n_q - 1 - i positions, all text).
+    const int endA = kGen ? Tu - (p.n_q - 1 - (c0 + 2 * tig) % p.n_q) : Tu;
+    const int endB = kGen ? Tu - (p.n_q - 1 - (c0 + 2 * tig + 1) % p.n_q) : Tu;
 
     // q of head column gid as the B operand, in the permuted d order; group sums.
     uint32_t qb[8][2];
@@ -892,7 +917,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       uint4 raw = make_uint4(0u, 0u, 0u, 0u);
       if (gid < nh)
         raw = __ldg(reinterpret_cast<const uint4*>(
-            p.q + (static_cast<int64_t>(ui.b) * p.Hq + hq0 + gid) * kD + 32 * P + 8 * tig));
+            p.q + out_row(gid) * kD + 32 * P + 8 * tig));
       const float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
                           bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
       qb[2 * P][0] = pack_f16x2(x[0], x[4]);
@@ -975,17 +1000,19 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       return nb;
     };
     if (ui.prot) {  // protected unit: bf16 rows only
-      walk_piece<kKO>(p, kClsProt, ps, pe, [&](int kind, int t0, int n) {
+      walk_piece<kGen>(p, kClsProt, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
         const int nb = deal(n, 32, first);
         for (int kb = first; kb < nb; kb += kConsumerWarps)
-          kblock<2, kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
-                                                  qb, zb, gid, tig, lane, acc);
+          kblock<2, kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n,
+                                                  kGen && kind == kTileText ? endA - t0 : kNoLimit,
+                                                  kGen && kind == kTileText ? endB - t0 : kNoLimit, sl2, qb,
+                                                  zb, gid, tig, lane, acc);
         end_tile();
       });
     } else {
-      walk_piece<kKO>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) {
+      walk_piece<kGen>(p, ui.cls, ps, pe, [&](int kind, int t0, int n) {
         const uint8_t* base = begin_tile(kind, t0, n);
         int first;
         if (kind == kTilePacked) {
@@ -998,9 +1025,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
             kblock<NHP, (KB < 16 ? kKPacked : kKBf16), (VB < 16 ? kVPacked : kVBf16D), KB, VB, G>(
-                base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16 * NHP, n, sl2,
-                qb, zb, gid, tig, lane, acc);
-        } else if (kKO && kind == kTileKonly) {  // bf16 K + packed V
+                base, base + p.pk_off_ksz, base + p.pk_off_vc, base + p.pk_off_vsz, kb * 16 * NHP, n,
+                kNoLimit, kNoLimit, sl2, qb, zb, gid, tig, lane, acc);
+        } else if (kGen && kind == kTileKonly) {  // bf16 K + packed V
           const int nb = deal(n, 32, first);
           if constexpr (VB < 16) {
             if (first < nb && !packed_acc) {
@@ -1010,8 +1037,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
             kblock<2, kKBf16, (VB < 16 ? kVPacked : kVBf16D), 16, VB, G>(
-                base, nullptr, base + p.ko_off_vc, base + p.ko_off_vsz, kb * 32, n, sl2, qb, zb, gid, tig,
-                lane, acc);
+                base, nullptr, base + p.ko_off_vc, base + p.ko_off_vsz, kb * 32, n, kNoLimit, kNoLimit, sl2,
+                qb, zb, gid, tig, lane, acc);
         } else {  // text rows of a packed or K-only unit
           const int nb = deal(n, 32, first);
           if constexpr (VB < 16) {
@@ -1021,7 +1048,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
             }
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
-            kblock<2, kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n, sl2,
+            kblock<2, kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n,
+                                                 kGen ? endA - t0 : kNoLimit, kGen ? endB - t0 : kNoLimit, sl2,
                                                  qb, zb, gid, tig, lane, acc);
         }
         end_tile();
@@ -1062,7 +1090,6 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     int cf = c, cl = c;
     if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
     const bool sole = kStep && cf == cl;
-    const int64_t row0 = static_cast<int64_t>(ui.b) * p.Hq + hq0;
     named_bar(1, kConsumerWarps * 32);
     const int64_t slot = static_cast<int64_t>(u) + c;
     for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
@@ -1082,8 +1109,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
       if (sole) {
         const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
-        p.out[(row0 + j) * kD + d] = f32_to_bf16_bits(O * inv);
-        if (d == 0 && p.lse) p.lse[row0 + j] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
+        const int64_t orow = out_row(j);
+        p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
+        if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
       } else {
         p.ws_o[(slot * kNH + j) * kD + d] = O;
         if (d == 0) {
@@ -1125,7 +1153,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
           float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
           for (int j = role; j < nh; j += nc)
-            combine_row<kConsumerWarps>(p, u, j, cf, cl, row0 + j, warp, lane, sm_ml, sm_o, bad,
+            combine_row<kConsumerWarps>(p, u, j, cf, cl, out_row(j), warp, lane, sm_ml, sm_o, bad,
                                         []() { named_bar(1, kConsumerWarps * 32); });
         }
       }
@@ -1134,8 +1162,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
 }
 
 // NHP: 16-row MMA halves per packed block (2 or 4; the launch's pk_halves).
-// kKO: the layout has K-only protected heads (a third unit class).
-template <int KB, int VB, int G, bool kStep, int NHP, bool kKO>
+// kGen: the general variant -- K-only protected heads (a third unit class)
+// and multi-query columns; the other variants run neither.
+template <int KB, int VB, int G, bool kStep, int NHP, bool kGen>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -1153,13 +1182,13 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
   __syncthreads();
   if (warp == kConsumerWarps) {
     if (lane == 0) {
-      producer_prefetch<kKO>(p, blockIdx.x);
+      producer_prefetch<kGen>(p, blockIdx.x);
       pdl_wait();  // the previous kernel in the stream may have written the cache
-      producer_loop<kStep, kKO>(p, sm, blockIdx.x);
+      producer_loop<kStep, kGen>(p, sm, blockIdx.x);
     }
     return;
   }
-  consumer_loop<KB, VB, G, kStep, NHP, kKO>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G, kStep, NHP, kGen>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq

@@ -64,7 +64,8 @@ extern "C" {
 #define KVQ_MAX_HEADS 128   /* H_kv limit (mask and slot tables are this long) */
 #define KVQ_NSEG 8          /* number of cache segments */
 #define KVQ_MAX_CTAS 1024   /* upper bound on split-KV work chunks per call */
-#define KVQ_HEADS_PER_UNIT 8 /* query heads handled together per KV head */
+#define KVQ_HEADS_PER_UNIT 8 /* query columns (query heads, or head x token pairs) handled together per KV head */
+#define KVQ_MAX_QUERY_TOKENS 64 /* query tokens per sequence of kvq_decode_attention_mq */
 
 typedef enum kvq_status {
   KVQ_OK = 0,
@@ -248,6 +249,60 @@ kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, const void* 
                                   const int32_t* t_new, int32_t T_max, float softmax_scale,
                                   void* out_bf16, float* lse, void* workspace, size_t ws_bytes,
                                   void* stream);
+
+/*
+ * kvq_decode_attention_mq -- multi-query decode: n_q query tokens per
+ * sequence (draft tokens being verified, or a chunk of new tokens), whose
+ * own K/V rows were appended at positions [T - n_q, T) before the call.
+ * Token i attends positions [0, T - n_q + 1 + i) (causal among the new
+ * tokens).  The (query head, token) pairs of a KV head share one pass over
+ * its cache: up to KVQ_HEADS_PER_UNIT of them are the N = 8 columns of one
+ * tensor-core tile (WSVD summary, section 2.라: QK, softmax and PV fused),
+ * so an MHA layer (g = 1) fills the tile with 8 tokens.
+ *   q_bf16    device bf16 [B][n_q][H_q][D], 16-byte aligned
+ *   n_q       1 <= n_q <= KVQ_MAX_QUERY_TOKENS
+ *   T         n_q <= T <= T_cap; the positions some token does not attend,
+ *             [T - n_q + 1, T), must lie outside [vis_start, vis_end)
+ *   out_bf16  device bf16 [B][n_q][H_q][D];  lse  fp32 [B][n_q][H_q] or NULL
+ *   workspace at least kvq_decode_mq_workspace_bytes(L, n_q) bytes (equal to
+ *             L->workspace_bytes for n_q = 1), 256-byte aligned
+ * n_q = 1 is kvq_decode_attention.  Other arguments and errors as there.
+ */
+size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q);
+kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                   int32_t n_q, int32_t T, float softmax_scale, void* out_bf16,
+                                   float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * kvq_sensitivity_probe -- how far the cache's quantisation moves attention,
+ * the model-free form of the K-vs-V study of "VLM_KV_Quantization",
+ * sections 3-4 (KL divergence of the distribution after quantising visual
+ * K or visual V alone -- same tokens, bits and group size -- from the
+ * unquantised one).  For every (b, hq), h = hq / g, in fp64:
+ *   kl_attn = D_KL(p || p_hat): p = softmax_t(scale q.k_t) over the raw bf16
+ *             K rows, p_hat the same over K as kvq_decode_attention reads it
+ *             (dequantised code * s + z, or the bf16 side store);
+ *   kl_out  = D_KL(P || P_hat): P = softmax(readout o), o the attention
+ *             output over the raw K/V rows, P_hat the same over the cache;
+ *   err     = ||o_hat - o||_2.
+ * To compare K with V, run it on two caches appended from the same rows with
+ * layouts that differ only in k_bits / v_bits (16 = unquantised).
+ *   cache, q_bf16, T, softmax_scale  as for kvq_decode_attention (positions [0, T))
+ *   k_bf16, v_bf16  device bf16, the raw rows that were appended: element
+ *             (b, h, t, d) at index b*stride_b + h*stride_h + t*stride_t + d;
+ *             16-byte aligned, strides >= 0 and multiples of 8 elements
+ *   readout   device fp32 [n_out][D], 4-byte aligned, 1 <= n_out <= 2048
+ *   result    device fp64 [B][H_q][3] = (kl_attn, kl_out, err), 8-byte aligned
+ *   workspace device scratch of at least kvq_probe_workspace_bytes(L, T)
+ *             bytes, 16-byte aligned; contents on entry are ignored
+ * Returns KVQ_ERR_UNSUPPORTED for D != 128 or B * H_q > 65535.
+ */
+size_t kvq_probe_workspace_bytes(const kvq_layout* L, int32_t T);
+kvq_status kvq_sensitivity_probe(const kvq_layout* L, const void* cache, const void* q_bf16,
+                                 const void* k_bf16, const void* v_bf16, int64_t stride_b,
+                                 int64_t stride_h, int64_t stride_t, int32_t T, float softmax_scale,
+                                 const float* readout, int32_t n_out, double* result, void* workspace,
+                                 size_t ws_bytes, void* stream);
 
 /* Size in bytes of the device scratch array used by
  * kvq_decode_attention_static_ws (16 MiB: enough for layouts with up to

@@ -20,7 +20,7 @@ def lib():
 
 def test_header_declares_what_library_exports(lib):
     text = open(HEADER).read()
-    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*|int)\s+(kvq_\w+)\s*\(", text, re.M))
+    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*|int|size_t)\s+(kvq_\w+)\s*\(", text, re.M))
     assert declared == set(kvq.EXPORTED_SYMBOLS)
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.lib_path()], capture_output=True,
                          text=True, check=True).stdout
@@ -241,3 +241,43 @@ def test_corrupted_layout_rejected(lib):
 def test_status_strings(lib):
     for code, name in kvq.STATUS.items():
         assert lib.kvq_status_string(code).decode() == name
+
+
+def test_probe_argument_checks(lib):
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ws = kvq.probe_workspace_bytes(L, 256)
+    assert ws > 0 and ws % 8 == 0
+    assert kvq.probe_workspace_bytes(L, 0) == 0
+    ok = dict(cache=FAKE, q=FAKE, k=FAKE, v=FAKE, strides=(4 * 256 * 128, 256 * 128, 128), T=200,
+              R=FAKE, n_out=64, res=FAKE, ws=FAKE, ws_bytes=ws)
+    for bad, code in ((dict(cache=0), 1), (dict(k=0), 1), (dict(v=FAKE + 4), 1), (dict(R=0), 1),
+                      (dict(res=FAKE + 4), 1), (dict(ws=0), 1), (dict(T=0), 1), (dict(T=257), 1),
+                      (dict(n_out=0), 1), (dict(n_out=2049), 1), (dict(strides=(8, 4, 128)), 1),
+                      (dict(k=FAKE + 8), 1),
+                      (dict(cache=FAKE + 128), 1), (dict(ws_bytes=ws - 1), 3)):
+        a = dict(ok)
+        a.update(bad)
+        st = lib.kvq_sensitivity_probe(ctypes.byref(L), a["cache"], a["q"], a["k"], a["v"],
+                                       *a["strides"], a["T"], 0.1, a["R"], a["n_out"], a["res"],
+                                       a["ws"], a["ws_bytes"], None)
+        assert st == code, (bad, st)
+
+
+def test_mq_argument_checks(lib):
+    # text 0-9 and 200-255, visual 10-199
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    assert kvq.decode_mq_workspace_bytes(L, 1) == L.workspace_bytes
+    assert kvq.decode_mq_workspace_bytes(L, 8) > L.workspace_bytes
+    assert kvq.decode_mq_workspace_bytes(L, 0) == 0
+    assert kvq.decode_mq_workspace_bytes(L, kvq.KVQ_MAX_QUERY_TOKENS + 1) == 0
+    ws4 = kvq.decode_mq_workspace_bytes(L, 4)
+    ok = dict(n_q=4, T=256, ws_bytes=ws4)
+    for bad, code in ((dict(n_q=0), 1), (dict(n_q=kvq.KVQ_MAX_QUERY_TOKENS + 1), 1),
+                      (dict(T=3), 1), (dict(T=257), 1),
+                      (dict(T=202), 1),   # token 0 would not see positions 199..201: 199 is visual
+                      (dict(ws_bytes=ws4 - 1), 3)):
+        a = dict(ok)
+        a.update(bad)
+        st = lib.kvq_decode_attention_mq(ctypes.byref(L), FAKE, FAKE, a["n_q"], a["T"], 0.1, FAKE, None,
+                                         FAKE, a["ws_bytes"], None)
+        assert st == code, (bad, st)
