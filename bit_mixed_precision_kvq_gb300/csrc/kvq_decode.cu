@@ -13,6 +13,7 @@
 // and reports lse = ln(2) * (M + log2 L).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -27,12 +28,13 @@ const void* split_kernel_k4(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k8(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k16(int vb, int G, bool step, int halves, bool general);
 
-constexpr int kCombineWarps = 16;
-
-// Combine: one CTA per output row (b, token i, hq), 16 warps (combine_row).
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ Params p) {
-  __shared__ float sm_ml[kCombineWarps][2];
-  __shared__ float4 sm_o[kCombineWarps][32];
+// Combine: one CTA per output row (b, token i, hq), NW warps (combine_row):
+// 16 when some unit has many chunks, 2 when every unit has at most 16 (the
+// two warps fold them in one pass, and many more rows are resident at once).
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) combine_kernel(const __grid_constant__ Params p) {
+  __shared__ float sm_ml[NW][2];
+  __shared__ float4 sm_o[NW][32];
   const int bq = blockIdx.x;  // (b * n_q + i) * Hq + hq
   const int bi = bq / p.Hq;
   const int hq = bq - bi * p.Hq;
@@ -44,8 +46,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   int cf, cl;
   plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
   pdl_wait();
-  combine_row<kCombineWarps>(p, u, c - hc * kNH, cf, cl, bq, threadIdx.x >> 5, threadIdx.x & 31, sm_ml,
-                             sm_o, false, []() { __syncthreads(); });
+  combine_row<NW>(p, u, c - hc * kNH, cf, cl, bq, threadIdx.x >> 5, threadIdx.x & 31, sm_ml, sm_o, false,
+                  []() { __syncthreads(); });
 }
 
 }  // namespace kvq
@@ -168,6 +170,26 @@ constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
 static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
 
 
+// Most chunks any unit of the plan is split over.
+int max_unit_chunks(const kvq::Params& p) {
+  const kvq::Plan& P = p.plan;
+  if (P.aligned) return std::max(std::max(P.n_p, P.n_k), P.n_q) + (P.R > 0 ? 1 : 0);
+  int best = 1;
+  int32_t run_u = -1, run = 0;  // chunks touching unit run_u so far (cuts are monotone)
+  for (int32_t c = 0; c < P.C; ++c) {
+    const int32_t u0 = p.cuts[c].u, u1 = kvq::chunk_last_unit(p.cuts, c, P.U);
+    if (u0 == run_u) ++run; else run = 1;
+    best = std::max(best, run);
+    if (u1 != u0) {  // the chunk ends in a later unit, which it starts
+      run_u = u1;
+      run = 1;
+    } else {
+      run_u = u0;
+    }
+  }
+  return best;
+}
+
 // The split kernel and the combine of one decode call (p prepared).
 kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p->pk_halves,
@@ -177,8 +199,10 @@ kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   if (st != KVQ_OK) return st;
   if (kvq_launch_pdl(split, p->plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, p) != 0)
     return KVQ_ERR_CUDA;
-  if (kvq_launch_pdl(reinterpret_cast<const void*>(&kvq::combine_kernel), L->d.B * p->n_q * L->d.H_q,
-                     kvq::kCombineWarps * 32, 0, stream, p) != 0)
+  const bool wide = max_unit_chunks(*p) > 16;
+  const void* comb = wide ? reinterpret_cast<const void*>(&kvq::combine_kernel<16>)
+                          : reinterpret_cast<const void*>(&kvq::combine_kernel<2>);
+  if (kvq_launch_pdl(comb, L->d.B * p->n_q * L->d.H_q, (wide ? 16 : 2) * 32, 0, stream, p) != 0)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

@@ -72,8 +72,16 @@ __device__ __forceinline__ int stored_slot(bool is_v, int bits, int d) {
   return 32 * t + 4 * (2 * P + (i >> 1)) + 2 * e + (i & 1);
 }
 
+// bf16 -> fp64 by assembling the fp64 bit pattern with integer operations
+// (GB300 issues fp64 arithmetic and conversions at 1/64 of the fp32 rate):
+// sign, exponent rebiased by 1023 - 127, mantissa shifted; zero, infinity
+// and NaN keep their meaning; a bf16 subnormal takes the conversion path.
 __device__ __forceinline__ double bf16d(uint16_t h) {
-  return static_cast<double>(__uint_as_float(static_cast<uint32_t>(h) << 16));
+  const uint32_t e = (h >> 7) & 0xffu, m = h & 0x7fu;
+  if (e == 0u && m != 0u) return static_cast<double>(__uint_as_float(static_cast<uint32_t>(h) << 16));
+  const uint32_t ed = e == 0u ? 0u : (e == 0xffu ? 0x7ffu : e + 896u);
+  const uint32_t hi = (static_cast<uint32_t>(h & 0x8000u) << 16) | (ed << 20) | (m << 13);
+  return __hiloint2double(static_cast<int>(hi), 0);
 }
 __device__ __forceinline__ double f16d(uint16_t h) {
   return static_cast<double>(__half2float(__ushort_as_half(h)));
@@ -88,9 +96,10 @@ __device__ __forceinline__ void load4_bf16(const uint8_t* row, int d0, double (&
   x[3] = bf16d(static_cast<uint16_t>(w.y >> 16));
 }
 
-// Elements d0 .. d0 + 3 of a packed row: code * s + z.
+// Elements d0 .. d0 + 3 of a packed row: code * s + z (ctab[c] = c as fp64,
+// a shared-memory table).
 __device__ __forceinline__ void load4_packed(const uint8_t* codes, const uint8_t* sz, bool is_v, int bits,
-                                             int G, int d0, double (&x)[4]) {
+                                             int G, int d0, const double* ctab, double (&x)[4]) {
   const int per_word = 32 / bits;
   const uint32_t mask = (1u << bits) - 1u;
   const uint16_t* szh = reinterpret_cast<const uint16_t*>(sz);
@@ -102,14 +111,14 @@ __device__ __forceinline__ void load4_packed(const uint8_t* codes, const uint8_t
     const uint32_t w = reinterpret_cast<const uint32_t*>(codes)[s / per_word];
     const uint32_t c = (w >> (bits * (s % per_word))) & mask;
     const int g = d / G;
-    x[j] = static_cast<double>(c) * f16d(szh[ng + g]) + f16d(szh[g]);
+    x[j] = ctab[c] * f16d(szh[ng + g]) + f16d(szh[g]);
   }
 }
 
 // Elements 4 lane .. 4 lane + 3 of K (is_v = false) or V at position t of
 // (b, h), as the decode reads them.
 __device__ __forceinline__ void load4_cached(const Params& p, bool is_v, int b, int h, int t, int lane,
-                                             double (&x)[4]) {
+                                             const double* ctab, double (&x)[4]) {
   const int d0 = 4 * lane;
   if (t < p.vs || t >= p.ve) {
     const int tr = t < p.vs ? t : t - p.Tv;
@@ -137,7 +146,7 @@ __device__ __forceinline__ void load4_cached(const Params& p, bool is_v, int b, 
     return;
   }
   const uint8_t* sz = p.seg[is_v ? KVQ_SEG_V_SZ : KVQ_SEG_K_SZ] + row * (is_v ? p.vszrow : p.kszrow);
-  load4_packed(codes, sz, is_v, bits, p.G, d0, x);
+  load4_packed(codes, sz, is_v, bits, p.G, d0, ctab, x);
 }
 
 __device__ __forceinline__ double warp_sum(double x) {
@@ -150,8 +159,8 @@ __device__ __forceinline__ double warp_sum(double x) {
 // row) and s_hat = q . k_hat (K as the decode reads it), both unscaled.
 // A packed K row is summed per group as s_g * sum_g q c + z_g * sum_g q.
 __device__ __forceinline__ void position_scores(const Params& p, const double* sq, const double* sQ,
-                                                const uint16_t* kraw, int b, int h, int t, double& s,
-                                                double& sh) {
+                                                const double* ctab, const uint16_t* kraw, int b, int h, int t,
+                                                double& s, double& sh) {
   s = 0.0;
 #pragma unroll 4
   for (int d0 = 0; d0 < kD; d0 += 8) {
@@ -198,7 +207,7 @@ __device__ __forceinline__ void position_scores(const Params& p, const double* s
     for (int d = g * p.G; d < (g + 1) * p.G; ++d) {
       const int sl = stored_slot(false, bits, d);
       const uint32_t c = (codes[sl / per_word] >> (bits * (sl % per_word))) & mask;
-      pg += sq[d] * static_cast<double>(c);
+      pg += sq[d] * ctab[c];
     }
     sh += f16d(sz[ng + g]) * pg + f16d(sz[g]) * sQ[g];
   }
@@ -213,6 +222,7 @@ __device__ __forceinline__ double warp_max(double x) {
 __global__ void __launch_bounds__(kProbeThreads) probe_partial(const __grid_constant__ ProbeArgs a) {
   __shared__ double sq[kD];      // q of the row
   __shared__ double sQ[kD / 32]; // its group sums (G >= 32)
+  __shared__ double ctab[256];   // code -> fp64
   const Params& p = a.p;
   const int row = blockIdx.y;  // b * Hq + hq
   const int b = row / p.Hq, hq = row - (row / p.Hq) * p.Hq;
@@ -221,6 +231,8 @@ __global__ void __launch_bounds__(kProbeThreads) probe_partial(const __grid_cons
   const int chunk = (a.T + a.S - 1) / a.S;
   const int t_begin = blockIdx.x * chunk, t_end = min(a.T, t_begin + chunk);
   sq[threadIdx.x] = bf16d(p.q[static_cast<int64_t>(row) * kD + threadIdx.x]);  // kProbeThreads == kD
+  ctab[threadIdx.x] = static_cast<double>(threadIdx.x);
+  ctab[threadIdx.x + kProbeThreads] = static_cast<double>(threadIdx.x + kProbeThreads);
   __syncthreads();
   if (threadIdx.x < kD / p.G) {
     double x = 0.0;
@@ -239,7 +251,7 @@ __global__ void __launch_bounds__(kProbeThreads) probe_partial(const __grid_cons
     const bool valid = t < t_end;
     double s = -INFINITY, sh = -INFINITY;
     if (valid) {
-      position_scores(p, sq, sQ, a.kin + b * a.sb + h * a.sh + t * a.st, b, h, t, s, sh);
+      position_scores(p, sq, sQ, ctab, a.kin + b * a.sb + h * a.sh + t * a.st, b, h, t, s, sh);
       s *= a.scale;
       sh *= a.scale;
     }
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kProbeThreads) probe_partial(const __grid_cons
       const int tj = tb + j;
       double v[4], vh[4];
       load4_bf16(reinterpret_cast<const uint8_t*>(a.vin + b * a.sb + h * a.sh + tj * a.st), 4 * lane, v);
-      load4_cached(p, true, b, h, tj, lane, vh);
+      load4_cached(p, true, b, h, tj, lane, ctab, vh);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         o[e] += wj * v[e];
