@@ -34,9 +34,6 @@ constexpr int kLanesPerRow = 4;                     // lanes per D = 128 row
 
 constexpr int kRowsPerWarp = 32 / kLanesPerRow;     // 8
 
-// The correctly rounded quotient, kept out of line: it is needed only for
-// near-ties.
-__device__ __noinline__ float exact_quotient(float d, float s) { return __fdiv_rn(d, s); }
 
 // The row's 4 lanes each own one slice of the stored row (kvq.h storage
 // order): K slice t = elements d = 32P + 8t + j (P = 0..3, j = 0..7); V
@@ -137,35 +134,53 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
   // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
   // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
   // it (0.5 - win is exact); only then is the IEEE division evaluated (out of
-  // line, rare).  Every lane runs the same instructions so the row's votes
-  // stay converged.
+  // line, rare), once per row slice after all its codes.  rint(u) comes from
+  // fl(u + 1.5 * 2^23): for |u| < 2^22 that sum is 1.5 * 2^23 + rint(u)
+  // exactly (round half to even), and its low mantissa bits are the signed
+  // integer -- no conversion instruction.  Every lane runs the same
+  // instructions so the row's votes stay converged.
   const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
   uint32_t out[BITS];
 #pragma unroll
   for (int q = 0; q < BITS; ++q) out[q] = 0u;
+  uint32_t need = 0;  // near-ties: bit 8k + j
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int g = k / CPG;
-    float d[8], u[8];
-    uint32_t need = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t pw = w[k][j >> 1];
       const float x = (j & 1) ? bf16_hi(pw) : bf16_lo(pw);
-      d[j] = __fsub_rn(x, zf[g]);
-      u[j] = __fmul_rn(d[j], rs[g]);
+      const float u = __fmul_rn(__fsub_rn(x, zf[g]), rs[g]);
+      const float t = __fadd_rn(u, kRound);
       // |u - rint(u)| is exact for |u| < 2^23; a near-tie lies within win of 1/2
-      if (fabsf(__fsub_rn(u[j], rintf(u[j]))) >= 0.5f - win) need |= 1u << j;
+      if (fabsf(__fsub_rn(u, __fsub_rn(t, kRound))) >= 0.5f - win) need |= 1u << (8 * k + j);
+      const int ci = static_cast<int>(__float_as_uint(t) - __float_as_uint(kRound));
+      const uint32_t code = static_cast<uint32_t>(min(max(ci, 0), static_cast<int>(cmax)));
+      out[dst_word<BITS, kV>(k, j)] |= code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
     }
-    if (__any_sync(gmask, need != 0)) {
+  }
+  if (__any_sync(gmask, need != 0)) {
+    // Rare: the flagged elements of each chunk one at a time; registers are
+    // picked with selects so that no array goes to local memory.
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (need & (1u << j)) u[j] = exact_quotient(d[j], sf[g]);
-    }
+    for (int k = 0; k < 4; ++k) {
+      uint32_t nk = (need >> (8 * k)) & 0xffu;
+#pragma unroll 1
+      while (nk) {
+        const int j = __ffs(nk) - 1;
+        nk &= nk - 1u;
+        const uint32_t lo = (j & 2) ? w[k][1] : w[k][0], hi = (j & 2) ? w[k][3] : w[k][2];
+        const uint32_t pw = (j & 4) ? hi : lo;
+        const float x = (j & 1) ? bf16_hi(pw) : bf16_lo(pw);
+        const float u = __fdiv_rn(__fsub_rn(x, zf[k / CPG]), sf[k / CPG]);
+        const uint32_t code = min(__float2uint_rn(u), cmax);  // round half to even; < 0 -> 0
+        const int wd = dst_word<BITS, kV>(k, j), bt = dst_bit<BITS, kV>(k, j);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t code = min(__float2uint_rn(u[j]), cmax);  // round half to even; < 0 -> 0
-      out[dst_word<BITS, kV>(k, j)] += code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
+        for (int q = 0; q < BITS; ++q)
+          if (q == wd) out[q] = (out[q] & ~(cmax << bt)) | (code << bt);
+      }
     }
   }
   uint8_t* dst = codes_row + part * 4 * BITS;
@@ -197,7 +212,7 @@ __device__ __forceinline__ int v_elem(int k, int q, int part) {
 // One warp per (b, h, 8 consecutive positions); 4 lanes per row, each lane
 // the elements of its slice of the stored row (K: four 16-byte loads; V:
 // sixteen 4-byte loads, all in flight before any use).
-__global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendArgs a) {
+__global__ void __launch_bounds__(256, 3) append_kernel(const __grid_constant__ AppendArgs a) {
   pdl_wait();  // the previous kernel in the stream may still read the cache
   pdl_launch_dependents();
   const Params& p = a.p;
