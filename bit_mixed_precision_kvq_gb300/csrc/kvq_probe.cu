@@ -155,23 +155,31 @@ __device__ __forceinline__ double warp_sum(double x) {
   return x;
 }
 
+// q . x for a bf16 row x (16-byte aligned), with four independent partial
+// sums (a single chain of dependent fp64 FMAs would leave the FP64 pipe idle
+// for most of its latency).
+__device__ __forceinline__ double dot_bf16_row(const double* sq, const uint8_t* row) {
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};
+#pragma unroll 2
+  for (int d0 = 0; d0 < kD; d0 += 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + 2 * d0);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc[e] = fma(sq[d0 + 2 * e], bf16d(static_cast<uint16_t>(ws[e] & 0xffffu)), acc[e]);
+      acc[e] = fma(sq[d0 + 2 * e + 1], bf16d(static_cast<uint16_t>(ws[e] >> 16)), acc[e]);
+    }
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Scores of one position for the lane that owns it: s = q . k (raw bf16 K
 // row) and s_hat = q . k_hat (K as the decode reads it), both unscaled.
 // A packed K row is summed per group as s_g * sum_g q c + z_g * sum_g q.
 __device__ __forceinline__ void position_scores(const Params& p, const double* sq, const double* sQ,
                                                 const double* ctab, const uint16_t* kraw, int b, int h, int t,
                                                 double& s, double& sh) {
-  s = 0.0;
-#pragma unroll 4
-  for (int d0 = 0; d0 < kD; d0 += 8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(kraw + d0);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      s += sq[d0 + 2 * e] * bf16d(static_cast<uint16_t>(ws[e] & 0xffffu));
-      s += sq[d0 + 2 * e + 1] * bf16d(static_cast<uint16_t>(ws[e] >> 16));
-    }
-  }
+  s = dot_bf16_row(sq, reinterpret_cast<const uint8_t*>(kraw));
   // where the decode reads this K row
   const uint8_t* bf = nullptr;
   if (t < p.vs || t >= p.ve) {
@@ -184,17 +192,7 @@ __device__ __forceinline__ void position_scores(const Params& p, const double* s
   const int64_t prow = (static_cast<int64_t>(b) * p.n_packed + p.slot[h]) * p.Tv_pad + (t - p.vs);
   if (!bf && p.kb == 16) bf = p.seg[KVQ_SEG_K_CODES] + prow * p.krow;
   if (bf) {
-    sh = 0.0;
-#pragma unroll 4
-    for (int d0 = 0; d0 < kD; d0 += 8) {
-      const uint4 w = *reinterpret_cast<const uint4*>(bf + 2 * d0);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sh += sq[d0 + 2 * e] * bf16d(static_cast<uint16_t>(ws[e] & 0xffffu));
-        sh += sq[d0 + 2 * e + 1] * bf16d(static_cast<uint16_t>(ws[e] >> 16));
-      }
-    }
+    sh = dot_bf16_row(sq, bf);
     return;
   }
   const int bits = p.kb, per_word = 32 / bits, ng = kD / p.G;
@@ -203,13 +201,16 @@ __device__ __forceinline__ void position_scores(const Params& p, const double* s
   const uint16_t* sz = reinterpret_cast<const uint16_t*>(p.seg[KVQ_SEG_K_SZ] + prow * p.kszrow);
   sh = 0.0;
   for (int g = 0; g < ng; ++g) {
-    double pg = 0.0;
-    for (int d = g * p.G; d < (g + 1) * p.G; ++d) {
-      const int sl = stored_slot(false, bits, d);
-      const uint32_t c = (codes[sl / per_word] >> (bits * (sl % per_word))) & mask;
-      pg += sq[d] * ctab[c];
+    double pg[4] = {0.0, 0.0, 0.0, 0.0};
+    for (int d = g * p.G; d < (g + 1) * p.G; d += 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int sl = stored_slot(false, bits, d + e);
+        const uint32_t c = (codes[sl / per_word] >> (bits * (sl % per_word))) & mask;
+        pg[e] = fma(sq[d + e], ctab[c], pg[e]);
+      }
     }
-    sh += f16d(sz[ng + g]) * pg + f16d(sz[g]) * sQ[g];
+    sh += f16d(sz[ng + g]) * ((pg[0] + pg[1]) + (pg[2] + pg[3])) + f16d(sz[g]) * sQ[g];
   }
 }
 
@@ -354,12 +355,16 @@ __global__ void __launch_bounds__(kProbeThreads) probe_finish(const __grid_const
   double zmax = -INFINITY, zhmax = -INFINITY;
   for (int i = threadIdx.x; i < a.n_out; i += kProbeThreads) {
     const float* r = a.R + static_cast<int64_t>(i) * kD;
-    double z = 0.0, zh = 0.0;
-    for (int e = 0; e < kD; ++e) {
-      const double w = static_cast<double>(r[e]);
-      z += w * so[e];
-      zh += w * soh[e];
+    double za[2] = {0.0, 0.0}, zha[2] = {0.0, 0.0};  // two chains per side (FP64 latency)
+#pragma unroll 4
+    for (int e = 0; e < kD; e += 2) {
+      const float2 w2 = *reinterpret_cast<const float2*>(r + e);
+      za[0] = fma(static_cast<double>(w2.x), so[e], za[0]);
+      za[1] = fma(static_cast<double>(w2.y), so[e + 1], za[1]);
+      zha[0] = fma(static_cast<double>(w2.x), soh[e], zha[0]);
+      zha[1] = fma(static_cast<double>(w2.y), soh[e + 1], zha[1]);
     }
+    const double z = za[0] + za[1], zh = zha[0] + zha[1];
     zbuf[i] = z;
     zbuf[a.n_out + i] = zh;
     zmax = fmax(zmax, z);
@@ -419,7 +424,7 @@ extern "C" kvq_status kvq_sensitivity_probe(const kvq_layout* L, const void* cac
     return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(cache) % 256 || reinterpret_cast<uintptr_t>(q_bf16) % 16 ||
       reinterpret_cast<uintptr_t>(k_bf16) % 16 || reinterpret_cast<uintptr_t>(v_bf16) % 16 ||
-      reinterpret_cast<uintptr_t>(readout) % 4 || reinterpret_cast<uintptr_t>(result) % 8 ||
+      reinterpret_cast<uintptr_t>(readout) % 8 || reinterpret_cast<uintptr_t>(result) % 8 ||
       reinterpret_cast<uintptr_t>(workspace) % 16)
     return KVQ_ERR_INVALID_ARG;
   if (stride_b % 8 || stride_h % 8 || stride_t % 8 || stride_b < 0 || stride_h < 0 || stride_t < 0)

@@ -291,7 +291,7 @@ kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const
  *   k_bf16, v_bf16  device bf16, the raw rows that were appended: element
  *             (b, h, t, d) at index b*stride_b + h*stride_h + t*stride_t + d;
  *             16-byte aligned, strides >= 0 and multiples of 8 elements
- *   readout   device fp32 [n_out][D], 4-byte aligned, 1 <= n_out <= 2048
+ *   readout   device fp32 [n_out][D], 8-byte aligned, 1 <= n_out <= 2048
  *   result    device fp64 [B][H_q][3] = (kl_attn, kl_out, err), 8-byte aligned
  *   workspace device scratch of at least kvq_probe_workspace_bytes(L, T)
  *             bytes, 16-byte aligned; contents on entry are ignored

@@ -253,7 +253,7 @@ def test_probe_argument_checks(lib):
     for bad, code in ((dict(cache=0), 1), (dict(k=0), 1), (dict(v=FAKE + 4), 1), (dict(R=0), 1),
                       (dict(res=FAKE + 4), 1), (dict(ws=0), 1), (dict(T=0), 1), (dict(T=257), 1),
                       (dict(n_out=0), 1), (dict(n_out=2049), 1), (dict(strides=(8, 4, 128)), 1),
-                      (dict(k=FAKE + 8), 1),
+                      (dict(k=FAKE + 8), 1), (dict(R=FAKE + 4), 1),
                       (dict(cache=FAKE + 128), 1), (dict(ws_bytes=ws - 1), 3)):
         a = dict(ok)
         a.update(bad)
