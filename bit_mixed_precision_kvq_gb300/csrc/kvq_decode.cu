@@ -300,7 +300,8 @@ extern "C" kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* c
   if (!L) return KVQ_ERR_INVALID_ARG;
   if (n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS || T < n_q) return KVQ_ERR_INVALID_ARG;
   // the positions some tokens do not attend, [T - n_q + 1, T), must be text
-  if (n_q > 1 && T - n_q + 1 < L->d.vis_end && T > L->d.vis_start) return KVQ_ERR_INVALID_ARG;
+  if (n_q > 1 && L->d.vis_start < L->d.vis_end && T - n_q + 1 < L->d.vis_end && T > L->d.vis_start)
+    return KVQ_ERR_INVALID_ARG;
   kvq::Params* p = &g_params;
   const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p, n_q);

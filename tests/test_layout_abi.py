@@ -281,3 +281,8 @@ def test_mq_argument_checks(lib):
         st = lib.kvq_decode_attention_mq(ctypes.byref(L), FAKE, FAKE, a["n_q"], a["T"], 0.1, FAKE, None,
                                          FAKE, a["ws_bytes"], None)
         assert st == code, (bad, st)
+    # an empty visual range leaves every position text: no constraint on T
+    L0 = kvq.cache_layout(2, 8, 4, 128, 256, 10, 10, 4, 4, 32, [])
+    st = lib.kvq_decode_attention_mq(ctypes.byref(L0), FAKE, FAKE, 4, 12, 0.1, FAKE, None, FAKE,
+                                     kvq.decode_mq_workspace_bytes(L0, 4) - 1, None)
+    assert st == 3  # past the position check, stopped by the workspace size
