@@ -157,7 +157,7 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
       // |u - rint(u)| is exact for |u| < 2^23; a near-tie lies within win of 1/2
       if (fabsf(__fsub_rn(u, __fsub_rn(t, kRound))) >= 0.5f - win) need |= 1u << (8 * k + j);
       const int ci = static_cast<int>(__float_as_uint(t) - __float_as_uint(kRound));
-      const uint32_t code = static_cast<uint32_t>(min(max(ci, 0), static_cast<int>(cmax)));
+      const uint32_t code = static_cast<uint32_t>(__vimin_s32_relu(ci, static_cast<int>(cmax)));
       out[dst_word<BITS, kV>(k, j)] |= code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
     }
   }

@@ -192,7 +192,7 @@ struct Params {
   // fused decode step only
   const uint16_t* k_new;  // bf16 [B][Hkv][D]
   const uint16_t* v_new;
-  int32_t t_new;          // the step's position (= T - 1), a text position
+  int32_t t_new;          // uniform fused step: its position (= T - 1); the kernels use each unit's end
   uint32_t* cnt;          // per-unit arrival counters (zero between calls)
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
