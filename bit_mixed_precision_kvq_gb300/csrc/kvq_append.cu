@@ -128,17 +128,18 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
       reinterpret_cast<__half*>(sz_row)[NG + g] = sh;
     }
   }
-  // code = clamp(rint(fl(fl(x - z) / s))).  The quotient is first formed as
-  // fl(d * fl(1/s)), within 3 * 2^-24 |u| of the correctly rounded one; rint
-  // is constant between half-integers, so both give the same code unless the
-  // product lies within that distance of k + 1/2.  |u| <= 1.5 (2^b - 1) + 1
-  // for finite inputs, so a fixed window of 2^-21 (2 (2^b - 1) + 2) covers
-  // it (0.5 - win is exact); only then is the IEEE division evaluated (out of
-  // line, rare), once per row slice after all its codes.  rint(u) comes from
-  // fl(u + 1.5 * 2^23): for |u| < 2^22 that sum is 1.5 * 2^23 + rint(u)
-  // exactly (round half to even), and its low mantissa bits are the signed
-  // integer -- no conversion instruction.  Every lane runs the same
-  // instructions so the row's votes stay converged.
+  // code = clamp(rint(fl(fl(x - z) / s))).  With d = fl(x - z) and
+  // rs = fl(1/s), the exact product p = d * rs is within 2^-24 |q| of the
+  // quotient q = d / s, so rint(p) = rint(q) unless p lies that close to
+  // k + 1/2.  One FMA, t = fl(p + 1.5 * 2^23), rounds p to an integer once
+  // (|p| < 2^22: t = 1.5 * 2^23 + rint(p), half to even) and its low mantissa
+  // bits are that integer -- no conversion instruction; a second FMA gives
+  // e = fl(p - rint(p)), within 2^-25 of the exact distance.  |q| <= 1.5
+  // (2^b - 1) + 1 for finite inputs, so a window of 2^-21 (2 (2^b - 1) + 2)
+  // around 1/2 (0.5 - win is exact) holds every near-tie with room to
+  // spare; only those are redone with the IEEE division (rare), after one
+  // vote for the row slice.  Every lane runs the same instructions so the
+  // row's votes stay converged.
   const float win = 4.76837158203125e-7f * (2.0f * static_cast<float>(cmax) + 2.0f);
   constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
   uint32_t out[BITS];
@@ -152,13 +153,13 @@ __device__ __forceinline__ void quantize_lane(const uint32_t (&w)[4][4], int par
     for (int j = 0; j < 8; ++j) {
       const uint32_t pw = w[k][j >> 1];
       const float x = (j & 1) ? bf16_hi(pw) : bf16_lo(pw);
-      const float u = __fmul_rn(__fsub_rn(x, zf[g]), rs[g]);
-      const float t = __fadd_rn(u, kRound);
-      // |u - rint(u)| is exact for |u| < 2^23; a near-tie lies within win of 1/2
-      if (fabsf(__fsub_rn(u, __fsub_rn(t, kRound))) >= 0.5f - win) need |= 1u << (8 * k + j);
+      const float d = __fsub_rn(x, zf[g]);
+      const float t = __fmaf_rn(d, rs[g], kRound);
+      const float e = __fmaf_rn(d, rs[g], -__fsub_rn(t, kRound));
+      if (fabsf(e) >= 0.5f - win) need |= 1u << (8 * k + j);
       const int ci = static_cast<int>(__float_as_uint(t) - __float_as_uint(kRound));
       const uint32_t code = static_cast<uint32_t>(__vimin_s32_relu(ci, static_cast<int>(cmax)));
-      out[dst_word<BITS, kV>(k, j)] |= code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
+      out[dst_word<BITS, kV>(k, j)] += code << dst_bit<BITS, kV>(k, j);  // disjoint bit fields
     }
   }
   if (__any_sync(gmask, need != 0)) {
