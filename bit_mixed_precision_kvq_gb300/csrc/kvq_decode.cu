@@ -170,26 +170,6 @@ constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
 static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
 
 
-// Most chunks any unit of the plan is split over.
-int max_unit_chunks(const kvq::Params& p) {
-  const kvq::Plan& P = p.plan;
-  if (P.aligned) return std::max(std::max(P.n_p, P.n_k), P.n_q) + (P.R > 0 ? 1 : 0);
-  int best = 1;
-  int32_t run_u = -1, run = 0;  // chunks touching unit run_u so far (cuts are monotone)
-  for (int32_t c = 0; c < P.C; ++c) {
-    const int32_t u0 = p.cuts[c].u, u1 = kvq::chunk_last_unit(p.cuts, c, P.U);
-    if (u0 == run_u) ++run; else run = 1;
-    best = std::max(best, run);
-    if (u1 != u0) {  // the chunk ends in a later unit, which it starts
-      run_u = u1;
-      run = 1;
-    } else {
-      run_u = u0;
-    }
-  }
-  return best;
-}
-
 // The split kernel and the combine of one decode call (p prepared).
 kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p->pk_halves,
@@ -199,7 +179,7 @@ kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   if (st != KVQ_OK) return st;
   if (kvq_launch_pdl(split, p->plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, p) != 0)
     return KVQ_ERR_CUDA;
-  const bool wide = max_unit_chunks(*p) > 16;
+  const bool wide = kvq::plan_max_unit_chunks(p->plan, p->cuts) > 16;
   const void* comb = wide ? reinterpret_cast<const void*>(&kvq::combine_kernel<16>)
                           : reinterpret_cast<const void*>(&kvq::combine_kernel<2>);
   if (kvq_launch_pdl(comb, L->d.B * p->n_q * L->d.H_q, (wide ? 16 : 2) * 32, 0, stream, p) != 0)

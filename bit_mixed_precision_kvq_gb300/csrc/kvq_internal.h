@@ -155,6 +155,23 @@ KVQ_HD void plan_unit_chunks(const Plan& P, const Cut* cuts, int32_t u, int32_t*
   *c_first = lo;
 }
 
+// Most chunks any unit of the plan is split over (host; sizes the combine).
+inline int32_t plan_max_unit_chunks(const Plan& P, const Cut* cuts) {
+  if (P.aligned) {
+    const int32_t n = P.n_p > P.n_k ? P.n_p : P.n_k;
+    return (n > P.n_q ? n : P.n_q) + (P.R > 0 ? 1 : 0);
+  }
+  int32_t best = 1, run_u = -1, run = 0;  // chunks touching unit run_u so far (cuts are monotone)
+  for (int32_t c = 0; c < P.C; ++c) {
+    const int32_t u0 = cuts[c].u, u1 = chunk_last_unit(cuts, c, P.U);
+    run = u0 == run_u ? run + 1 : 1;
+    if (run > best) best = run;
+    run_u = u1;
+    if (u1 != u0) run = 1;  // the chunk ends in a later unit, which it starts
+  }
+  return best;
+}
+
 // Decode workspace: the per-unit arrival counters of the fused step, then one
 // partial (o[kNH][kD] fp32, then (m, l)[kNH] fp32 in a second array) per
 // slot, slots <= units + C - 1 <= units + KVQ_MAX_CTAS - 1; each part

@@ -1,7 +1,8 @@
 // Host-side check of the split-KV work plan (kvq_make_plan + kvq_plan_cuts +
 // plan_unit_chunks) over many random layouts: every unit's positions are
 // covered exactly once by the chunks' pieces, the per-unit chunk ranges
-// agree with a brute-force scan, partial slots u + c are unique, visual cuts
+// agree with a brute-force scan (and so does the most chunks of any unit),
+// multi-query plans have their unit count, partial slots u + c are unique, visual cuts
 // of packed units are 16-row aligned, and with at least as many chunks as
 // units no chunk holds work of two units.  Prints "ok" or the first failure.
 #include <cstdio>
@@ -58,7 +59,10 @@ int main(int argc, char** argv) {
     if (kvq_cache_layout(&d, &L) != KVQ_OK) FAIL("layout rejected at case %d", it);
     const int T = 1 + static_cast<int>(next(static_cast<uint32_t>(d.T_cap)));
     const int targets[] = {1, 7, 152, 304, 1024};
-    kvq::Plan P = kvq_make_plan(&L, T, targets[next(5)]);
+    const int nqs[] = {1, 1, 2, 3, 8, 64};  // query tokens (multi-query plans have more units)
+    const int n_q = nqs[next(6)];
+    kvq::Plan P = kvq_make_plan(&L, T, targets[next(5)], n_q);
+    if (P.U != d.B * d.H_kv * ((L.g * n_q + kvq::kNH - 1) / kvq::kNH)) FAIL("case %d: unit count", it);
     kvq_plan_cuts(&P, cuts);
     (P.aligned ? n_aligned : n_stream)++;
     if (cuts[0].u != 0 || cuts[0].p != 0) FAIL("case %d: cut 0 = (%d,%d)", it, cuts[0].u, cuts[0].p);
@@ -84,6 +88,7 @@ int main(int argc, char** argv) {
       }
       if (P.aligned && work_units > 1) FAIL("case %d: chunk %d spans %d units", it, c, work_units);
     }
+    int most = 0;
     for (int u = 0; u < P.U; ++u) {
       if (covered[u] != P.T) FAIL("case %d: unit %d covered to %d of %d", it, u, covered[u], P.T);
       int bf = -1, bl = -1;
@@ -97,7 +102,11 @@ int main(int argc, char** argv) {
       kvq::plan_unit_chunks(P, cuts, u, &cf, &cl);
       if (cf != bf || cl != bl)
         FAIL("case %d (aligned %d): unit %d chunks [%d,%d], brute force [%d,%d]", it, P.aligned, u, cf, cl, bf, bl);
+      if (bl - bf + 1 > most) most = bl - bf + 1;
     }
+    if (kvq::plan_max_unit_chunks(P, cuts) != most)
+      FAIL("case %d (aligned %d): most chunks per unit %d, brute force %d", it, P.aligned,
+           kvq::plan_max_unit_chunks(P, cuts), most);
   }
   std::printf("ok %d cases (%d per-unit, %d stream)\n", cases, n_aligned, n_stream);
   return 0;
