@@ -267,6 +267,8 @@ kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, const void* 
  *   workspace at least kvq_decode_mq_workspace_bytes(L, n_q) bytes (equal to
  *             L->workspace_bytes for n_q = 1), 256-byte aligned
  * n_q = 1 is kvq_decode_attention.  Other arguments and errors as there.
+ * kvq_decode_mq_workspace_bytes returns 0 for an invalid layout or n_q
+ * outside [1, KVQ_MAX_QUERY_TOKENS].
  */
 size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q);
 kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const void* q_bf16,
@@ -296,6 +298,7 @@ kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const
  *   workspace device scratch of at least kvq_probe_workspace_bytes(L, T)
  *             bytes, 16-byte aligned; contents on entry are ignored
  * Returns KVQ_ERR_UNSUPPORTED for D != 128 or B * H_q > 65535.
+ * kvq_probe_workspace_bytes returns 0 for an invalid layout or T < 1.
  */
 size_t kvq_probe_workspace_bytes(const kvq_layout* L, int32_t T);
 kvq_status kvq_sensitivity_probe(const kvq_layout* L, const void* cache, const void* q_bf16,
