@@ -40,6 +40,7 @@ CASES = [
     (Case(3, 4, 2, 64, 20, 40, 4, 4, 64, []), 5, 5),                      # all in the text prefix
     (Case(1, 4, 4, 400, 16, 300, 2, 4, 32, [0]), 64, 400),                # g = 1, 64 tokens: 8 units
     (Case(2, 16, 2, 2500, 30, 2400, 4, 2, 64, [], konly=[1]), 6, 2450),   # long history, K-only head
+    (Case(16, 16, 16, 130, 10, 120, 4, 2, 32, [3]), 8, 130),              # 256 units: stream-cut plan
 ]
 
 
