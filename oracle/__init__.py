@@ -5,8 +5,10 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 and shares no code with it.
 
 The arithmetic lives in ``kvq_oracle.cpp`` (plain C++, fp32 quantiser spec,
-fp64 attention); this module only builds and loads that library with ctypes
-and offers numpy-level wrappers.  ``build_oracle()`` compiles it with g++ and
+fp64 attention); this module builds and loads that library with ctypes and
+offers numpy-level wrappers.  The one computation written here is the K-vs-V
+sensitivity reference (``sensitivity_reference``): fp64 divergences in numpy
+over the library's reconstruction, attention weights and outputs.  ``build_oracle()`` compiles it with g++ and
 ``-ffp-contract=off`` so that no multiply-add is fused on any host.
 """
 from __future__ import annotations
