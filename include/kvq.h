@@ -41,8 +41,11 @@
  *
  * Conventions for every entry point:
  *   - All device buffers are allocated and owned by the caller.  The library
- *     allocates no device memory and keeps no state between calls except a
- *     per-device cache of the SM count.
+ *     allocates no device memory (kvq_decode_attention_static_ws uses a
+ *     fixed array of its device image) and keeps no state between calls
+ *     except host-side caches: the SM count per device, the kernel
+ *     attributes it has set, and whether the runtime accepted programmatic
+ *     dependent launch.
  *   - Every argument is checked on the host before any launch; a failed
  *     check returns a status and launches nothing.  A launch failure returns
  *     KVQ_ERR_CUDA.  Faults of already-launched kernels surface at the
