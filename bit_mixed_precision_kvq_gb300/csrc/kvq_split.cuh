@@ -9,24 +9,27 @@
 //   producer : one lane walks the CTA's tiles and issues 1-D bulk async
 //              copies (TMA) of the tile's K/V rows (+ scale/zero rows) into a
 //              5-stage ring of 32 KB stages, signalled by mbarriers.
-//   consumers: the CTA's 32-position blocks are dealt round-robin to the 11
-//              warps across tile boundaries (every warp still waits for and
-//              releases every tile, which keeps the mbarrier phases exact).  QK and PV
-//              run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
-//              accumulate) with the unit's <= 8 query heads as N = 8; a block
-//              is two 16-row MMA halves sharing one softmax update:
+//   consumers: the CTA's blocks (32 positions, or 64 for long packed
+//              chunks) are dealt round-robin to the 11 warps across tile
+//              boundaries (every warp still waits for and releases every
+//              tile, which keeps the mbarrier phases exact).  QK and PV run on
+//              the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate)
+//              with the unit's <= 8 query columns as N = 8; a block is two (or
+//              four) 16-row MMA halves sharing one softmax update:
 //                QK: S^T[t][j] = K[t][:] . q[j][:]    (M = 16 positions)
 //                PV: O^T[d][j] += V^T[d][t] P^T[t][j] (M = 16 of the D rows)
-//              K codes enter QK as the fp16 values v = 1 + c * 2^-m (code in
-//              the mantissa below the 1.0 exponent; m = b for 2/4 bits, 10 for
-//              8 bits), so per quantisation group
-//                sum_d q_d c_d = 2^m (sum_d q_d v_d - sum_d q_d)
-//                q.k_hat = sum_g ( 2^m s_g * sum_g q v + (z_g - 2^m s_g) * sum_g q ).
-//              V codes become exact fp16 integers (1024 + c, minus 1024) and are
-//              dequantised per element in f16x2 (c*s + z, one rounding)
-//              because the PV reduction runs over positions.
-// Per unit piece the 4 warps' (m, l, o) are merged in shared memory and
-// written to the workspace slot (unit + chunk).
+//              Packed codes enter the MMAs as exact fp16 subnormals (a code
+//              masked in place at mantissa bits [p, p + b) is c * 2^(p - 24));
+//              the storage order of the rows (kvq.h) makes every operand
+//              register one AND of a word.  Per quantisation group
+//                q.k_hat = s_g * sum_g q c + z_g * sum_g q
+//              (the z-term on the tensor cores as well); for V the scales
+//              fold into the B operand (s * P^T per group) and the zeros
+//              accumulate in a separate MMA fragment.  Details at the
+//              fragment builders below.
+// Per unit piece the 11 warps' (m, l, o) are merged in shared memory and
+// either finish the unit (fused step, unit held by one CTA) or go to the
+// workspace slot (unit + chunk) for the cross-split combine.
 #pragma once
 
 #include "kvq_device.cuh"
