@@ -1,5 +1,8 @@
-// kvq_decode.cu -- kvq_decode_attention: host launcher for the split-KV
-// partial kernel (kvq_split.cuh) and the cross-split log-sum-exp combine.
+// kvq_decode.cu -- the decode entry points (kvq_decode_attention and its
+// ragged and multi-query forms, kvq_decode_step and its ragged form): argument
+// checks, the work plan, and the launches of the split-KV kernel
+// (kvq_split.cuh) and, for the two-call forms, the cross-split log-sum-exp
+// combine.
 //
 // Method sources: WSVD summary (gist.science 2604.02570), section 2.라 --
 // K/V are rebuilt on chip inside a flash-decoding pipeline and used at once

@@ -2,9 +2,11 @@
 //
 // Work decomposition for split-KV decoding (flash-decoding pipeline of the
 // WSVD summary, section 2.라, restated for a mixed-precision cache):
-//   * a "unit" is one (sequence b, KV head h, chunk hc of up to 8 of the g
-//     query heads that read h).  Protected-head units come first, then the
-//     packed-head units; inside each kind the order is (b, slot, hc).
+//   * a "unit" is one (sequence b, KV head h, chunk hc of up to 8 of the
+//     query columns that read h: its g query heads, or for a multi-query
+//     call its g * n_q (head, token) pairs).  Protected-head units come
+//     first, then the K-only ones, then the packed-head units; inside each
+//     class the order is (b, slot, hc).
 //   * every unit is a stream of positions 0..T-1; a position costs its cache
 //     bytes -- 512 (bf16 K + V rows), or for a visual position of a packed
 //     head the packed K and V rows plus their fp16 scale/zero -- plus a
