@@ -42,10 +42,34 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# roofline kernel, from one ncu capture of the same launch configuration with
-# the current kernels: (workload, layers, fused) -> bytes.  Other workloads:
-# not captured (null).
-NCU_TRAFFIC = {("llava_ov_7b", 28, True): 5450496}
+# roofline kernel from one ncu capture, keyed by the hash of the CUDA sources
+# it was taken with (kernel_source_hash) and then by (workload, layers,
+# fused).  A source change makes the key miss, so a stale count is reported
+# as null rather than carried over.
+NCU_TRAFFIC = {}
+
+# Extra workloads timed in every default run (the "sweep" object of the JSON
+# line): (workload, history T or None, layer ids or None = all layers).
+SWEEP = [
+    ("longctx", 4096, None),
+    ("longctx", 16384, None),
+    ("longctx", 32768, None),
+    ("llava15_7b", None, None),
+    ("llava_next_13b", None, [0, 4]),
+]
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the library's sources (the
+    kernels, their headers and the public header), in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_mixed_precision_kvq_gb300", "csrc")
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h", ".cpp")))
+    for f in files + ["../../include/kvq.h"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 METRIC = ("decode-attention µs/step and achieved HBM GB/s (compressed bytes) vs 8 TB/s peak")
 UNIT = "GB/s"
@@ -61,6 +85,9 @@ def parse_args():
     ap.add_argument("--T", type=int, default=None, help="history length for the longctx workload")
     ap.add_argument("--layers", type=int, default=None, help="limit layers (parity/debug only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the other workloads' per-launch lines (long context 4K/16K/32K, "
+                         "LLaVA-1.5, LLaVA-Next decode and append)")
     ap.add_argument("--fused", choices=["yes", "no"], default="yes",
                     help="kvq_decode_step (one launch per layer) or append + decode (three)")
     ap.add_argument("--prefill-in-step", choices=["auto", "yes", "no"], default="auto",
@@ -221,7 +248,7 @@ class Model:
     """Per-layer caches (history quantised once), per-step inputs, outputs."""
 
     def __init__(self, w: synth.Workload, dev, n_layers: int, prefill_in_step: bool = False,
-                 fused: bool = True, n_q: int = 1):
+                 fused: bool = True, n_q: int = 1, layer_ids=None):
         import bit_mixed_precision_kvq_gb300 as kvq
         self.kvq = kvq
         self.n_q = n_q
@@ -232,7 +259,9 @@ class Model:
         self.prefill_in_step = prefill_in_step
         self.layers = []
         self.ws = {}  # one workspace per unit count (its counter area is sized by it)
-        for l in range(n_layers):
+        self.layer_ids = list(range(n_layers)) if layer_ids is None else list(layer_ids)
+        n_layers = len(self.layer_ids)
+        for l in self.layer_ids:
             ls = w.layers[l]
             L = kvq.cache_layout(w.B, w.H_q, w.H_kv, w.D, self.T, w.vis_start, w.vis_end,
                                  ls.k_bits, ls.v_bits, w.group_size, ls.protected)
@@ -254,18 +283,19 @@ class Model:
         nL = n_layers
         # per-step device inputs/outputs, packed per layer so that the e2e leg
         # moves them with one copy each way
+        ids = self.layer_ids
         if n_q == 1:
-            self.q = torch.stack([synth.make_q(w, l, 0, dev) for l in range(nL)])
+            self.q = torch.stack([synth.make_q(w, l, 0, dev) for l in ids])
             self.out = torch.empty((nL, w.B, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
         else:  # [layer][B][n_q][H_q][D]
             self.q = torch.stack([torch.stack([synth.make_q(w, l, s, dev) for s in range(n_q)], 1)
-                                  for l in range(nL)])
+                                  for l in ids])
             self.out = torch.empty((nL, w.B, n_q, w.H_q, w.D), dtype=torch.bfloat16, device=dev)
         # the step's own K/V rows, [layer][B][H_kv][n_q][D]
         self.ks = torch.stack([torch.cat([synth.make_step_kv(w, l, "k", s, dev) for s in range(n_q)], 2)
-                               for l in range(nL)])
+                               for l in ids])
         self.vs = torch.stack([torch.cat([synth.make_step_kv(w, l, "v", s, dev) for s in range(n_q)], 2)
-                               for l in range(nL)])
+                               for l in ids])
         self.scale = 1.0 / math.sqrt(w.D)
         torch.cuda.synchronize()
 
@@ -306,6 +336,86 @@ class Model:
         if self.prefill_in_step:
             b += sum(prefill_bytes(ly["L"], self.T_hist) for ly in self.layers)
         return b
+
+
+def time_decode_layers(model: "Model", flush, reps: int = 20) -> dict:
+    """Per-launch device time of the model's layer decodes: a CUDA graph of
+    every layer's decode back to back (as inside a step), L2 flushed before
+    each replay, CUDA events on the launching stream; per launch = replay
+    time / layers.  Returns median / p10 / p90 in microseconds."""
+    n = len(model.layers)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l in range(n):
+            model.decode_layer(l)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        flush()
+        g.replay()
+    ev = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    us = np.array([a.elapsed_time(b) * 1e3 / n for a, b in ev])
+    return {"median": float(np.median(us)), "p10": float(np.percentile(us, 10)),
+            "p90": float(np.percentile(us, 90))}
+
+
+def time_prefill_layers(model: "Model", flush, reps: int = 3) -> float:
+    """Mean device time (us) of one layer's quantise-append of its bf16
+    history, L2 flushed before each launch."""
+    ev = []
+    for _ in range(reps):
+        for l in range(len(model.layers)):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            model.prefill_layer(l)
+            b.record()
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) * 1e3 for a, b in ev]))
+
+
+def run_sweep(dev, flush, peak: float) -> list:
+    """The other workloads of the pages, one entry each: the per-launch
+    decode time (fused step per layer) of the listed layers with its
+    algorithmic bytes and roofline fraction, and for LLaVA-Next the
+    quantise-append of the bf16 history."""
+    rows = []
+    for name, T, ids in SWEEP:
+        w = synth.workload(name, T)
+        prefill = name == "llava_next_13b"
+        model = Model(w, dev, w.n_layers, prefill_in_step=prefill, layer_ids=ids)
+        model.step()  # eager warm-up
+        torch.cuda.synchronize()
+        t = time_decode_layers(model, flush)
+        layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T) + append_bytes(ly["L"], 1)
+                                     for ly in model.layers]))
+        gbs = layer_bytes / (t["median"] * 1e-6) / 1e9
+        row = {"workload": w.name, "layers": model.layer_ids, "T": model.T,
+               "kernel": "kvq_decode_step (one launch per layer)",
+               "per_launch_us": round(t["median"], 3), "p10_us": round(t["p10"], 3),
+               "p90_us": round(t["p90"], 3), "per_launch_bytes": int(layer_bytes),
+               "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4)}
+        rows.append(row)
+        if prefill:
+            ap_us = time_prefill_layers(model, flush)
+            ap_bytes = float(np.mean([prefill_bytes(ly["L"], model.T_hist) for ly in model.layers]))
+            ap_gbs = ap_bytes / (ap_us * 1e-6) / 1e9
+            rows.append({"workload": w.name, "layers": model.layer_ids, "T": model.T_hist,
+                         "kernel": "append_kernel (kvq_quantize_append of the bf16 history)",
+                         "per_launch_us": round(ap_us, 2), "per_launch_bytes": int(ap_bytes),
+                         "achieved": round(ap_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(ap_gbs / peak, 4)})
+        del model
+        torch.cuda.empty_cache()
+    return rows
 
 
 def run_ours(args, rank, world, local):
@@ -350,7 +460,8 @@ def run_ours(args, rank, world, local):
     barrier(world, True)
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
-    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    dev_ms = float(step_ms.sum())
     dev_ms = max_over_ranks(dev_ms, world, True)
     step_bytes = model.step_bytes()
     total_bytes = sum_over_ranks(float(step_bytes) * args.steps, world, True)
@@ -361,22 +472,8 @@ def run_ours(args, rank, world, local):
     # split + combine), timed with events on the launching stream around a
     # CUDA graph of every layer's decode (back-to-back, as in the step), L2
     # flushed before each replay; per launch = replay time / layers
-    rl_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(rl_graph):
-        for l in range(n_layers):
-            model.decode_layer(l)
-    torch.cuda.synchronize()
-    reps = 20
-    rl_ev = []
-    for r in range(reps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        rl_graph.replay()
-        b.record()
-        rl_ev.append((a, b))
-    torch.cuda.synchronize()
-    launch_ms = float(np.median([a.elapsed_time(b) for a, b in rl_ev])) / n_layers
+    rl = time_decode_layers(model, flush)
+    launch_ms = rl["median"] * 1e-3
     layer_bytes = float(np.mean([decode_bytes(ly["L"], model.T, model.n_q) + append_bytes(ly["L"], model.n_q)
                                  for ly in model.layers]))
     peaks = {}
@@ -390,21 +487,11 @@ def run_ours(args, rank, world, local):
 
     append_line = None
     if prefill:
-        ap_ev = []
-        for r in range(3):
-            for l in range(n_layers):
-                flush()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                model.prefill_layer(l)
-                b.record()
-                ap_ev.append((a, b))
-        torch.cuda.synchronize()
-        ap_ms = float(np.mean([a.elapsed_time(b) for a, b in ap_ev]))
+        ap_us = time_prefill_layers(model, flush)
         ap_bytes = float(np.mean([prefill_bytes(ly["L"], model.T_hist) for ly in model.layers]))
-        ap_gbs = ap_bytes / (ap_ms * 1e-3) / 1e9
+        ap_gbs = ap_bytes / (ap_us * 1e-6) / 1e9
         append_line = {"kernel": "append_kernel (kvq_quantize_append of the bf16 history)",
-                       "per_launch_us": round(ap_ms * 1e3, 2), "per_launch_bytes": int(ap_bytes),
+                       "per_launch_us": round(ap_us, 2), "per_launch_bytes": int(ap_bytes),
                        "achieved": round(ap_gbs, 1), "peak": peak, "unit": "GB/s",
                        "frac": round(ap_gbs / peak, 4)}
 
@@ -434,6 +521,14 @@ def run_ours(args, rank, world, local):
     d2h = h_out.numel() * 2
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
 
+    m_T, m_nq, m_fused = model.T, model.n_q, model.fused
+    sweep = None
+    if world == 1 and not args.no_sweep and args.workload == "llava_ov_7b" and args.layers is None \
+            and args.n_q == 1 and args.fused == "yes":
+        del graph, model
+        torch.cuda.empty_cache()
+        sweep = run_sweep(dev, flush, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, n_layers=min(4, n_layers))
@@ -441,25 +536,32 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "us_per_step": round(ms_per_step * 1e3, 2), "higher_is_better": True,
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "step_us_median_p10_p90": [round(float(np.median(step_ms)) * 1e3, 2),
+                                   round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                                   round(float(np.percentile(step_ms, 90)) * 1e3, 2)],
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8/u4/u2 codes + bf16; fp32 accumulate",
         "data": "synthetic (seeded; shapes of the pages' LLaVA-OneVision-7B video workload)",
         "config": {"workload": f"{w.name}: {n_layers} layers, B={w.B}, H_q={w.H_q}, "
-                               f"H_kv={w.H_kv}, D={w.D}, T={model.T} (history {w.T} + current), "
+                               f"H_kv={w.H_kv}, D={w.D}, T={m_T} (history {w.T} + current), "
                                f"K{w.layers[0].k_bits}/V{w.layers[0].v_bits} G{w.group_size}, "
                                f"protected {w.layers[0].protected}",
                    "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
                    "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
-                   "query_tokens": model.n_q},
+                   "query_tokens": m_nq},
         "roofline": {"bound": "hbm",
-                     "traffic": NCU_TRAFFIC.get((w.name, n_layers, model.fused)) if model.n_q == 1 else None,
-                     "kernel": ("split_mma_kernel<..., step> (kvq_decode_step, one launch)" if model.fused
+                     "traffic": (NCU_TRAFFIC.get(kernel_source_hash(), {}).get((w.name, n_layers, m_fused))
+                                 if m_nq == 1 else None),
+                     "kernel_source_hash": kernel_source_hash(),
+                     "kernel": ("split_mma_kernel<..., step> (kvq_decode_step, one launch)" if m_fused
                                 else ("kvq_quantize_append + kvq_decode_attention_mq (3 launches)"
-                                      if model.n_q > 1 else
+                                      if m_nq > 1 else
                                       "kvq_quantize_append + kvq_decode_attention (3 launches)")),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "per_launch_bytes": int(layer_bytes), "per_launch_us": round(launch_ms * 1e3, 3),
+                     "per_launch_us_p10_p90": [round(rl["p10"], 3), round(rl["p90"], 3)],
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if peaks else
                                     "fallback 6800 GB/s"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -471,6 +573,8 @@ def run_ours(args, rank, world, local):
     if append_line is not None:
         line["append"] = append_line
         line["config"]["step"] = "per layer: quantise-append of the bf16 history + current token, decode"
+    if sweep is not None:
+        line["sweep"] = sweep
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:

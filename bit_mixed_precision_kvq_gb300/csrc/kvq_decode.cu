@@ -238,18 +238,21 @@ kvq_status launch_step(const kvq_layout* L, kvq::Params* p, void* stream) {
   return KVQ_OK;
 }
 
-// One parameter block for every decode entry point: it is large (the cut
-// table), so it stays off the host stack, and calls are serialised on it.
-std::mutex g_call_mu;
-kvq::Params g_params;
+// The parameter block of a call is built on the calling host thread and
+// copied into the launch; it is large (the cut table), so it lives in
+// thread-local storage rather than on the stack.  Calls from different host
+// threads therefore neither share nor wait for one another.
+kvq::Params* call_params() {
+  thread_local kvq::Params p;
+  return &p;
+}
 
 }  // namespace
 
 extern "C" kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const void* q_bf16,
                                            int32_t T, float softmax_scale, void* out_bf16, float* lse,
                                            void* workspace, size_t ws_bytes, void* stream) {
-  std::lock_guard<std::mutex> lock(g_call_mu);
-  kvq::Params* p = &g_params;
+  kvq::Params* p = call_params();
   const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p);
   if (st != KVQ_OK) return st;
@@ -261,9 +264,8 @@ extern "C" kvq_status kvq_decode_attention_ragged(const kvq_layout* L, const voi
                                                   int32_t T_max, float softmax_scale, void* out_bf16,
                                                   float* lse, void* workspace, size_t ws_bytes,
                                                   void* stream) {
-  std::lock_guard<std::mutex> lock(g_call_mu);
   if (!seq_len || reinterpret_cast<uintptr_t>(seq_len) % 4) return KVQ_ERR_INVALID_ARG;
-  kvq::Params* p = &g_params;
+  kvq::Params* p = call_params();
   const kvq_status st = decode_params(L, cache, q_bf16, T_max, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p);
   if (st != KVQ_OK) return st;
@@ -279,13 +281,12 @@ extern "C" size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q
 extern "C" kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* cache, const void* q_bf16,
                                               int32_t n_q, int32_t T, float softmax_scale, void* out_bf16,
                                               float* lse, void* workspace, size_t ws_bytes, void* stream) {
-  std::lock_guard<std::mutex> lock(g_call_mu);
   if (!L) return KVQ_ERR_INVALID_ARG;
   if (n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS || T < n_q) return KVQ_ERR_INVALID_ARG;
   // the positions some tokens do not attend, [T - n_q + 1, T), must be text
   if (n_q > 1 && L->d.vis_start < L->d.vis_end && T - n_q + 1 < L->d.vis_end && T > L->d.vis_start)
     return KVQ_ERR_INVALID_ARG;
-  kvq::Params* p = &g_params;
+  kvq::Params* p = call_params();
   const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p, n_q);
   if (st != KVQ_OK) return st;
@@ -296,12 +297,11 @@ extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const vo
                                       const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,
                                       float softmax_scale, void* out_bf16, float* lse, void* workspace,
                                       size_t ws_bytes, void* stream) {
-  std::lock_guard<std::mutex> lock(g_call_mu);
   kvq_status st = step_rows_ok(L, k_new_bf16, v_new_bf16);
   if (st != KVQ_OK) return st;
   if (t_new < 0 || t_new >= L->d.T_cap) return KVQ_ERR_INVALID_ARG;
   if (t_new >= L->d.vis_start && t_new < L->d.vis_end) return KVQ_ERR_INVALID_ARG;
-  kvq::Params* p = &g_params;
+  kvq::Params* p = call_params();
   st = decode_params(L, cache, q_bf16, t_new + 1, softmax_scale, out_bf16, lse, workspace, ws_bytes, p);
   if (st != KVQ_OK) return st;
   p->k_new = static_cast<const uint16_t*>(k_new_bf16);
@@ -315,11 +315,10 @@ extern "C" kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, c
                                              const int32_t* t_new, int32_t T_max, float softmax_scale,
                                              void* out_bf16, float* lse, void* workspace, size_t ws_bytes,
                                              void* stream) {
-  std::lock_guard<std::mutex> lock(g_call_mu);
   kvq_status st = step_rows_ok(L, k_new_bf16, v_new_bf16);
   if (st != KVQ_OK) return st;
   if (!t_new || reinterpret_cast<uintptr_t>(t_new) % 4) return KVQ_ERR_INVALID_ARG;
-  kvq::Params* p = &g_params;
+  kvq::Params* p = call_params();
   st = decode_params(L, cache, q_bf16, T_max, softmax_scale, out_bf16, lse, workspace, ws_bytes, p);
   if (st != KVQ_OK) return st;
   p->k_new = static_cast<const uint16_t*>(k_new_bf16);
