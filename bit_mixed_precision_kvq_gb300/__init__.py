@@ -22,7 +22,8 @@ __all__ = [
     "decode_step_ragged", "kvq_decode_step_ragged", "sensitivity_probe", "kvq_sensitivity_probe",
     "probe_workspace_bytes", "kvq_probe_workspace_bytes", "decode_attention_mq",
     "kvq_decode_attention_mq", "decode_mq_workspace_bytes", "kvq_decode_mq_workspace_bytes",
-    "KVQ_MAX_QUERY_TOKENS",
+    "KVQ_MAX_QUERY_TOKENS", "workspace_status", "kvq_workspace_status", "set_wait_limits",
+    "kvq_set_wait_limits", "STATUS_TILE_WAIT", "STATUS_PEER_WAIT", "STATUS_COUNTER",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
@@ -38,7 +39,9 @@ EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_atten
                     "kvq_decode_step", "kvq_decode_attention_ragged", "kvq_decode_step_ragged",
                     "kvq_sensitivity_probe", "kvq_probe_workspace_bytes", "kvq_decode_attention_mq",
                     "kvq_decode_mq_workspace_bytes",
-                    "kvq_decode_attention_static_ws", "kvq_last_cuda_error", "kvq_status_string"]
+                    "kvq_decode_attention_static_ws", "kvq_workspace_status", "kvq_set_wait_limits",
+                    "kvq_last_cuda_error", "kvq_status_string"]
+STATUS_TILE_WAIT, STATUS_PEER_WAIT, STATUS_COUNTER = 1, 2, 4  # KVQ_STATUS_* bits
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -121,6 +124,10 @@ def load() -> ctypes.CDLL:
     lib.kvq_sensitivity_probe.restype = ctypes.c_int
     lib.kvq_decode_attention_static_ws.argtypes = [ctypes.POINTER(Layout), P, P, i32, f32, P, P, P]
     lib.kvq_decode_attention_static_ws.restype = ctypes.c_int
+    lib.kvq_workspace_status.argtypes = [P, P, P]
+    lib.kvq_workspace_status.restype = ctypes.c_int
+    lib.kvq_set_wait_limits.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    lib.kvq_set_wait_limits.restype = None
     lib.kvq_last_cuda_error.argtypes = []
     lib.kvq_last_cuda_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -325,6 +332,28 @@ def decode_attention_static_ws(L: Layout, cache, q, T: int, out,
         raise KvqError(st, "kvq_decode_attention_static_ws")
 
 
+def workspace_status(workspace, stream=None) -> int:
+    """kvq_workspace_status: the KVQ_STATUS_* bits OR-ed into the
+    workspace's status word (synchronises the stream to read them)."""
+    import torch
+    host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    st = load().kvq_workspace_status(_addr(workspace), _addr(host), _stream(stream))
+    if st != 0:
+        raise KvqError(st, "kvq_workspace_status")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    if isinstance(s, int):
+        torch.cuda.synchronize()
+    else:
+        s.synchronize()
+    return int(host.item()) & 0xFFFFFFFF
+
+
+def set_wait_limits(tile_polls: int = 0, peer_polls: int = 0) -> None:
+    """kvq_set_wait_limits: bounded-wait limits of later decode calls from
+    this host thread (0 = default)."""
+    load().kvq_set_wait_limits(int(tile_polls), int(peer_polls))
+
+
 # Same names as the C entry points.
 kvq_cache_layout = cache_layout
 kvq_quantize_append = quantize_append
@@ -337,3 +366,5 @@ kvq_sensitivity_probe = sensitivity_probe
 kvq_decode_attention_mq = decode_attention_mq
 kvq_decode_mq_workspace_bytes = decode_mq_workspace_bytes
 kvq_probe_workspace_bytes = probe_workspace_bytes
+kvq_workspace_status = workspace_status
+kvq_set_wait_limits = set_wait_limits

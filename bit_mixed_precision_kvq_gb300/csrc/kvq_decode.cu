@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "kvq_device.cuh"
@@ -100,15 +101,24 @@ const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool 
   return nullptr;
 }
 
-// One-time per kernel: >48 KB dynamic shared memory, and a check that the
-// 12-warp block fits (per-partition register budget).
-kvq_status prepare_split(const void* fn, size_t smem) {
+// One-time per kernel: >48 KB dynamic shared memory, clusters of 16 CTAs
+// allowed, a check that the 12-warp block fits (per-partition register
+// budget), and how many 16-CTA clusters of it the GPU holds at once.
+constexpr int kClusterCtas = kvq::kMaxClusterCtas;
+struct SplitInfo {
+  const void* fn;
+  int max_clusters;  // 16-CTA clusters resident at once (0: cluster launches unavailable)
+};
+kvq_status prepare_split(const void* fn, size_t smem, int* max_clusters) {
   static std::mutex mu;
-  static const void* done[512];
+  static SplitInfo done[512];
   static int n_done = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_done; ++i)
-    if (done[i] == fn) return KVQ_OK;
+    if (done[i].fn == fn) {
+      *max_clusters = done[i].max_clusters;
+      return KVQ_OK;
+    }
   const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
   if (e != cudaSuccess) return kvq_cuda_fail(e);
@@ -116,9 +126,45 @@ kvq_status prepare_split(const void* fn, size_t smem) {
   const cudaError_t e2 = cudaFuncGetAttributes(&fa, fn);
   if (e2 != cudaSuccess) return kvq_cuda_fail(e2);
   if (fa.maxThreadsPerBlock < kvq::kSplitThreads) return kvq_cuda_fail(cudaErrorLaunchOutOfResources);
-  if (n_done < 512) done[n_done++] = fn;
+  int ncl = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas);
+    cfg.blockDim = dim3(kvq::kSplitThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = kClusterCtas;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg) != cudaSuccess) ncl = 0;
+  }
+  (void)cudaGetLastError();  // a refused cluster query only disables cluster mode
+  if (n_done < 512) done[n_done++] = SplitInfo{fn, ncl};
+  *max_clusters = ncl;
   return KVQ_OK;
 }
+
+// Cluster mode pays when every unit fits one resident 16-CTA cluster and a
+// sixteenth of the largest unit is still a small piece of work (at most
+// kClusterMaxCtaCost cost units, about that many bytes): then the cluster's
+// merge through distributed shared memory replaces the workspace partials,
+// the counters and the combine.  Larger units stream faster over every SM
+// (global mode).
+constexpr int64_t kClusterMaxCtaCost = 512 * 1024;
+bool use_cluster_mode(const kvq::Plan& P, int max_clusters) {
+  if (P.U > max_clusters || static_cast<int64_t>(P.U) * kClusterCtas > KVQ_MAX_CTAS) return false;
+  int64_t biggest = P.U_p ? P.ub_p : 0;
+  if (P.U_k) biggest = std::max(biggest, P.ub_k);
+  if (P.U - P.U_p - P.U_k) biggest = std::max(biggest, P.ub_u);
+  return biggest / kClusterCtas <= kClusterMaxCtaCost;
+}
+
+// Wait limits of the calling host thread (kvq_set_wait_limits); 0 = default.
+thread_local uint32_t tl_tile_polls = 0;
+thread_local uint32_t tl_peer_polls = 0;
 
 // Units of a decode call with n_q query tokens per sequence.
 int64_t decode_units(const kvq_layout* L, int32_t n_q) {
@@ -152,9 +198,12 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   p->lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t cnt_bytes = kvq::ws_counter_bytes(units);
-  p->cnt = reinterpret_cast<uint32_t*>(ws);
-  p->ws_o = reinterpret_cast<float*>(ws + cnt_bytes);
-  p->ws_ml = reinterpret_cast<float*>(ws + cnt_bytes + kvq::ws_o_bytes(units));
+  p->status = reinterpret_cast<uint32_t*>(ws);
+  p->cnt = reinterpret_cast<uint32_t*>(ws + kvq::kWsHeadBytes);
+  p->ws_o = reinterpret_cast<float*>(ws + kvq::kWsHeadBytes + cnt_bytes);
+  p->ws_ml = reinterpret_cast<float*>(ws + kvq::kWsHeadBytes + cnt_bytes + kvq::ws_o_bytes(units));
+  p->tile_polls = tl_tile_polls ? tl_tile_polls : kvq::kDefaultTilePolls;
+  p->peer_polls = tl_peer_polls ? tl_peer_polls : kvq::kDefaultPeerPolls;
   p->scale_log2 = softmax_scale * 1.4426950408889634f;
   p->seq_len = nullptr;  // uniform call; the ragged entry points set it
   p->n_q = n_q;
@@ -173,15 +222,80 @@ constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
 static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
 
 
-// The split kernel and the combine of one decode call (p prepared).
-kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
-  const void* split = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, false, p->pk_halves,
-                                       L->n_konly > 0 || p->n_q > 1);
-  if (!split) return KVQ_ERR_UNSUPPORTED;
-  kvq_status st = prepare_split(split, kSplitSmemBytes);
+// Launch the split kernel: one CTA per chunk, programmatic serialisation
+// allowed (the kernel waits with griddepcontrol.wait before touching
+// memory), in clusters of plan.cs CTAs in cluster mode, cooperative when
+// requested (the global-mode fused step, whose combining CTAs may wait for
+// other CTAs of their unit).  Programmatic serialisation is dropped if the
+// runtime refuses it.
+kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool cooperative) {
+  static std::atomic<int> pdl_ok{1};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p->plan.C);
+  cfg.blockDim = dim3(kvq::kSplitThreads);
+  cfg.dynamicSmemBytes = kSplitSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[3];
+  int na = 0;
+  if (p->plan.cs > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p->plan.cs;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  } else if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  void* args[1] = {p};
+  cudaError_t e = cudaErrorUnknown;
+  if (pdl_ok.load()) {
+    cfg.numAttrs = na + 1;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      pdl_ok.store(0);
+    }
+  }
+  if (!pdl_ok.load()) {
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  if (e != cudaSuccess) return kvq_cuda_fail(e);
+  return KVQ_OK;
+}
+
+// Pick the split kernel of a call (p prepared in global mode), switching the
+// plan to cluster mode where that pays; *fn gets the kernel.
+kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const void** fn) {
+  const bool general = L->n_konly > 0 || p->n_q > 1;
+  *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general);
+  if (!*fn) return KVQ_ERR_UNSUPPORTED;
+  int max_clusters = 0;
+  kvq_status st = prepare_split(*fn, kSplitSmemBytes, &max_clusters);
   if (st != KVQ_OK) return st;
-  if (kvq_launch_pdl(split, p->plan.C, kvq::kSplitThreads, kSplitSmemBytes, stream, p) != 0)
-    return KVQ_ERR_CUDA;
+  if (!use_cluster_mode(p->plan, max_clusters)) return KVQ_OK;
+  p->plan.cs = kClusterCtas;
+  kvq_plan_cuts(&p->plan, p->cuts);
+  p->pk_halves = packed_halves(p->plan, L, p->n_q);
+  packed_tile_geometry(p);
+  *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general);
+  if (!*fn) return KVQ_ERR_UNSUPPORTED;
+  return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
+}
+
+// The split kernel and, in global mode, the combine of one decode call (p
+// prepared).  In cluster mode the split kernel writes the outputs itself.
+kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
+  const void* split = nullptr;
+  kvq_status st = choose_split(L, p, false, &split);
+  if (st != KVQ_OK) return st;
+  st = launch_split(split, p, stream, false);
+  if (st != KVQ_OK || p->plan.cs > 1) return st;
   const bool wide = kvq::plan_max_unit_chunks(p->plan, p->cuts) > 16;
   const void* comb = wide ? reinterpret_cast<const void*>(&kvq::combine_kernel<16>)
                           : reinterpret_cast<const void*>(&kvq::combine_kernel<2>);
@@ -198,44 +312,15 @@ kvq_status step_rows_ok(const kvq_layout* L, const void* k_new_bf16, const void*
   return KVQ_OK;
 }
 
-// The fused step's single launch (p prepared).  Cooperative: a combining CTA
-// may wait for other CTAs of its unit, so all CTAs must be resident together
-// (one per SM, C <= SM count).  Programmatic serialisation is added while
-// the runtime accepts both.
+// The fused step's single launch (p prepared).  Global mode is cooperative:
+// a combining CTA may wait for other CTAs of its unit, so all CTAs must be
+// resident together (one per SM, C <= SM count).  Cluster mode merges inside
+// each unit's cluster and never waits on another cluster.
 kvq_status launch_step(const kvq_layout* L, kvq::Params* p, void* stream) {
-  const void* fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, true, p->pk_halves,
-                                    L->n_konly > 0);  // the fused step is single-query
-  if (!fn) return KVQ_ERR_UNSUPPORTED;
-  const kvq_status st = prepare_split(fn, kSplitSmemBytes);
+  const void* fn = nullptr;
+  const kvq_status st = choose_split(L, p, true, &fn);  // the fused step is single-query
   if (st != KVQ_OK) return st;
-  static int pdl_ok = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p->plan.C);
-  cfg.blockDim = dim3(kvq::kSplitThreads);
-  cfg.dynamicSmemBytes = kSplitSmemBytes;
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  void* args[1] = {p};
-  cudaError_t e = cudaErrorUnknown;
-  if (pdl_ok) {
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();
-      pdl_ok = 0;
-    }
-  }
-  if (!pdl_ok) {
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-  }
-  if (e != cudaSuccess) return kvq_cuda_fail(e);
-  return KVQ_OK;
+  return launch_split(fn, p, stream, true);
 }
 
 // The parameter block of a call is built on the calling host thread and
@@ -326,4 +411,17 @@ extern "C" kvq_status kvq_decode_step_ragged(const kvq_layout* L, void* cache, c
   p->t_new = T_max - 1;  // the largest step position a sequence may have
   p->seq_len = t_new;
   return launch_step(L, p, stream);
+}
+
+extern "C" void kvq_set_wait_limits(uint32_t tile_polls, uint32_t peer_polls) {
+  tl_tile_polls = tile_polls;
+  tl_peer_polls = peer_polls;
+}
+
+extern "C" kvq_status kvq_workspace_status(const void* workspace, uint32_t* status, void* stream) {
+  if (!workspace || !status || reinterpret_cast<uintptr_t>(workspace) % 4) return KVQ_ERR_INVALID_ARG;
+  const cudaError_t e = cudaMemcpyAsync(status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return kvq_cuda_fail(e);
+  return KVQ_OK;
 }

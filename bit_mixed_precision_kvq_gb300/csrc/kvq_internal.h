@@ -22,9 +22,14 @@
 //   * CTA c writes one partial result (o, m, l) per unit it touches into
 //     workspace slot u + c.  The (u, c) pairs form a monotone staircase, so
 //     u + c is unique; there are at most units + C - 1 slots.
-//   * the fused decode step combines a unit's partials in the CTA that
-//     finishes the unit's last chunk (per-unit arrival counters at the start
-//     of the workspace).
+//   * the fused decode step combines a unit's partials in the CTAs that
+//     finish the unit's last chunks (per-unit arrival counters in the
+//     workspace).
+//   * cluster mode (plan.cs > 1, when every unit fits one thread-block
+//     cluster of the GPU at once): unit u is cut into exactly cs chunks,
+//     processed by the cs CTAs of cluster u, which merge their partials
+//     through distributed shared memory -- no workspace partials, no
+//     counters, no inter-CTA waiting -- and write the outputs directly.
 #pragma once
 
 #include <stdint.h>
@@ -89,6 +94,7 @@ struct Plan {
   int32_t w_kvis;     // cost of one K-only visual position
   int64_t ub_k;       // cost of a K-only unit
   int64_t K_bytes;    // U_k * ub_k
+  int32_t cs;         // cluster mode: CTAs per cluster (= chunks per unit); 1 otherwise
 };
 
 struct Cut {
@@ -174,18 +180,27 @@ inline int32_t plan_max_unit_chunks(const Plan& P, const Cut* cuts) {
   return best;
 }
 
-// Decode workspace: the per-unit arrival counters of the fused step, then one
-// partial (o[kNH][kD] fp32, then (m, l)[kNH] fp32 in a second array) per
-// slot, slots <= units + C - 1 <= units + KVQ_MAX_CTAS - 1; each part
-// 256-byte aligned.
+// Decode workspace: a 256-byte head whose first word is the status word
+// (KVQ_STATUS_* bits, OR-ed by the kernels, never cleared by them), the
+// per-unit arrival counters of the fused step, then one partial
+// (o[kNH][kD] fp32, then (m, l)[kNH] fp32 in a second array) per slot,
+// slots <= units + C - 1 <= units + KVQ_MAX_CTAS - 1; each part 256-byte
+// aligned.
+constexpr int64_t kWsHeadBytes = 256;
 KVQ_HD int64_t ws_counter_bytes(int64_t units) { return (4 * units + 255) / 256 * 256; }
 KVQ_HD int64_t ws_o_bytes(int64_t units) {
   return ((units + KVQ_MAX_CTAS - 1) * kNH * kD * 4 + 255) / 256 * 256;
 }
 KVQ_HD int64_t ws_ml_bytes(int64_t units) { return ((units + KVQ_MAX_CTAS - 1) * kNH * 8 + 255) / 256 * 256; }
 KVQ_HD int64_t ws_total_bytes(int64_t units) {
-  return ws_counter_bytes(units) + ws_o_bytes(units) + ws_ml_bytes(units);
+  return kWsHeadBytes + ws_counter_bytes(units) + ws_o_bytes(units) + ws_ml_bytes(units);
 }
+
+// Bounded waits: polls of an mbarrier try_wait (each suspends the thread for
+// a hardware-chosen interval) and of the fused step's inter-CTA counter
+// (each followed by a short sleep) before a wait gives up.
+constexpr uint32_t kDefaultTilePolls = 1u << 24;
+constexpr uint32_t kDefaultPeerPolls = 1u << 21;
 
 // Everything a kernel needs about one layer and one call (passed by value).
 struct Params {
@@ -213,6 +228,9 @@ struct Params {
   const uint16_t* v_new;
   int32_t t_new;          // uniform fused step: its position (= T - 1); the kernels use each unit's end
   uint32_t* cnt;          // per-unit arrival counters (zero between calls)
+  uint32_t* status;       // workspace status word (KVQ_STATUS_* bits)
+  uint32_t tile_polls;    // bounded mbarrier waits on staged tiles
+  uint32_t peer_polls;    // bounded wait of the fused step's combining CTAs
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
   Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host

@@ -188,12 +188,29 @@ kvq::Plan kvq_make_plan(const kvq_layout* L, int32_t T, int32_t n_chunks_target,
   if (C > KVQ_MAX_CTAS) C = KVQ_MAX_CTAS;
   if (C < 1) C = 1;
   P.C = static_cast<int32_t>(C);
+  P.cs = 1;
   return P;
 }
 
 void kvq_plan_cuts(kvq::Plan* Pp, kvq::Cut* cuts) {
   using kvq::Cut;
   kvq::Plan& P = *Pp;
+  if (P.cs > 1) {
+    // Cluster mode: unit u is cut into exactly cs chunks of equal cost,
+    // chunks u * cs .. u * cs + cs - 1 (the CTAs of cluster u).
+    P.C = P.U * P.cs;
+    P.aligned = 1;
+    P.n_p = P.n_k = P.n_q = P.cs;
+    P.R = 0;
+    int32_t c = 0;
+    for (int32_t u = 0; u < P.U; ++u) {
+      const int cls = kvq::unit_class(P, u);
+      const int64_t ucost = cls == kvq::kClsProt ? P.ub_p : (cls == kvq::kClsKonly ? P.ub_k : P.ub_u);
+      for (int32_t k = 0; k < P.cs; ++k) cuts[c++] = Cut{u, kvq::unit_cut_pos(P, cls, ucost * k / P.cs)};
+    }
+    cuts[P.C] = Cut{P.U, 0};
+    return;
+  }
   cuts[P.C] = Cut{P.U, 0};
   P.aligned = P.C >= P.U ? 1 : 0;
   P.n_p = P.n_k = P.n_q = P.R = 0;

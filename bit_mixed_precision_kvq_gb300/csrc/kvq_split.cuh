@@ -46,21 +46,34 @@ constexpr int kStages = 5;
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
 constexpr uint32_t kPrefetchBytes = kStageBytes;  // L2 prefetch before the dependency wait
-constexpr uint32_t kWaitPolls = 1u << 24;      // bounded mbarrier waits
-constexpr uint32_t kSpinPolls = 1u << 21;      // bounded inter-CTA wait (fused step)
 constexpr int kNoLimit = 1 << 30;              // kblock: no multi-query column limit
+constexpr int kMaxClusterCtas = 16;            // cluster mode: CTAs per cluster (at most)
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
   float merge_o[kConsumerWarps][kNH][kD + 4];  // padded rows: fewer bank conflicts
   float merge_ml[kConsumerWarps][kNH][2];
+  float merge_sc[kConsumerWarps][kNH];         // exp2(m_warp - M) per (warp, column)
+  float merge_ML[kNH][2];                      // the CTA's (M, L) per column
   float qsum[kConsumerWarps][kNH][4];
+  // cluster mode: the CTA's merged partial, read by the cluster's other CTAs
+  float cl_o[kNH][kD];
+  alignas(16) float cl_ml[kNH][2];
+  float cl_w[kMaxClusterCtas];                 // the combining CTA's weights per cluster rank
+  float cl_ML[2];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort;
   int role;   // fused step: combine role of this CTA for the current unit
   int ncomb;  // fused step: CTAs combining the current unit
 };
+
+// A bounded wait gave up (or a counter was found corrupt): mark the call's
+// status word and this CTA's outputs.
+__device__ __forceinline__ void report_failure(const Params& p, SplitSmem& sm, uint32_t bit) {
+  sm.abort = 1;
+  if (p.status) atomicOr(p.status, bit);
+}
 
 // Tile kinds: bf16 text rows, bf16 protected visual rows, packed visual
 // rows, K-only visual rows (bf16 K + packed V).
@@ -190,7 +203,27 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
 // copies into shared memory all come after the wait.
 template <bool kGen>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
-  uint32_t budget = kPrefetchBytes;
+  // The query rows of the chunk's units first: the consumers need them before
+  // any tile (single-query units read nh consecutive rows of D bf16).
+  {
+    const Cut a = p.cuts[c];
+    const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
+    for (int u = a.u; u <= u_last; ++u) {
+      const UnitInfo ui = unit_info<kGen>(p, u);
+      const int c0 = ui.hc * kNH;
+      if (kGen && p.n_q > 1) {
+        const int nh = min(kNH, p.g * p.n_q - c0);
+        for (int j = 0; j < nh; ++j) prefetch_l2(p.q + col_row(p, ui.b, ui.h, c0 + j) * kD, 2 * kD);
+      } else {
+        const int nh = min(kNH, p.g - c0);
+        prefetch_l2(p.q + (static_cast<int64_t>(ui.b) * p.Hq + ui.h * p.g + c0) * kD,
+                    static_cast<uint32_t>(nh) * 2 * kD);
+      }
+    }
+  }
+  // Cluster mode launches fewer CTAs than SMs, so the next layer's CTAs find
+  // free SMs early and have time to prefetch their whole chunk.
+  uint32_t budget = p.plan.cs > 1 ? 0xffffffffu : kPrefetchBytes;
   walk_chunk<kGen, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     if (budget == 0) return;
     tile_sources<false, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
@@ -207,7 +240,8 @@ __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, in
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     const int st = it % kStages;
     const uint32_t round = it / kStages;
-    if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, kWaitPolls)) sm.abort = 1;
+    if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
+      report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
     uint8_t* dst = sm.stage[st];
     uint32_t total = 0;
     tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
@@ -873,8 +907,8 @@ __device__ __forceinline__ void combine_row(const Params& p, int u, int j, int c
 
 // Fused step: wait (bounded) until the unit's last arrival has reset its
 // counter to zero.
-__device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt) {
-  for (uint32_t i = 0; i < kSpinPolls; ++i) {
+__device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (ld_acquire_gpu(cnt) == 0u) return true;
     __nanosleep(32);
   }
@@ -974,7 +1008,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     auto begin_tile = [&](int kind, int t0, int n) -> const uint8_t* {
       const int st = it % kStages;
       const uint32_t round = it / kStages;
-      if (!mbar_wait(&sm.full[st], round & 1, kWaitPolls)) sm.abort = 1;
+      if (!mbar_wait(&sm.full[st], round & 1, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
       const uint8_t* base = sm.stage[st];
       if (kStep && kind == kTileText && t0 + n == Tu && ui.hc == 0 && warp == 0) {
         // lanes 0-15 the K row, lanes 16-31 the V row (position Tu - 1)
@@ -1089,28 +1123,46 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     if (ui.prot) store_rows(16 * gid, 1);
     else store_rows(gid, 16);
     // The fused step finishes a unit held by this CTA alone right here;
-    // otherwise the partial goes to slot u + c.
+    // otherwise the partial goes to slot u + c (global mode) or, in cluster
+    // mode, to this CTA's shared memory for the cluster's combine.
+    const bool cluster = p.plan.cs > 1;
     int cf = c, cl = c;
     if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
-    const bool sole = kStep && cf == cl;
+    const bool sole = kStep && !cluster && cf == cl;
+    named_bar(1, kConsumerWarps * 32);
+    // Per column: the CTA's running max M and sum L, and each warp's weight.
+    if (ctid < kNH) {
+      const int j = ctid;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float m = sm.merge_ml[w][j][0];
+        const float sc = (M == -INFINITY) ? 0.f : exp2f(m - M);
+        sm.merge_sc[w][j] = sc;
+        L = fmaf(sm.merge_ml[w][j][1], sc, L);
+      }
+      if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
+      sm.merge_ML[j][0] = M;
+      sm.merge_ML[j][1] = L;
+    }
     named_bar(1, kConsumerWarps * 32);
     const int64_t slot = static_cast<int64_t>(u) + c;
     for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
       const int j = idx / kD, d = idx - j * kD;
-      float M = -INFINITY;
+      float O = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float sc = exp2f(sm.merge_ml[w][j][0] - M);
-          L = fmaf(sm.merge_ml[w][j][1], sc, L);
-          O = fmaf(sm.merge_o[w][j][d], sc, O);
+      for (int w = 0; w < kConsumerWarps; ++w) O = fmaf(sm.merge_o[w][j][d], sm.merge_sc[w][j], O);
+      const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
+      if (cluster) {
+        sm.cl_o[j][d] = O;
+        if (d == 0) {
+          sm.cl_ml[j][0] = M;
+          sm.cl_ml[j][1] = L;
         }
-      }
-      if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
-      if (sole) {
+      } else if (sole) {
         const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
         const int64_t orow = out_row(j);
         p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
@@ -1123,6 +1175,56 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         }
       }
     }
+    if (cluster) {
+      // Cluster mode: the cs CTAs of this unit's cluster hold one partial
+      // each; CTA rank j combines column j from all of them through
+      // distributed shared memory and writes its output row.  The second
+      // cluster barrier keeps every CTA's shared memory alive until the
+      // reads are done (the producer warp takes part in both barriers).
+      cluster_sync();
+      const int rank = static_cast<int>(cluster_ctarank());
+      if (rank < nh) {
+        const int j = rank;
+        if (warp == 0) {
+          const int cs = p.plan.cs;
+          float2 ml = make_float2(-INFINITY, 0.f);
+          if (lane < cs) ml = ld_dsmem2(dsmem_addr(&sm.cl_ml[j][0], lane));
+          bool bad = ml.x != ml.x;
+          float M = bad ? -INFINITY : ml.x;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          bad = __any_sync(0xffffffffu, bad);
+          const float w = (ml.x == -INFINITY || ml.x != ml.x) ? 0.f : exp2f(ml.x - M);
+          float L = ml.y * w;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+          if (lane < kMaxClusterCtas) sm.cl_w[lane] = w;
+          if (lane == 0) {
+            sm.cl_ML[0] = bad ? __int_as_float(0x7fffffff) : M;
+            sm.cl_ML[1] = L;
+          }
+        }
+        named_bar(1, kConsumerWarps * 32);
+        if (ctid < kD) {
+          const int d = ctid, cs = p.plan.cs;
+          // issue every rank's load before using any (distributed shared
+          // memory round trips overlap); ranks past cs weigh nothing
+          float x[kMaxClusterCtas];
+#pragma unroll
+          for (int r = 0; r < kMaxClusterCtas; ++r) x[r] = r < cs ? ld_dsmem(dsmem_addr(&sm.cl_o[j][d], r)) : 0.f;
+          float O = 0.f;
+#pragma unroll
+          for (int r = 0; r < kMaxClusterCtas; ++r) O = fmaf(x[r], sm.cl_w[r], O);
+          const float M = sm.cl_ML[0], L = sm.cl_ML[1];
+          const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
+          const int64_t orow = out_row(j);
+          p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
+          if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
+        }
+      }
+      cluster_sync();
+      continue;  // one unit per CTA in cluster mode
+    }
     named_bar(1, kConsumerWarps * 32);
     if constexpr (kStep) {
       if (!sole) {
@@ -1130,20 +1232,25 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         // counter (n = its chunks) combine its rows, arrival n - nh + r
         // taking rows r, r + min(n, nh), ...; the very last one resets the
         // counter to zero (for the next call), which also releases the
-        // others, who wait for that.
+        // others, who wait (bounded) for that.  An arrival that finds the
+        // counter at n or more (it was not zero when the call started)
+        // reports it and writes NaN rows.
         if (ctid == 0) {
           __threadfence();
           const uint32_t n = static_cast<uint32_t>(cl - cf + 1);
           const uint32_t nc = min(n, static_cast<uint32_t>(nh));
           const uint32_t k = atomicAdd(&p.cnt[u], 1u);
           int role = -1;
-          if (k == n - 1) {
+          if (k >= n) {
+            report_failure(p, sm, KVQ_STATUS_COUNTER);
+            role = -2;
+          } else if (k == n - 1) {
             __threadfence();
             atomicExch(&p.cnt[u], 0u);
             role = static_cast<int>(nc) - 1;
           } else if (k >= n - nc) {
             role = static_cast<int>(k - (n - nc));
-            if (!wait_unit_released(&p.cnt[u])) sm.abort = 1;
+            if (!wait_unit_released(&p.cnt[u], p.peer_polls)) report_failure(p, sm, KVQ_STATUS_PEER_WAIT);
           }
           __threadfence();
           sm.role = role;
@@ -1151,7 +1258,14 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         }
         named_bar(1, kConsumerWarps * 32);
         const int role = sm.role, nc = sm.ncomb;
-        if (role >= 0) {
+        if (role == -2) {  // corrupt counter: every row of the unit becomes NaN
+          for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
+            const int j = idx / kD, d = idx - j * kD;
+            const int64_t orow = out_row(j);
+            p.out[orow * kD + d] = 0x7fffu;  // bf16 NaN
+            if (d == 0 && p.lse) p.lse[orow] = __int_as_float(0x7fffffff);
+          }
+        } else if (role >= 0) {
           const bool bad = sm.abort != 0;
           float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
           float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
@@ -1188,6 +1302,11 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
       producer_prefetch<kGen>(p, blockIdx.x);
       pdl_wait();  // the previous kernel in the stream may have written the cache
       producer_loop<kStep, kGen>(p, sm, blockIdx.x);
+    }
+    if (p.plan.cs > 1) {  // the consumers' two cluster barriers (cluster mode)
+      __syncwarp();
+      cluster_sync();
+      cluster_sync();
     }
     return;
   }

@@ -70,6 +70,21 @@ extern "C" {
 #define KVQ_HEADS_PER_UNIT 8 /* query columns (query heads, or head x token pairs) handled together per KV head */
 #define KVQ_MAX_QUERY_TOKENS 64 /* query tokens per sequence of kvq_decode_attention_mq */
 
+/* Bits of the status word that the decode kernels OR into the first 4 bytes
+ * of their workspace (never cleared by the library; zero it to start).  A
+ * set bit means that some output rows of a call are NaN (or, for a corrupt
+ * counter found by only some CTAs, unreliable):
+ *   KVQ_STATUS_TILE_WAIT  a staged cache tile did not arrive within the
+ *                         bounded wait (only a fault elsewhere causes it)
+ *   KVQ_STATUS_PEER_WAIT  a combining CTA of kvq_decode_step(_ragged) gave up
+ *                         waiting for the other CTAs of its unit
+ *   KVQ_STATUS_COUNTER    an arrival counter of kvq_decode_step(_ragged) was
+ *                         not zero when the call started (workspace not
+ *                         zeroed, or shared by calls that overlap) */
+#define KVQ_STATUS_TILE_WAIT 1u
+#define KVQ_STATUS_PEER_WAIT 2u
+#define KVQ_STATUS_COUNTER 4u
+
 typedef enum kvq_status {
   KVQ_OK = 0,
   KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer, corrupt layout */
@@ -170,8 +185,11 @@ kvq_status kvq_quantize_append(const kvq_layout* L, void* cache, const void* k_b
  *   lse       device fp32 [B][H_q] (natural-log sum of exp of the scaled
  *             scores) or NULL
  *   workspace device scratch of at least L->workspace_bytes, 256-byte
- *             aligned; contents on entry are ignored; overlapping calls
- *             must not share one workspace
+ *             aligned; its first 4 bytes are the status word (KVQ_STATUS_*
+ *             bits OR-ed in by the kernels, never cleared by the library:
+ *             zero it to use it, read it with kvq_workspace_status); other
+ *             contents on entry are ignored; overlapping calls must not
+ *             share one workspace
  * out[b, hq, :] = sum_p softmax_p(scale * q[b,hq] . khat[b,h,p]) * vhat[b,h,p],
  * h = hq / g, where khat/vhat are the dequantised (or bf16) cache rows.
  * Returns KVQ_ERR_CAPACITY if ws_bytes < L->workspace_bytes.
@@ -189,12 +207,20 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
  * kvq_quantize_append(t0 = t_new, n_tok = 1) followed by
  * kvq_decode_attention(T = t_new + 1), up to the summation order of the
  * cross-split combine.  The append, the split-KV pass and the combine run in
- * one kernel: each (b, KV head, query-head chunk) unit is combined by the
- * CTA that finishes the unit's last split, found with a per-unit arrival
- * counter; nothing waits on another CTA.
+ * one kernel, in one of two ways chosen per call:
+ *   - cluster mode, when every (b, KV head, query-head chunk) unit fits one
+ *     16-CTA thread-block cluster resident on the GPU and a sixteenth of a
+ *     unit is small: the CTAs of a unit's cluster merge their partials
+ *     through distributed shared memory; no CTA waits for another cluster;
+ *   - global mode otherwise: CTAs publish partials in the workspace and
+ *     count arrivals on a per-unit counter; the last min(chunks, heads)
+ *     arrivals of a unit combine its rows, the earlier of them waiting
+ *     (bounded) until the very last arrival has reset the counter, so the
+ *     launch is cooperative (all CTAs resident).
  *   k_new_bf16, v_new_bf16  device bf16 [B][H_kv][D], contiguous, 16-byte aligned
  *   t_new      0 <= t_new < T_cap, outside [vis_start, vis_end)
- *   workspace  as for kvq_decode_attention; in addition its first
+ *   workspace  as for kvq_decode_attention; in addition, after its
+ *              256-byte head (status word), the next
  *              ceil(4 * L->units / 256) * 256 bytes hold the arrival
  *              counters and must be zero before the first kvq_decode_step
  *              call that uses the workspace (zero the whole workspace once
@@ -203,9 +229,11 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
  *              one workspace must be ordered (one stream), and use layouts
  *              with the same L->units (the counter area's size), or zero
  *              the workspace again when switching.
- * If a staged tile does not arrive within a bounded wait (which only a
- * fault elsewhere can cause) the call still terminates and the affected
- * outputs are NaN.
+ * A bounded wait that gives up (a staged tile that does not arrive, or in
+ * global mode a combining CTA whose unit's last arrival does not come) and
+ * an arrival counter found non-zero at entry never hang the call: the
+ * affected output rows become NaN and the KVQ_STATUS_* bit is OR-ed into
+ * the workspace status word.
  */
 kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,
                            const void* k_new_bf16, const void* v_new_bf16, int32_t t_new,
@@ -311,8 +339,9 @@ kvq_status kvq_sensitivity_probe(const kvq_layout* L, const void* cache, const v
                                  size_t ws_bytes, void* stream);
 
 /* Size in bytes of the device scratch array used by
- * kvq_decode_attention_static_ws (16 MiB: enough for layouts with up to
- * 3008 units, i.e. B * H_kv * ceil(g/8) <= 3008). */
+ * kvq_decode_attention_static_ws (16 MiB).  A layout fits when
+ * L->workspace_bytes <= KVQ_STATIC_WS_BYTES, which holds for up to 3007
+ * units (B * H_kv * ceil(g/8) <= 3007). */
 #define KVQ_STATIC_WS_BYTES (16u * 1024u * 1024u)
 
 /*
@@ -338,6 +367,27 @@ kvq_status kvq_sensitivity_probe(const kvq_layout* L, const void* cache, const v
 kvq_status kvq_decode_attention_static_ws(const kvq_layout* L, const void* cache,
                                           const void* q_bf16, int32_t T, float softmax_scale,
                                           void* out_bf16, float* lse, void* stream);
+
+/*
+ * kvq_workspace_status -- enqueue on `stream` a copy of the workspace's
+ * status word (KVQ_STATUS_* bits of every call that used the workspace
+ * since it was last zeroed) into *status (host memory; pinned memory keeps
+ * the copy asynchronous).  The value is there once the stream has reached
+ * this point (synchronise it).  KVQ_ERR_INVALID_ARG for null or misaligned
+ * pointers, KVQ_ERR_CUDA if the copy cannot be enqueued.
+ */
+kvq_status kvq_workspace_status(const void* workspace, uint32_t* status, void* stream);
+
+/*
+ * kvq_set_wait_limits -- for decode calls made later from the calling host
+ * thread: how many times a kernel polls a staged tile's barrier
+ * (tile_polls; each poll suspends the thread for a hardware-chosen
+ * interval) and, in the global-mode fused step, the unit's counter
+ * (peer_polls; each poll followed by a ~32 ns sleep) before the wait gives
+ * up.  0 restores the default (2^24 and 2^21).  The defaults are far beyond
+ * any healthy wait; shorter limits exist for testing the failure path.
+ */
+void kvq_set_wait_limits(uint32_t tile_polls, uint32_t peer_polls);
 
 /* The cudaError_t value (as int) of the last CUDA call that made an entry
  * point return KVQ_ERR_CUDA on the calling host thread; 0 if none. */

@@ -22,18 +22,21 @@ pytestmark = pytest.mark.gpu
 SCALE = 1.0 / math.sqrt(128)
 
 
+HEAD = 256  # workspace head: the status word, then padding
+
+
 def _cnt_bytes(L):
     return (4 * int(L.units) + 255) // 256 * 256
 
 
 def _ws(L, dev):
     ws = torch.full((int(L.workspace_bytes),), 0x5A, dtype=torch.uint8, device=dev)
-    ws[:_cnt_bytes(L)] = 0  # the per-unit arrival counters
+    ws[:HEAD + _cnt_bytes(L)] = 0  # status word and the per-unit arrival counters
     return ws
 
 
 def _counters_zero(L, ws) -> bool:
-    return bool((ws[:_cnt_bytes(L)] == 0).all().item())
+    return bool((ws[HEAD:HEAD + _cnt_bytes(L)] == 0).all().item())
 
 
 def _step(L, cache, q, ks, vs, t_new, ws):

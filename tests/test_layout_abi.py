@@ -20,7 +20,7 @@ def lib():
 
 def test_header_declares_what_library_exports(lib):
     text = open(HEADER).read()
-    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*|int|size_t)\s+(kvq_\w+)\s*\(", text, re.M))
+    declared = set(re.findall(r"^\s*(?:kvq_status|const char\*|int|size_t|void)\s+(kvq_\w+)\s*\(", text, re.M))
     assert declared == set(kvq.EXPORTED_SYMBOLS)
     out = subprocess.run(["nm", "-D", "--defined-only", kvq.lib_path()], capture_output=True,
                          text=True, check=True).stdout
@@ -99,7 +99,8 @@ def test_layout_matches_formula(lib, case):
     if kb < 16:
         assert L.row_bytes[kvq.SEG_K_CODES] * 8 == kb * D
     slots = L.units + 1024 - 1
-    assert L.workspace_bytes == (_align(4 * L.units, 256) + _align(slots * 8 * D * 4, 256)
+    # 256-byte head (status word), arrival counters, partial o and (m, l)
+    assert L.workspace_bytes == (256 + _align(4 * L.units, 256) + _align(slots * 8 * D * 4, 256)
                                  + _align(slots * 8 * 8, 256))
 
 

@@ -22,7 +22,7 @@ SCALE = 1.0 / math.sqrt(128)
 
 def _ws(L, dev):
     ws = torch.full((int(L.workspace_bytes),), 0x5A, dtype=torch.uint8, device=dev)
-    ws[:(4 * int(L.units) + 255) // 256 * 256] = 0  # the fused step's arrival counters
+    ws[:256 + (4 * int(L.units) + 255) // 256 * 256] = 0  # status word and the fused step's counters
     return ws
 
 
