@@ -23,6 +23,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_ptx.cuh"
+#include "kvq_mq_umma.cuh"
 #include "kvq_split.cuh"
 
 namespace kvq {
@@ -31,6 +32,10 @@ const void* split_kernel_k2(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k4(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k8(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k16(int vb, int G, bool step, int halves, bool general);
+const void* mq_umma_kernel_k2(int vb, int G);
+const void* mq_umma_kernel_k4(int vb, int G);
+const void* mq_umma_kernel_k8(int vb, int G);
+const void* mq_umma_kernel_k16(int vb, int G);
 
 // Combine: one CTA per output row (b, token i, hq), NW warps (combine_row):
 // 16 when some unit has many chunks, 2 when every unit has at most 16 (the
@@ -88,6 +93,16 @@ void packed_tile_geometry(kvq::Params* p) {
   p->pk_off_vc = r128(tt * p->krow);
   p->pk_off_ksz = p->pk_off_vc + r128(tt * p->vrow);
   p->pk_off_vsz = p->pk_off_ksz + r128(tt * p->kszrow);
+}
+
+// Every staged tile holds at least one 32-row block and fits its stage (the
+// kernels walk pieces in steps of whole tiles).
+bool tile_geometry_ok(const kvq::Params* p) {
+  const int bs = 16 * p->pk_halves;
+  if (p->tt_pk < bs || p->tt_pk % bs || p->tt_ko < 32 || p->tt_ko % 32) return false;
+  if (p->pk_off_vsz + p->tt_pk * p->vszrow > kvq::kStageBytes) return false;
+  if (p->ko_off_vsz + p->tt_ko * p->vszrow > kvq::kStageBytes) return false;
+  return p->pk_off_vc + p->tt_pk * p->vrow <= kvq::kStageBytes && p->ko_off_vc + p->tt_ko * p->vrow <= kvq::kStageBytes;
 }
 
 // general: the variant for layouts with K-only heads and multi-query calls.
@@ -213,6 +228,7 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   p->pk_halves = packed_halves(p->plan, L, n_q);
   packed_tile_geometry(p);
   konly_tile_geometry(p);
+  if (!tile_geometry_ok(p)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -228,12 +244,13 @@ static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one
 // requested (the global-mode fused step, whose combining CTAs may wait for
 // other CTAs of their unit).  Programmatic serialisation is dropped if the
 // runtime refuses it.
-kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool cooperative) {
+kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool cooperative,
+                        size_t smem = kSplitSmemBytes, int threads = kvq::kSplitThreads) {
   static std::atomic<int> pdl_ok{1};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p->plan.C);
-  cfg.blockDim = dim3(kvq::kSplitThreads);
-  cfg.dynamicSmemBytes = kSplitSmemBytes;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[3];
   int na = 0;
@@ -283,6 +300,7 @@ kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const vo
   kvq_plan_cuts(&p->plan, p->cuts);
   p->pk_halves = packed_halves(p->plan, L, p->n_q);
   packed_tile_geometry(p);
+  if (!tile_geometry_ok(p)) return KVQ_ERR_UNSUPPORTED;
   *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general);
   if (!*fn) return KVQ_ERR_UNSUPPORTED;
   return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
@@ -358,6 +376,111 @@ extern "C" kvq_status kvq_decode_attention_ragged(const kvq_layout* L, const voi
   return launch_decode(L, p, stream);
 }
 
+// ---- multi-query decode on the tensor-core kernel (kvq_mq_umma.cuh) ----------
+// Used when a KV head has more than eight (query head, token) columns: one
+// pass over a unit's cache serves up to 128 columns.
+
+const void* mq_umma_for(int kb, int vb, int G) {
+  switch (kb) {
+    case 2: return kvq::mq_umma_kernel_k2(vb, G);
+    case 4: return kvq::mq_umma_kernel_k4(vb, G);
+    case 8: return kvq::mq_umma_kernel_k8(vb, G);
+    case 16: return kvq::mq_umma_kernel_k16(vb, G);
+  }
+  return nullptr;
+}
+
+constexpr size_t kMqSmemBytes = sizeof(kvq::mq::Smem);
+static_assert(kMqSmemBytes <= 232448, "multi-query kernel shared memory exceeds one CTA's limit");
+
+// One-time per kernel: shared memory, non-portable clusters, and how many
+// clusters of 16 / 8 / 4 / 2 CTAs the GPU holds at once (index log2(cs)).
+struct MqInfo {
+  const void* fn;
+  int max_clusters[5];
+};
+kvq_status prepare_mq(const void* fn, int* max_clusters) {
+  static std::mutex mu;
+  static MqInfo done[64];
+  static int n_done = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].fn == fn) {
+      for (int k = 0; k < 5; ++k) max_clusters[k] = done[i].max_clusters[k];
+      return KVQ_OK;
+    }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMqSmemBytes));
+  if (e != cudaSuccess) return kvq_cuda_fail(e);
+  MqInfo info;
+  info.fn = fn;
+  info.max_clusters[0] = 0;
+  const bool nonportable = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  for (int k = 1; k < 5; ++k) {
+    const int cs = 1 << k;
+    int ncl = 0;
+    if (cs <= 8 || nonportable) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs);
+      cfg.blockDim = dim3(kvq::mq::kThreads);
+      cfg.dynamicSmemBytes = kMqSmemBytes;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = cs;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg) != cudaSuccess) ncl = 0;
+    }
+    info.max_clusters[k] = ncl;
+  }
+  (void)cudaGetLastError();
+  if (n_done < 64) done[n_done++] = info;
+  for (int k = 0; k < 5; ++k) max_clusters[k] = info.max_clusters[k];
+  return KVQ_OK;
+}
+
+// Units of up to 128 columns; a cluster of cs CTAs per unit at a time, cs
+// chosen for the shortest estimated run: rounds of units over the resident
+// clusters times a cs-th of the largest unit's cost, plus a merge per round
+// for cs > 1.
+kvq_status launch_mq_umma(const kvq_layout* L, kvq::Params* p, void* stream) {
+  const void* fn = mq_umma_for(L->d.k_bits, L->d.v_bits, L->d.group_size);
+  if (!fn) return KVQ_ERR_UNSUPPORTED;
+  int maxcl[5];
+  kvq_status st = prepare_mq(fn, maxcl);
+  if (st != KVQ_OK) return st;
+  int n_sm = 0;
+  if (kvq_device_sm_count(&n_sm) != 0) return KVQ_ERR_CUDA;
+  const int cols = kvq::mq::kCols;
+  p->NHC = (L->g * p->n_q + cols - 1) / cols;
+  const kvq::Plan& P = p->plan;
+  const int64_t U = static_cast<int64_t>(L->d.B) * L->d.H_kv * p->NHC;
+  int64_t biggest = P.U_p ? P.ub_p : 0;
+  if (P.U_k) biggest = std::max(biggest, P.ub_k);
+  if (P.U - P.U_p - P.U_k) biggest = std::max(biggest, P.ub_u);
+  constexpr int64_t kMergeCost = 64 * 1024;  // cost units of one cluster merge (measured order)
+  int best_cs = 1;
+  int64_t best_grid = std::min<int64_t>(U, n_sm);
+  double best = 1e300;
+  for (int k = 4; k >= 0; --k) {
+    const int cs = 1 << k;
+    const int64_t ncl = k == 0 ? n_sm : maxcl[k];
+    if (ncl <= 0) continue;
+    const int64_t rounds = (U + ncl - 1) / ncl;
+    const double est = static_cast<double>(rounds) * (static_cast<double>(biggest) / cs + (cs > 1 ? kMergeCost : 0));
+    if (est < best) {
+      best = est;
+      best_cs = cs;
+      best_grid = std::min<int64_t>(ncl, U) * cs;
+    }
+  }
+  p->plan.U = static_cast<int32_t>(U);
+  p->plan.cs = best_cs;
+  p->plan.C = static_cast<int32_t>(best_grid);
+  return launch_split(fn, p, stream, false, kMqSmemBytes, kvq::mq::kThreads);
+}
+
 extern "C" size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q) {
   if (kvq_check_layout(L) != KVQ_OK || n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS) return 0;
   return static_cast<size_t>(kvq::ws_total_bytes(decode_units(L, n_q)));
@@ -375,6 +498,7 @@ extern "C" kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* c
   const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p, n_q);
   if (st != KVQ_OK) return st;
+  if (L->g * n_q > kvq::kNH) return launch_mq_umma(L, p, stream);  // one pass for every column
   return launch_decode(L, p, stream);
 }
 

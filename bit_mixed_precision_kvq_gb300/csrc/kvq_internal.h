@@ -58,9 +58,15 @@ constexpr int kStageBytes = 32 * 1024;
 KVQ_HD constexpr int packed_row_bytes(int kb, int vb, int G) {
   return 16 * kb + 16 * vb + (kb < 16 ? 4 * (kD / G) : 0) + (vb < 16 ? 4 * (kD / G) : 0);
 }
+// Tiles are whole multiples of 32 rows and every row size is a multiple of
+// 4 bytes, so each of a stage's sub-buffers (K codes, V codes, K and V
+// scale/zero rows) ends on a 128-byte boundary by itself: w bytes per row
+// fill a stage with (kStageBytes / w) rows, rounded down to 32.  A row is at
+// most 512 bytes (bf16 K and V), so every tile holds at least 32 rows.
 KVQ_HD constexpr int packed_tile_rows32(int w) {
-  return ((kStageBytes - 4 * 128) / w) / 32 * 32 > 512 ? 512 : ((kStageBytes - 4 * 128) / w) / 32 * 32;
+  return (kStageBytes / w) / 32 * 32 > 512 ? 512 : (kStageBytes / w) / 32 * 32;
 }
+static_assert(packed_tile_rows32(4 * kD) >= 32, "a stage must hold 32 bf16 K + V rows");
 KVQ_HD constexpr int packed_block_halves(int kb, int vb, int G) {
   return packed_tile_rows32(packed_row_bytes(kb, vb, G)) >= 256 ? 4 : 2;
 }

@@ -42,23 +42,25 @@ namespace kvq {
 // allow 168 registers per thread.
 constexpr int kConsumerWarps = 11;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 5;
+constexpr int kStages = 6;                     // 6 x 32 KB = 192 KB in flight per CTA
 constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
-constexpr uint32_t kPrefetchBytes = kStageBytes;  // L2 prefetch before the dependency wait
+constexpr uint32_t kPrefetchBytes = 32 * 1024;  // L2 prefetch before the dependency wait
 constexpr int kNoLimit = 1 << 30;              // kblock: no multi-query column limit
 constexpr int kMaxClusterCtas = 16;            // cluster mode: CTAs per cluster (at most)
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
-  float merge_o[kConsumerWarps][kNH][kD + 4];  // padded rows: fewer bank conflicts
+  // Merge of the consumer warps' rows: warps 3r .. 3r + 2 fold their scaled
+  // o rows into the three buffers in round r (a fixed order, so results are
+  // reproducible bit for bit); buffer 0 then holds the CTA's merged rows,
+  // which the cluster's other CTAs read in cluster mode.
+  float mbuf[3][kNH][kD + 4];                  // padded rows: fewer bank conflicts
   float merge_ml[kConsumerWarps][kNH][2];
   float merge_sc[kConsumerWarps][kNH];         // exp2(m_warp - M) per (warp, column)
   float merge_ML[kNH][2];                      // the CTA's (M, L) per column
   float qsum[kConsumerWarps][kNH][4];
-  // cluster mode: the CTA's merged partial, read by the cluster's other CTAs
-  float cl_o[kNH][kD];
-  alignas(16) float cl_ml[kNH][2];
+  alignas(16) float cl_ml[kNH][2];             // cluster mode: the CTA's (M, L) per column
   float cl_w[kMaxClusterCtas];                 // the combining CTA's weights per cluster rank
   float cl_ML[2];
   uint64_t full[kStages];
@@ -1108,20 +1110,6 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       sm.merge_ml[warp][2 * tig + 1][0] = acc.m[1];
       sm.merge_ml[warp][2 * tig + 1][1] = acc.l[1];
     }
-    // output rows: protected units d = 16 gid + mt (+ 8); packed units
-    // d = 16 mt + gid (+ 8) (kept as two compile-time patterns)
-    auto store_rows = [&](int dbase, int dstep) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int d0 = dbase + dstep * mt, d1 = d0 + 8;
-        sm.merge_o[warp][2 * tig][d0] = acc.o[mt][0];
-        sm.merge_o[warp][2 * tig + 1][d0] = acc.o[mt][1];
-        sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
-        sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
-      }
-    };
-    if (ui.prot) store_rows(16 * gid, 1);
-    else store_rows(gid, 16);
     // The fused step finishes a unit held by this CTA alone right here;
     // otherwise the partial goes to slot u + c (global mode) or, in cluster
     // mode, to this CTA's shared memory for the cluster's combine.
@@ -1149,15 +1137,44 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       sm.merge_ML[j][1] = L;
     }
     named_bar(1, kConsumerWarps * 32);
+    // The warps' scaled o rows into the three buffers, three warps a round.
+    // Output rows: protected units d = 16 gid + mt (+ 8); packed units
+    // d = 16 mt + gid (+ 8) (two compile-time patterns).
+    auto put_rows = [&](float (*buf)[kD + 4], bool add, int dbase, int dstep) {
+      const float s0 = sm.merge_sc[warp][2 * tig], s1 = sm.merge_sc[warp][2 * tig + 1];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = dbase + dstep * mt, d1 = d0 + 8;
+        float* r0 = &buf[2 * tig][0];
+        float* r1 = &buf[2 * tig + 1][0];
+        if (add) {
+          r0[d0] += acc.o[mt][0] * s0;
+          r1[d0] += acc.o[mt][1] * s1;
+          r0[d1] += acc.o[mt][2] * s0;
+          r1[d1] += acc.o[mt][3] * s1;
+        } else {
+          r0[d0] = acc.o[mt][0] * s0;
+          r1[d0] = acc.o[mt][1] * s1;
+          r0[d1] = acc.o[mt][2] * s0;
+          r1[d1] = acc.o[mt][3] * s1;
+        }
+      }
+    };
+#pragma unroll 1
+    for (int round = 0; round < (kConsumerWarps + 2) / 3; ++round) {
+      if (warp / 3 == round) {
+        if (ui.prot) put_rows(sm.mbuf[warp % 3], round > 0, 16 * gid, 1);
+        else put_rows(sm.mbuf[warp % 3], round > 0, gid, 16);
+      }
+      named_bar(1, kConsumerWarps * 32);
+    }
     const int64_t slot = static_cast<int64_t>(u) + c;
     for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
       const int j = idx / kD, d = idx - j * kD;
-      float O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) O = fmaf(sm.merge_o[w][j][d], sm.merge_sc[w][j], O);
+      const float O = (sm.mbuf[0][j][d] + sm.mbuf[1][j][d]) + sm.mbuf[2][j][d];
       const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
       if (cluster) {
-        sm.cl_o[j][d] = O;
+        sm.mbuf[0][j][d] = O;  // this thread alone touches (j, d)
         if (d == 0) {
           sm.cl_ml[j][0] = M;
           sm.cl_ml[j][1] = L;
@@ -1184,9 +1201,14 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       cluster_sync();
       const int rank = static_cast<int>(cluster_ctarank());
       if (rank < nh) {
-        const int j = rank;
-        if (warp == 0) {
-          const int cs = p.plan.cs;
+        const int j = rank, cs = p.plan.cs;
+        // every rank's row element first (the loads overlap the weights)
+        float x[kMaxClusterCtas];
+        if (ctid < kD) {
+#pragma unroll
+          for (int r = 0; r < kMaxClusterCtas; ++r) x[r] = r < cs ? ld_dsmem(dsmem_addr(&sm.mbuf[0][j][ctid], r)) : 0.f;
+        }
+        if (warp == kConsumerWarps - 1) {  // a warp without row loads takes the weights
           float2 ml = make_float2(-INFINITY, 0.f);
           if (lane < cs) ml = ld_dsmem2(dsmem_addr(&sm.cl_ml[j][0], lane));
           bool bad = ml.x != ml.x;
@@ -1206,12 +1228,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         }
         named_bar(1, kConsumerWarps * 32);
         if (ctid < kD) {
-          const int d = ctid, cs = p.plan.cs;
-          // issue every rank's load before using any (distributed shared
-          // memory round trips overlap); ranks past cs weigh nothing
-          float x[kMaxClusterCtas];
-#pragma unroll
-          for (int r = 0; r < kMaxClusterCtas; ++r) x[r] = r < cs ? ld_dsmem(dsmem_addr(&sm.cl_o[j][d], r)) : 0.f;
+          const int d = ctid;
           float O = 0.f;
 #pragma unroll
           for (int r = 0; r < kMaxClusterCtas; ++r) O = fmaf(x[r], sm.cl_w[r], O);
@@ -1268,7 +1285,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         } else if (role >= 0) {
           const bool bad = sm.abort != 0;
           float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
-          float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
+          float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.mbuf[0][0][0]);
           for (int j = role; j < nh; j += nc)
             combine_row<kConsumerWarps>(p, u, j, cf, cl, out_row(j), warp, lane, sm_ml, sm_o, bad,
                                         []() { named_bar(1, kConsumerWarps * 32); });

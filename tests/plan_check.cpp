@@ -4,7 +4,9 @@
 // agree with a brute-force scan (and so does the most chunks of any unit),
 // multi-query plans have their unit count, partial slots u + c are unique, visual cuts
 // of packed units are 16-row aligned, and with at least as many chunks as
-// units no chunk holds work of two units.  Prints "ok" or the first failure.
+// units no chunk holds work of two units.  Cluster-mode plans (cs chunks per
+// unit, unit u on chunks u * cs .. u * cs + cs - 1) are drawn too.  Prints
+// "ok" or the first failure.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -28,10 +30,35 @@ static uint32_t next(uint32_t n) {
     return 1;                          \
   } while (0)
 
+// Staged-tile geometry for every bit-width and group size: at least one
+// 32-row block per tile, whole multiples of 32 rows, and the sub-buffers
+// (each a multiple of 128 bytes) inside one stage.
+static int check_tiles() {
+  const int bits[] = {2, 4, 8, 16};
+  const int groups[] = {32, 64, 128};
+  for (int kb : bits)
+    for (int vb : bits)
+      for (int G : groups) {
+        const int krow = 16 * kb, vrow = 16 * vb;
+        const int ksz = kb < 16 ? 4 * (kvq::kD / G) : 0, vsz = vb < 16 ? 4 * (kvq::kD / G) : 0;
+        const int tt = kvq::packed_tile_rows32(krow + vrow + ksz + vsz);
+        const int ttk = kvq::packed_tile_rows32(2 * kvq::kD + vrow + vsz);
+        for (int t : {tt, ttk}) {
+          if (t < 32 || t % 32) FAIL("tile of %d rows for K%d V%d G%d", t, kb, vb, G);
+        }
+        if (tt * (krow + vrow + ksz + vsz) > kvq::kStageBytes) FAIL("packed tile overflows (K%d V%d G%d)", kb, vb, G);
+        if ((tt * krow) % 128 || (tt * vrow) % 128 || (tt * ksz) % 128)
+          FAIL("sub-buffer not 128-byte aligned (K%d V%d G%d)", kb, vb, G);
+        if (ttk * (2 * kvq::kD + vrow + vsz) > kvq::kStageBytes) FAIL("K-only tile overflows (V%d G%d)", vb, G);
+      }
+  return 0;
+}
+
 int main(int argc, char** argv) {
   const int cases = argc > 1 ? std::atoi(argv[1]) : 3000;
+  if (check_tiles()) return 1;
   static kvq::Cut cuts[KVQ_MAX_CTAS + 1];
-  int n_aligned = 0, n_stream = 0;
+  int n_aligned = 0, n_stream = 0, n_cluster = 0;
   for (int it = 0; it < cases; ++it) {
     kvq_layout_desc d;
     std::memset(&d, 0, sizeof(d));
@@ -63,8 +90,13 @@ int main(int argc, char** argv) {
     const int n_q = nqs[next(6)];
     kvq::Plan P = kvq_make_plan(&L, T, targets[next(5)], n_q);
     if (P.U != d.B * d.H_kv * ((L.g * n_q + kvq::kNH - 1) / kvq::kNH)) FAIL("case %d: unit count", it);
+    const int css[] = {2, 4, 8, 16};
+    const int cs = css[next(4)];
+    const bool cluster_mode = next(3) == 0 && P.U * cs <= KVQ_MAX_CTAS;
+    if (cluster_mode) P.cs = cs;
     kvq_plan_cuts(&P, cuts);
-    (P.aligned ? n_aligned : n_stream)++;
+    (cluster_mode ? n_cluster : (P.aligned ? n_aligned : n_stream))++;
+    if (cluster_mode && (P.C != P.U * cs || !P.aligned)) FAIL("case %d: cluster plan has %d chunks", it, P.C);
     if (cuts[0].u != 0 || cuts[0].p != 0) FAIL("case %d: cut 0 = (%d,%d)", it, cuts[0].u, cuts[0].p);
     if (cuts[P.C].u != P.U || cuts[P.C].p != 0) FAIL("case %d: last cut", it);
     std::vector<int> covered(P.U, 0);  // next uncovered position of each unit
@@ -100,6 +132,8 @@ int main(int argc, char** argv) {
         }
       int cf, cl;
       kvq::plan_unit_chunks(P, cuts, u, &cf, &cl);
+      if (cluster_mode && (cf != u * cs || cl != u * cs + cs - 1))
+        FAIL("case %d: cluster unit %d on chunks [%d,%d]", it, u, cf, cl);
       if (cf != bf || cl != bl)
         FAIL("case %d (aligned %d): unit %d chunks [%d,%d], brute force [%d,%d]", it, P.aligned, u, cf, cl, bf, bl);
       if (bl - bf + 1 > most) most = bl - bf + 1;
@@ -108,6 +142,6 @@ int main(int argc, char** argv) {
       FAIL("case %d (aligned %d): most chunks per unit %d, brute force %d", it, P.aligned,
            kvq::plan_max_unit_chunks(P, cuts), most);
   }
-  std::printf("ok %d cases (%d per-unit, %d stream)\n", cases, n_aligned, n_stream);
+  std::printf("ok %d cases (%d per-unit, %d stream, %d cluster)\n", cases, n_aligned, n_stream, n_cluster);
   return 0;
 }

@@ -2,7 +2,9 @@
 CPU oracle: token i of sequence b is an ordinary decode query over positions
 [0, T - n_q + 1 + i), so the oracle runs once per token.  Bar as for the
 single-query decode (4e-3 * max|V_hat|); n_q = 1 gives the same bits as
-kvq_decode_attention."""
+kvq_decode_attention.  Calls with more than eight (query head, token)
+columns per KV head run on the tensor-core (tcgen05) kernel, the others on
+the split-KV kernel; the cases cover both."""
 import math
 
 import pytest
@@ -72,3 +74,37 @@ def test_mq_single_token_is_plain_decode(cuda_dev, kvq):
         out1, lse1 = decode(L, cache, q[:, 0].contiguous(), T, SCALE)
         assert torch.equal(out[:, 0].view(torch.int16), out1.view(torch.int16)), T
         assert torch.equal(lse[:, 0], lse1), T
+
+
+def _full_check(c, n_q, T, seed, dev, b_sel=None):
+    L = c.layout()
+    _, k, v = synth.random_case(seed, c.B, c.H_q, c.H_kv, c.D, c.T_cap, dev)
+    cache = alloc_cache(L)
+    append(L, cache, k, v, 0)
+    q = _q(c, n_q, seed + 1, dev)
+    ws = torch.zeros((kvq.decode_mq_workspace_bytes(L, n_q),), dtype=torch.uint8, device=dev)
+    B, _, Hq, D = q.shape
+    out = torch.full((B, n_q, Hq, D), 5.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((B, n_q, Hq), dtype=torch.float32, device=dev)
+    kvq.decode_attention_mq(L, cache, q, T, out, SCALE, lse, ws)
+    torch.cuda.synchronize()
+    assert kvq.workspace_status(ws) == 0
+    kb, vb = bits(k), bits(v)
+    for i in range(n_q):
+        ref, lr, vmax = oracle_decode(c, bits(q[:, i].contiguous()), kb, vb, T - n_q + 1 + i, SCALE)
+        check_decode(c, out[:, i], lse[:, i], ref, lr, vmax)
+
+
+def test_mq_llava_ov_4_tokens(cuda_dev, kvq):
+    """The LLaVA-OneVision-7B layer shape (28/4 heads, 14 text + 6273 visual
+    positions + 4 new text rows, K4/V2 G64, head 0 bf16) with 4 query
+    tokens: 28 columns per KV head in one tensor-core pass."""
+    T = 14 + 6273 + 4
+    _full_check(Case(1, 28, 4, T, 14, 14 + 6273, 4, 2, 64, [0]), 4, T, 1800, cuda_dev)
+
+
+def test_mq_llava_ov_64_tokens(cuda_dev, kvq):
+    """64 query tokens on the same layout: 448 columns per KV head, four
+    128-column units per head."""
+    T = 14 + 1200 + 64
+    _full_check(Case(1, 28, 4, T, 14, 14 + 1200, 4, 2, 64, [0]), 64, T, 1820, cuda_dev)
