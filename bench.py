@@ -96,6 +96,9 @@ def parse_args():
     ap.add_argument("--n-q", type=int, default=1,
                     help="query tokens per sequence and step: > 1 appends n_q rows and runs "
                          "kvq_decode_attention_mq (multi-query decode) per layer")
+    ap.add_argument("--preload", choices=["yes", "no"], default="yes",
+                    help="kvq_set_cache_preload: each layer's kernel copies its first cache tiles "
+                         "while the previous layer's kernel runs (no other kernel writes the caches)")
     ap.add_argument("--probe", action="store_true",
                     help="instead of the decode step: the K-vs-V sensitivity study "
                          "(kvq_sensitivity_probe) on the workload's synthetic cache")
@@ -426,6 +429,8 @@ def run_ours(args, rank, world, local):
     n_layers = args.layers or w.n_layers
     prefill = (args.prefill_in_step == "yes" or
                (args.prefill_in_step == "auto" and args.workload == "llava_next_13b"))
+    import bit_mixed_precision_kvq_gb300 as kvq
+    kvq.set_cache_preload(args.preload == "yes")
     model = Model(w, dev, n_layers, prefill_in_step=prefill, fused=(args.fused == "yes"), n_q=args.n_q)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
@@ -549,7 +554,7 @@ def run_ours(args, rank, world, local):
                                f"protected {w.layers[0].protected}",
                    "bytes_per_step": step_bytes, "l2": "flushed before every timed step",
                    "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
-                   "query_tokens": m_nq},
+                   "query_tokens": m_nq, "cache_preload": args.preload == "yes"},
         "roofline": {"bound": "hbm",
                      "traffic": (NCU_TRAFFIC.get(kernel_source_hash(), {}).get((w.name, n_layers, m_fused))
                                  if m_nq == 1 else None),

@@ -23,7 +23,7 @@ __all__ = [
     "probe_workspace_bytes", "kvq_probe_workspace_bytes", "decode_attention_mq",
     "kvq_decode_attention_mq", "decode_mq_workspace_bytes", "kvq_decode_mq_workspace_bytes",
     "KVQ_MAX_QUERY_TOKENS", "workspace_status", "kvq_workspace_status", "set_wait_limits",
-    "kvq_set_wait_limits", "STATUS_TILE_WAIT", "STATUS_PEER_WAIT", "STATUS_COUNTER",
+    "kvq_set_wait_limits", "set_cache_preload", "kvq_set_cache_preload", "STATUS_TILE_WAIT", "STATUS_PEER_WAIT", "STATUS_COUNTER",
     "SEG_K_CODES", "SEG_K_SZ", "SEG_V_CODES", "SEG_V_SZ", "SEG_PROT_K", "SEG_PROT_V",
     "SEG_TEXT_K", "SEG_TEXT_V", "EXPORTED_SYMBOLS",
 ]
@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = ["kvq_cache_layout", "kvq_quantize_append", "kvq_decode_atten
                     "kvq_sensitivity_probe", "kvq_probe_workspace_bytes", "kvq_decode_attention_mq",
                     "kvq_decode_mq_workspace_bytes",
                     "kvq_decode_attention_static_ws", "kvq_workspace_status", "kvq_set_wait_limits",
+                    "kvq_set_cache_preload",
                     "kvq_last_cuda_error", "kvq_status_string"]
 STATUS_TILE_WAIT, STATUS_PEER_WAIT, STATUS_COUNTER = 1, 2, 4  # KVQ_STATUS_* bits
 STATIC_WS_BYTES = 16 * 1024 * 1024  # KVQ_STATIC_WS_BYTES
@@ -128,6 +129,8 @@ def load() -> ctypes.CDLL:
     lib.kvq_workspace_status.restype = ctypes.c_int
     lib.kvq_set_wait_limits.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
     lib.kvq_set_wait_limits.restype = None
+    lib.kvq_set_cache_preload.argtypes = [ctypes.c_int32]
+    lib.kvq_set_cache_preload.restype = None
     lib.kvq_last_cuda_error.argtypes = []
     lib.kvq_last_cuda_error.restype = ctypes.c_int
     lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -354,6 +357,14 @@ def set_wait_limits(tile_polls: int = 0, peer_polls: int = 0) -> None:
     load().kvq_set_wait_limits(int(tile_polls), int(peer_polls))
 
 
+def set_cache_preload(enable: bool) -> None:
+    """kvq_set_cache_preload: later uniform single-query decode calls from
+    this host thread copy their first cache tiles before the previous
+    kernel in the stream has finished (requires that no kernel outside this
+    library writes the cache just before a call)."""
+    load().kvq_set_cache_preload(1 if enable else 0)
+
+
 # Same names as the C entry points.
 kvq_cache_layout = cache_layout
 kvq_quantize_append = quantize_append
@@ -368,3 +379,4 @@ kvq_decode_mq_workspace_bytes = decode_mq_workspace_bytes
 kvq_probe_workspace_bytes = probe_workspace_bytes
 kvq_workspace_status = workspace_status
 kvq_set_wait_limits = set_wait_limits
+kvq_set_cache_preload = set_cache_preload

@@ -213,9 +213,7 @@ __device__ __forceinline__ int v_elem(int k, int q, int part) {
 // One warp per (b, h, 8 consecutive positions); 4 lanes per row, each lane
 // the elements of its slice of the stored row (K: four 16-byte loads; V:
 // sixteen 4-byte loads, all in flight before any use).
-__global__ void __launch_bounds__(256, 3) append_kernel(const __grid_constant__ AppendArgs a) {
-  pdl_wait();  // the previous kernel in the stream may still read the cache
-  pdl_launch_dependents();
+__device__ __forceinline__ void append_rows(const AppendArgs& a) {
   const Params& p = a.p;
   const int lane = threadIdx.x & 31;
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -291,6 +289,17 @@ __global__ void __launch_bounds__(256, 3) append_kernel(const __grid_constant__ 
       }
     }
   }
+}
+
+// The next kernel in the stream may read cache rows before its own
+// dependency wait (decode preload), so a CTA lets it launch only once all of
+// the CTA's rows are written and fenced.
+__global__ void __launch_bounds__(256, 3) append_kernel(const __grid_constant__ AppendArgs a) {
+  pdl_wait();  // the previous kernel in the stream may still read the cache
+  append_rows(a);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) pdl_launch_dependents();
 }
 
 }  // namespace

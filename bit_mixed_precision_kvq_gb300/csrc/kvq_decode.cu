@@ -180,6 +180,8 @@ bool use_cluster_mode(const kvq::Plan& P, int max_clusters) {
 // Wait limits of the calling host thread (kvq_set_wait_limits); 0 = default.
 thread_local uint32_t tl_tile_polls = 0;
 thread_local uint32_t tl_peer_polls = 0;
+// Early cache-tile copies of the calling host thread (kvq_set_cache_preload).
+thread_local int32_t tl_preload = 0;
 
 // Units of a decode call with n_q query tokens per sequence.
 int64_t decode_units(const kvq_layout* L, int32_t n_q) {
@@ -219,6 +221,7 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
   p->ws_ml = reinterpret_cast<float*>(ws + kvq::kWsHeadBytes + cnt_bytes + kvq::ws_o_bytes(units));
   p->tile_polls = tl_tile_polls ? tl_tile_polls : kvq::kDefaultTilePolls;
   p->peer_polls = tl_peer_polls ? tl_peer_polls : kvq::kDefaultPeerPolls;
+  p->preload = tl_preload;
   p->scale_log2 = softmax_scale * 1.4426950408889634f;
   p->seq_len = nullptr;  // uniform call; the ragged entry points set it
   p->n_q = n_q;
@@ -541,6 +544,8 @@ extern "C" void kvq_set_wait_limits(uint32_t tile_polls, uint32_t peer_polls) {
   tl_tile_polls = tile_polls;
   tl_peer_polls = peer_polls;
 }
+
+extern "C" void kvq_set_cache_preload(int32_t enable) { tl_preload = enable != 0; }
 
 extern "C" kvq_status kvq_workspace_status(const void* workspace, uint32_t* status, void* stream) {
   if (!workspace || !status || reinterpret_cast<uintptr_t>(workspace) % 4) return KVQ_ERR_INVALID_ARG;

@@ -237,6 +237,7 @@ struct Params {
   uint32_t* status;       // workspace status word (KVQ_STATUS_* bits)
   uint32_t tile_polls;    // bounded mbarrier waits on staged tiles
   uint32_t peer_polls;    // bounded wait of the fused step's combining CTAs
+  int32_t preload;        // uniform calls: copy the leading cache tiles before the dependency wait
   float scale_log2;    // softmax_scale * log2(e)
   Plan plan;
   Cut cuts[KVQ_MAX_CTAS + 1];         // cut(c) for c = 0..C, computed on the host

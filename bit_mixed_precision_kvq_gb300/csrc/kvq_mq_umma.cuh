@@ -58,6 +58,11 @@ constexpr int kDequantWarps = 6;
 constexpr int kProducerWarp = 10;
 constexpr int kMmaWarp = 11;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
+// Cluster merge rows in the ring: a column's 128 floats at a pitch of 132
+// (consecutive columns start 16 bytes apart in the bank cycle, so a warp's
+// 16-byte stores spread over every bank slot).
+constexpr int kMergePitch = kD + 4;
+static_assert(kCols * kMergePitch * 4 <= kRing * kStageBytes, "merge rows must fit the ring");
 
 // TMEM columns
 constexpr uint32_t kTmS = 0;      // acc_P, P = 0..3, 32 columns each (bf16 tiles use acc_0)
@@ -310,7 +315,7 @@ __device__ __forceinline__ void cluster_merge(const Params& p, Smem& sm, const M
   const int cs = p.plan.cs;
   const int rank = static_cast<int>(cluster_ctarank());
   const int nloc = rank < un.ncols ? (un.ncols - rank + cs - 1) / cs : 0;
-  const float* mo = reinterpret_cast<const float*>(sm.stage[0]);
+  const float* mo = reinterpret_cast<const float*>(sm.stage[0]);  // rows of kMergePitch floats
   cluster_sync();  // every CTA's partial rows are in its shared memory
   for (int i = threadIdx.x; i < nloc * cs; i += kThreads) {
     const int jj = i / cs, rr = i - jj * cs;
@@ -342,7 +347,7 @@ __device__ __forceinline__ void cluster_merge(const Params& p, Smem& sm, const M
     const int c = rank + jj * cs;
     float x[kMaxClusterCtas];
 #pragma unroll
-    for (int rr = 0; rr < kMaxClusterCtas; ++rr) x[rr] = rr < cs ? ld_dsmem(dsmem_addr(&mo[c * kD + d], rr)) : 0.f;
+    for (int rr = 0; rr < kMaxClusterCtas; ++rr) x[rr] = rr < cs ? ld_dsmem(dsmem_addr(&mo[c * kMergePitch + d], rr)) : 0.f;
     float O = 0.f;
 #pragma unroll
     for (int rr = 0; rr < kMaxClusterCtas; ++rr)
@@ -377,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
     sm.abort = 0;
     fence_barrier_init();
   }
-  pdl_launch_dependents();
   if (warp == kMmaWarp) tmem_alloc(&sm.tmem_base, kTmCols);
   tc_fence_before();
   __syncthreads();
@@ -391,16 +395,25 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
 
   if (warp == kProducerWarp) {
     // ---------------- staged tiles (bulk copies into the ring) ----------------
-    if (lane == 0) {  // L2 prefetch of the pieces before the dependency wait (L2 is coherent)
+    // L2 prefetch (L2 is coherent with the previous kernel's stores): the
+    // tiles of the first ring fill before the dependency wait, the rest of
+    // the pieces once those tiles' copies are queued behind the wait.
+    auto prefetch_tiles = [&](uint32_t from, uint32_t to) {
+      uint32_t k = 0;
       mq_walk(p, nothing, [&](int, const MqUnit& un, int kind, int t0, int n) {
-        tile_sources<false, true>(p, mq_info(p, un), p.plan.T, kind, t0, n,
-                                  [&](uint32_t, const uint8_t* src, uint32_t bytes) { prefetch_l2(src, bytes); });
+        if (k >= from && k < to)
+          tile_sources<false, true>(p, mq_info(p, un), p.plan.T, kind, t0, n,
+                                    [&](uint32_t, const uint8_t* src, uint32_t bytes) { prefetch_l2(src, bytes); });
+        ++k;
       }, nothing);
-    }
+    };
+    if (lane == 0) prefetch_tiles(0, kRing);
     __syncwarp();
     pdl_wait();
+    if (lane == 0) pdl_launch_dependents();  // past the dependency wait; this kernel writes no cache row
     uint32_t it = 0;
     mq_walk(p, nothing, [&](int, const MqUnit& un, int kind, int t0, int n) {
+      if (lane == 0 && it == kRing) prefetch_tiles(kRing, 0xffffffffu);
       if (lane == 0) {
         const int st = it % kRing;
         const uint32_t round = it / kRing;
@@ -534,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             uint4 r = make_uint4(0u, 0u, 0u, 0u);
-            if (active) r = __ldg(qrow + 4 * P + t);
+            if (active) r = __ldcg(qrow + 4 * P + t);
             const float x[8] = {bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y),
                                 bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w)};
 #pragma unroll
@@ -664,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
       float M = sm.abort ? __int_as_float(0x7fffffff) : m_use;
       const float inv = (M != M) ? M : (l > 0.f ? 1.0f / l : 0.f);
       const int64_t row = active ? col_row(p, un.b, un.h, un.hc * kCols + c) : 0;
-      float* mo = reinterpret_cast<float*>(sm.stage[0]) + c * kD;
+      float* mo = reinterpret_cast<float*>(sm.stage[0]) + c * kMergePitch;
       uint32_t a[32];
 #pragma unroll 1
       for (int k = 0; k < 4; ++k) {

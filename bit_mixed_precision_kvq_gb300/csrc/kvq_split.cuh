@@ -49,22 +49,25 @@ constexpr uint32_t kPrefetchBytes = 32 * 1024;  // L2 prefetch before the depend
 constexpr int kNoLimit = 1 << 30;              // kblock: no multi-query column limit
 constexpr int kMaxClusterCtas = 16;            // cluster mode: CTAs per cluster (at most)
 
+// Cluster mode: one rank's partial of a column (o row, then M and L).
+constexpr uint32_t kRecvBytes = (kD + 2) * 4;
+
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
-  // Merge of the consumer warps' rows: warps 3r .. 3r + 2 fold their scaled
-  // o rows into the three buffers in round r (a fixed order, so results are
-  // reproducible bit for bit); buffer 0 then holds the CTA's merged rows,
-  // which the cluster's other CTAs read in cluster mode.
+  // Global mode: merge of the consumer warps' rows -- warps 3r .. 3r + 2
+  // fold their scaled o rows into the three buffers in round r (a fixed
+  // order, so results are reproducible bit for bit).
   float mbuf[3][kNH][kD + 4];                  // padded rows: fewer bank conflicts
   float merge_ml[kConsumerWarps][kNH][2];
   float merge_sc[kConsumerWarps][kNH];         // exp2(m_warp - M) per (warp, column)
   float merge_ML[kNH][2];                      // the CTA's (M, L) per column
   float qsum[kConsumerWarps][kNH][4];
-  alignas(16) float cl_ml[kNH][2];             // cluster mode: the CTA's (M, L) per column
-  float cl_w[kMaxClusterCtas];                 // the combining CTA's weights per cluster rank
-  float cl_ML[2];
+  // Cluster mode: CTA rank j receives column j's partial of every rank r
+  // here (o row, then M and L), stored by rank r.
+  alignas(16) float recv[kMaxClusterCtas][kD + 4];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t recv_bar;  // cluster mode: the other ranks' partials landed (transaction bytes)
   int abort;
   int role;   // fused step: combine role of this CTA for the current unit
   int ncomb;  // fused step: CTAs combining the current unit
@@ -198,36 +201,82 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   }
 }
 
-// Before griddepcontrol.wait: pull the first stage's worth of the CTA's
-// cache rows into L2 (more only delays the first tile and q behind the
-// other SMs' prefetches when the previous kernel does not overlap).  L2 is coherent with every SM's stores, so a
-// line that the previous kernel writes later is simply updated there; the
-// copies into shared memory all come after the wait.
+// Issue the bulk copies of one tile into ring position it.
+template <bool kStep, bool kGen>
+__device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const UnitInfo& ui, int Tu, int kind,
+                                           int t0, int n, uint32_t it) {
+  const int st = it % kStages;
+  const uint32_t round = it / kStages;
+  if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
+    report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
+  uint8_t* dst = sm.stage[st];
+  uint32_t total = 0;
+  tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
+  mbar_arrive_expect_tx(&sm.full[st], total);
+  tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
+    bulk_g2s(dst + off, src, bytes, &sm.full[st]);
+  });
+}
+
+// Before griddepcontrol.wait, with preload set in a uniform call: copy the
+// CTA's leading tiles (one ring at most) into shared memory, stopping at the
+// first tile that holds the fused step's own row (it comes from the previous
+// kernel).  Only cache rows are read.  Sound because every kernel of this
+// library lets the next kernel in the stream launch only after its own
+// dependency wait and after its cache writes are fenced (so when this CTA
+// runs, every earlier cache write of the stream's library kernels is in L2);
+// the caller enables it only where no other kernel writes the cache just
+// before.  Returns the number of tiles issued.
+template <bool kStep, bool kGen>
+__device__ __forceinline__ uint32_t producer_preload(const Params& p, SplitSmem& sm, int c) {
+  if (!p.preload || p.seq_len != nullptr) return 0;
+  uint32_t it = 0;
+  bool stop = false;
+  walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
+    if (stop || it >= static_cast<uint32_t>(kStages) || (kStep && kind == kTileText && t0 + n == Tu)) {
+      stop = true;
+      return;
+    }
+    issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, it);
+    ++it;
+  });
+  return it;
+}
+
+// Before griddepcontrol.wait, first of all: the query rows of the chunk's
+// units into L2 -- the consumers need them before any tile (single-query
+// units read nh consecutive rows of D bf16).
 template <bool kGen>
-__device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
-  // The query rows of the chunk's units first: the consumers need them before
-  // any tile (single-query units read nh consecutive rows of D bf16).
-  {
-    const Cut a = p.cuts[c];
-    const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
-    for (int u = a.u; u <= u_last; ++u) {
-      const UnitInfo ui = unit_info<kGen>(p, u);
-      const int c0 = ui.hc * kNH;
-      if (kGen && p.n_q > 1) {
-        const int nh = min(kNH, p.g * p.n_q - c0);
-        for (int j = 0; j < nh; ++j) prefetch_l2(p.q + col_row(p, ui.b, ui.h, c0 + j) * kD, 2 * kD);
-      } else {
-        const int nh = min(kNH, p.g - c0);
-        prefetch_l2(p.q + (static_cast<int64_t>(ui.b) * p.Hq + ui.h * p.g + c0) * kD,
-                    static_cast<uint32_t>(nh) * 2 * kD);
-      }
+__device__ __forceinline__ void prefetch_q(const Params& p, int c) {
+  const Cut a = p.cuts[c];
+  const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
+  for (int u = a.u; u <= u_last; ++u) {
+    const UnitInfo ui = unit_info<kGen>(p, u);
+    const int c0 = ui.hc * kNH;
+    if (kGen && p.n_q > 1) {
+      const int nh = min(kNH, p.g * p.n_q - c0);
+      for (int j = 0; j < nh; ++j) prefetch_l2(p.q + col_row(p, ui.b, ui.h, c0 + j) * kD, 2 * kD);
+    } else {
+      const int nh = min(kNH, p.g - c0);
+      prefetch_l2(p.q + (static_cast<int64_t>(ui.b) * p.Hq + ui.h * p.g + c0) * kD,
+                  static_cast<uint32_t>(nh) * 2 * kD);
     }
   }
-  // Cluster mode launches fewer CTAs than SMs, so the next layer's CTAs find
-  // free SMs early and have time to prefetch their whole chunk.
+}
+
+// Before griddepcontrol.wait: pull the CTA's next cache rows (after the
+// `skip` tiles already copied) into L2 -- a stage's worth, or in cluster mode
+// the whole chunk (cluster mode launches fewer CTAs than SMs, so the next
+// layer's CTAs find free SMs early and have time for it).  More only delays
+// the first tile and q behind the other SMs' prefetches when the previous
+// kernel does not overlap.  L2 is coherent with every SM's stores, so a line
+// that the previous kernel writes later is simply updated there.
+template <bool kGen>
+__device__ __forceinline__ void producer_prefetch(const Params& p, int c, uint32_t skip) {
   uint32_t budget = p.plan.cs > 1 ? 0xffffffffu : kPrefetchBytes;
+  uint32_t k = 0;
   walk_chunk<kGen, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    if (budget == 0) return;
+    if (k++ < skip || budget == 0) return;
     tile_sources<false, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t* src, uint32_t bytes) {
       const uint32_t b = min(bytes, budget);
       if (b) prefetch_l2(src, b);
@@ -236,21 +285,41 @@ __device__ __forceinline__ void producer_prefetch(const Params& p, int c) {
   });
 }
 
+// The fused step's own K/V row (position Tu - 1, from k_new / v_new) into
+// the cache's text segment, for the units (column chunk 0) whose last
+// position this CTA holds.  Whole producer warp, after the dependency wait:
+// lanes 0-15 the K row, 16-31 the V row, 16 bytes each; then a fence, so the
+// row is visible before this CTA lets the next kernel launch.
+template <bool kGen>
+__device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane) {
+  const Cut a = p.cuts[c];
+  const Cut e = p.cuts[c + 1];
+  const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
+  for (int u = a.u; u <= u_last; ++u) {
+    const UnitInfo ui = unit_info<kGen>(p, u);
+    if (ui.hc != 0) continue;
+    const int Tu = seq_end<true>(p, ui.b);
+    const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
+    const int ps = min((u == a.u) ? a.p : 0, pe);
+    if (ps >= pe || pe != Tu) continue;
+    const int tr = Tu - 1 < p.vs ? Tu - 1 : Tu - 1 - p.Tv;
+    const int64_t bh = static_cast<int64_t>(ui.b) * p.Hkv + ui.h;
+    const int half = lane >> 4, q = lane & 15;
+    const uint4 w = __ldcg(reinterpret_cast<const uint4*>((half ? p.v_new : p.k_new) + bh * kD) + q);
+    uint8_t* dst = const_cast<uint8_t*>(p.seg[half ? KVQ_SEG_TEXT_V : KVQ_SEG_TEXT_K]) +
+                   (bh * p.T_text + tr) * (2 * kD) + 16 * q;
+    *reinterpret_cast<uint4*>(dst) = w;
+  }
+  __threadfence();
+}
+
+// After the dependency wait: the CTA's tiles from ring position `skip` on
+// (the first `skip` were issued by producer_preload).
 template <bool kStep, bool kGen>
-__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c) {
+__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c, uint32_t skip) {
   uint32_t it = 0;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    const int st = it % kStages;
-    const uint32_t round = it / kStages;
-    if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
-      report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
-    uint8_t* dst = sm.stage[st];
-    uint32_t total = 0;
-    tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
-    mbar_arrive_expect_tx(&sm.full[st], total);
-    tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
-      bulk_g2s(dst + off, src, bytes, &sm.full[st]);
-    });
+    if (it >= skip) issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, it);
     ++it;
   });
 }
@@ -917,6 +986,111 @@ __device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt, uint32_t
   return false;
 }
 
+// Cluster mode, after the consumer warps' barrier (every tile consumed,
+// merge_ml published; consumer threads only).  The CTA's partial of column
+// j < nh -- its warps' o rows scaled to the CTA's running max M and summed
+// in warp order, and (M, L) -- goes to slot [this rank] of CTA rank j's
+// receive rows: asynchronous stores that complete on rank j's receive
+// barrier (a plain store for j = this rank).  The warps' scaled rows meet in
+// the staged-tile ring, idle now (one unit per CTA).  CTA rank j < nh then
+// waits (bounded) for the other ranks' slots and writes column j's output
+// row, orow; a CTA that receives nothing is done once its stores are issued.
+__device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem& sm, const Acc& acc, bool prot,
+                                                     int nh, int64_t orow, int warp, int lane) {
+  constexpr int kPitch = kD + 4;  // padded rows: the fragment stores spread over the banks
+  const int gid = lane >> 2, tig = lane & 3;
+  const int ctid = threadIdx.x;
+  float* scr = reinterpret_cast<float*>(sm.stage[0]);  // [warp][kNH][kPitch]
+  {
+    float sc[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = 2 * tig + e;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+      sc[e] = (M == -INFINITY) ? 0.f : exp2f(sm.merge_ml[warp][j][0] - M);
+    }
+    // Output rows: packed units d = 16 mt + gid (+ 8), stored at slot d;
+    // protected units d = 16 gid + mt (+ 8), stored at slot
+    // (d mod 16) * 8 + d / 16 = 8 mt + gid (+ 64) -- both spread a warp's
+    // stores over all banks.  The receiver reads slot_of(d).
+    float* r0 = scr + (warp * kNH + 2 * tig) * kPitch;
+    float* r1 = r0 + kPitch;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int q0 = prot ? 8 * mt + gid : 16 * mt + gid, q1 = q0 + (prot ? 64 : 8);
+      r0[q0] = acc.o[mt][0] * sc[0];
+      r1[q0] = acc.o[mt][1] * sc[1];
+      r0[q1] = acc.o[mt][2] * sc[0];
+      r1[q1] = acc.o[mt][3] * sc[1];
+    }
+  }
+  named_bar(1, kConsumerWarps * 32);
+  const int rank = static_cast<int>(cluster_ctarank()), cs = p.plan.cs;
+  if (ctid < nh * 32) {  // column j, slots d .. d + 3
+    const int j = ctid >> 5, d = (ctid & 31) * 4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(scr + (w * kNH + j) * kPitch + d);
+      o.x += x.x;
+      o.y += x.y;
+      o.z += x.z;
+      o.w += x.w;
+    }
+    float* dst = &sm.recv[rank][d];
+    if (j == rank) *reinterpret_cast<float4*>(dst) = o;
+    else st_async_v4(dsmem_addr(dst, j), o, dsmem_addr(&sm.recv_bar, j));
+  } else if (ctid >= 256 && ctid < 256 + nh) {  // column j's (M, L)
+    const int j = ctid - 256;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float sc = (M == -INFINITY) ? 0.f : exp2f(sm.merge_ml[w][j][0] - M);
+      L = fmaf(sm.merge_ml[w][j][1], sc, L);
+    }
+    if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
+    float* dst = &sm.recv[rank][kD];
+    const float2 ml = make_float2(M, L);
+    if (j == rank) *reinterpret_cast<float2*>(dst) = ml;
+    else st_async_v2(dsmem_addr(dst, j), ml, dsmem_addr(&sm.recv_bar, j));
+  }
+  if (rank >= nh) return;
+  named_bar(1, kConsumerWarps * 32);  // this CTA's own slot is written
+  if (ctid >= kD) return;
+  const bool ok = mbar_wait_cluster(&sm.recv_bar, 0, p.tile_polls);
+  if (!ok) report_failure(p, sm, KVQ_STATUS_PEER_WAIT);
+  // Every receiving warp forms the cs weights itself, lane r for rank r.
+  float mr = -INFINITY, lr = 0.f;
+  if (lane < cs) {
+    mr = sm.recv[lane][kD];
+    lr = sm.recv[lane][kD + 1];
+  }
+  const bool bad = __any_sync(0xffffffffu, !ok || mr != mr);
+  float M = mr != mr ? -INFINITY : mr;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = (mr == -INFINITY || mr != mr || M == -INFINITY) ? 0.f : exp2f(mr - M);
+  float L = lr * w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const int d = ctid, slot = prot ? (d & 15) * 8 + (d >> 4) : d;
+  float O = 0.f;
+#pragma unroll
+  for (int r = 0; r < kMaxClusterCtas; ++r) {
+    const float wr = __shfl_sync(0xffffffffu, w, r);
+    if (r < cs) O = fmaf(sm.recv[r][slot], wr, O);
+  }
+  if (bad) M = __int_as_float(0x7fffffff);
+  const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
+  p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
+  if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
+}
+
 template <int KB, int VB, int G, bool kStep, int NHP, bool kGen>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
@@ -955,8 +1129,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     for (int P = 0; P < 4; ++P) {
       uint4 raw = make_uint4(0u, 0u, 0u, 0u);
       if (gid < nh)
-        raw = __ldg(reinterpret_cast<const uint4*>(
-            p.q + out_row(gid) * kD + 32 * P + 8 * tig));
+        raw = __ldcg(reinterpret_cast<const uint4*>(
+            p.q + out_row(gid) * kD + 32 * P + 8 * tig));  // L2 path: written by the previous kernel
       const float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
                           bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
       qb[2 * P][0] = pack_f16x2(x[0], x[4]);
@@ -1005,25 +1179,12 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     acc.zo[0] = acc.zo[1] = acc.zo[2] = acc.zo[3] = 0.f;
     bool packed_acc = false;  // packed accumulation (see Acc); packed units only
 
-    // Wait for a tile; in the fused step the CTA holding the step's row
-    // (the last row of the last text tile) also writes it into the cache.
-    auto begin_tile = [&](int kind, int t0, int n) -> const uint8_t* {
+    // Wait for a tile.
+    auto begin_tile = [&](int, int, int) -> const uint8_t* {
       const int st = it % kStages;
       const uint32_t round = it / kStages;
       if (!mbar_wait(&sm.full[st], round & 1, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
-      const uint8_t* base = sm.stage[st];
-      if (kStep && kind == kTileText && t0 + n == Tu && ui.hc == 0 && warp == 0) {
-        // lanes 0-15 the K row, lanes 16-31 the V row (position Tu - 1)
-        const int tr = Tu - 1 < p.vs ? Tu - 1 : Tu - 1 - p.Tv;
-        const int64_t row = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * p.T_text + tr;
-        const int half = lane >> 4, q = lane & 15;
-        const uint4 w = *reinterpret_cast<const uint4*>(base + (half ? kBf16VOff : 0) +
-                                                       (n - 1) * (2 * kD) + 16 * q);
-        uint8_t* dst = const_cast<uint8_t*>(p.seg[half ? KVQ_SEG_TEXT_V : KVQ_SEG_TEXT_K]) +
-                       row * (2 * kD) + 16 * q;
-        *reinterpret_cast<uint4*>(dst) = w;
-      }
-      return base;
+      return sm.stage[st];
     };
     // Release the tile's stage once this warp is done with it.
     auto end_tile = [&]() {
@@ -1118,6 +1279,12 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
     const bool sole = kStep && !cluster && cf == cl;
     named_bar(1, kConsumerWarps * 32);
+    if (cluster) {
+      cluster_push_combine(p, sm, acc, ui.prot, nh, out_row(static_cast<int>(cluster_ctarank()) < nh
+                                                                    ? static_cast<int>(cluster_ctarank()) : 0),
+                           warp, lane);
+      continue;  // one unit per CTA in cluster mode
+    }
     // Per column: the CTA's running max M and sum L, and each warp's weight.
     if (ctid < kNH) {
       const int j = ctid;
@@ -1173,13 +1340,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
       const int j = idx / kD, d = idx - j * kD;
       const float O = (sm.mbuf[0][j][d] + sm.mbuf[1][j][d]) + sm.mbuf[2][j][d];
       const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
-      if (cluster) {
-        sm.mbuf[0][j][d] = O;  // this thread alone touches (j, d)
-        if (d == 0) {
-          sm.cl_ml[j][0] = M;
-          sm.cl_ml[j][1] = L;
-        }
-      } else if (sole) {
+      if (sole) {
         const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
         const int64_t orow = out_row(j);
         p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
@@ -1191,56 +1352,6 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
         }
       }
-    }
-    if (cluster) {
-      // Cluster mode: the cs CTAs of this unit's cluster hold one partial
-      // each; CTA rank j combines column j from all of them through
-      // distributed shared memory and writes its output row.  The second
-      // cluster barrier keeps every CTA's shared memory alive until the
-      // reads are done (the producer warp takes part in both barriers).
-      cluster_sync();
-      const int rank = static_cast<int>(cluster_ctarank());
-      if (rank < nh) {
-        const int j = rank, cs = p.plan.cs;
-        // every rank's row element first (the loads overlap the weights)
-        float x[kMaxClusterCtas];
-        if (ctid < kD) {
-#pragma unroll
-          for (int r = 0; r < kMaxClusterCtas; ++r) x[r] = r < cs ? ld_dsmem(dsmem_addr(&sm.mbuf[0][j][ctid], r)) : 0.f;
-        }
-        if (warp == kConsumerWarps - 1) {  // a warp without row loads takes the weights
-          float2 ml = make_float2(-INFINITY, 0.f);
-          if (lane < cs) ml = ld_dsmem2(dsmem_addr(&sm.cl_ml[j][0], lane));
-          bool bad = ml.x != ml.x;
-          float M = bad ? -INFINITY : ml.x;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          bad = __any_sync(0xffffffffu, bad);
-          const float w = (ml.x == -INFINITY || ml.x != ml.x) ? 0.f : exp2f(ml.x - M);
-          float L = ml.y * w;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-          if (lane < kMaxClusterCtas) sm.cl_w[lane] = w;
-          if (lane == 0) {
-            sm.cl_ML[0] = bad ? __int_as_float(0x7fffffff) : M;
-            sm.cl_ML[1] = L;
-          }
-        }
-        named_bar(1, kConsumerWarps * 32);
-        if (ctid < kD) {
-          const int d = ctid;
-          float O = 0.f;
-#pragma unroll
-          for (int r = 0; r < kMaxClusterCtas; ++r) O = fmaf(x[r], sm.cl_w[r], O);
-          const float M = sm.cl_ML[0], L = sm.cl_ML[1];
-          const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
-          const int64_t orow = out_row(j);
-          p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
-          if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
-        }
-      }
-      cluster_sync();
-      continue;  // one unit per CTA in cluster mode
     }
     named_bar(1, kConsumerWarps * 32);
     if constexpr (kStep) {
@@ -1309,21 +1420,34 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
+    mbar_init(&sm.recv_bar, 1);
     sm.abort = 0;
     fence_barrier_init();
   }
-  pdl_launch_dependents();
   __syncthreads();
+  if (p.plan.cs > 1) {
+    // Cluster mode: each CTA expects the other ranks' partials of its column
+    // as transaction bytes; the cluster barrier makes every CTA's receive
+    // barrier initialised before any rank stores into it.
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.recv_bar, (p.plan.cs - 1) * kRecvBytes);
+    cluster_sync();
+  }
   if (warp == kConsumerWarps) {
+    uint32_t pre = 0;
     if (lane == 0) {
-      producer_prefetch<kGen>(p, blockIdx.x);
-      pdl_wait();  // the previous kernel in the stream may have written the cache
-      producer_loop<kStep, kGen>(p, sm, blockIdx.x);
+      prefetch_q<kGen>(p, blockIdx.x);
+      pre = producer_preload<kStep, kGen>(p, sm, blockIdx.x);
+      producer_prefetch<kGen>(p, blockIdx.x, pre);
     }
-    if (p.plan.cs > 1) {  // the consumers' two cluster barriers (cluster mode)
-      __syncwarp();
-      cluster_sync();
-      cluster_sync();
+    __syncwarp();
+    pdl_wait();  // the previous kernel in the stream may have written the cache, q, k_new, v_new
+    if constexpr (kStep) write_step_rows<kGen>(p, blockIdx.x, lane);
+    __syncwarp();
+    if (lane == 0) {
+      // The next kernel may launch (and read cache rows) from here on: this
+      // CTA is past its dependency wait and its cache writes are fenced.
+      pdl_launch_dependents();
+      producer_loop<kStep, kGen>(p, sm, blockIdx.x, pre);
     }
     return;
   }

@@ -76,8 +76,10 @@ extern "C" {
  * counter found by only some CTAs, unreliable):
  *   KVQ_STATUS_TILE_WAIT  a staged cache tile did not arrive within the
  *                         bounded wait (only a fault elsewhere causes it)
- *   KVQ_STATUS_PEER_WAIT  a combining CTA of kvq_decode_step(_ragged) gave up
- *                         waiting for the other CTAs of its unit
+ *   KVQ_STATUS_PEER_WAIT  a combining CTA gave up waiting for the other
+ *                         CTAs of its unit (their partials, in cluster
+ *                         mode; the unit's last arrival, in the global-mode
+ *                         kvq_decode_step(_ragged))
  *   KVQ_STATUS_COUNTER    an arrival counter of kvq_decode_step(_ragged) was
  *                         not zero when the call started (workspace not
  *                         zeroed, or shared by calls that overlap) */
@@ -210,8 +212,11 @@ kvq_status kvq_decode_attention(const kvq_layout* L, const void* cache, const vo
  * one kernel, in one of two ways chosen per call:
  *   - cluster mode, when every (b, KV head, query-head chunk) unit fits one
  *     16-CTA thread-block cluster resident on the GPU and a sixteenth of a
- *     unit is small: the CTAs of a unit's cluster merge their partials
- *     through distributed shared memory; no CTA waits for another cluster;
+ *     unit is small: each CTA of a unit's cluster stores its partial of
+ *     column j into the shared memory of the cluster's CTA j (asynchronous
+ *     distributed-shared-memory stores counted on that CTA's barrier),
+ *     which waits (bounded) for them and writes the row; no CTA waits for
+ *     another cluster;
  *   - global mode otherwise: CTAs publish partials in the workspace and
  *     count arrivals on a per-unit counter; the last min(chunks, heads)
  *     arrivals of a unit combine its rows, the earlier of them waiting
@@ -388,6 +393,26 @@ kvq_status kvq_workspace_status(const void* workspace, uint32_t* status, void* s
  * any healthy wait; shorter limits exist for testing the failure path.
  */
 void kvq_set_wait_limits(uint32_t tile_polls, uint32_t peer_polls);
+
+/*
+ * kvq_set_cache_preload -- for decode calls made later from the calling host
+ * thread: with enable != 0, the uniform single-query calls
+ * (kvq_decode_attention, kvq_decode_attention_static_ws,
+ * kvq_decode_attention_mq with n_q = 1, kvq_decode_step) copy each CTA's
+ * first cache tiles into shared memory before the previous kernel in the
+ * stream has finished (programmatic dependent launch), so a chain of
+ * layers overlaps one layer's cache reads with the previous layer's work.
+ * Only cache rows are read early; q, k_new and v_new after the wait.
+ *
+ * Requirement: every kernel that writes the cache before the call in its
+ * stream is a call of this library, or the host synchronises with it (or
+ * a memory copy separates it) before the call.  The library's own writers
+ * (kvq_quantize_append, kvq_decode_step, kvq_decode_step_ragged) fence
+ * their cache writes and let the next kernel launch only after them and
+ * after their own dependency wait, which makes the early copies see every
+ * row written before.  Off (0) by default.
+ */
+void kvq_set_cache_preload(int32_t enable);
 
 /* The cudaError_t value (as int) of the last CUDA call that made an entry
  * point return KVQ_ERR_CUDA on the calling host thread; 0 if none. */
