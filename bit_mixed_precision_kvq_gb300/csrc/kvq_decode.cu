@@ -298,7 +298,14 @@ kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const vo
   int max_clusters = 0;
   kvq_status st = prepare_split(*fn, kSplitSmemBytes, &max_clusters);
   if (st != KVQ_OK) return st;
-  if (!use_cluster_mode(p->plan, max_clusters)) return KVQ_OK;
+  if (!use_cluster_mode(p->plan, max_clusters)) {
+    // Global mode copies early only when a CTA's share fits one ring: with
+    // more, its early copies would compete for memory with the tail of a
+    // previous kernel as heavy as this one, for no gain.
+    if (p->plan.total / std::max(p->plan.C, 1) > static_cast<int64_t>(kvq::kStages) * kvq::kStageBytes)
+      p->preload = 0;
+    return KVQ_OK;
+  }
   p->plan.cs = kClusterCtas;
   kvq_plan_cuts(&p->plan, p->cuts);
   p->pk_halves = packed_halves(p->plan, L, p->n_q);

@@ -54,7 +54,7 @@ constexpr int kVisAlign = 16;            // visual-row alignment of chunk cuts
 // positions (4 MMA row-tiles per softmax update) when a tile holds >= 256
 // positions, else 32; a call uses 64 only when its chunks are long enough to
 // keep the consumer warps busy with it.
-constexpr int kStageBytes = 32 * 1024;
+constexpr int kStageBytes = 40 * 1024;
 KVQ_HD constexpr int packed_row_bytes(int kb, int vb, int G) {
   return 16 * kb + 16 * vb + (kb < 16 ? 4 * (kD / G) : 0) + (vb < 16 ? 4 * (kD / G) : 0);
 }

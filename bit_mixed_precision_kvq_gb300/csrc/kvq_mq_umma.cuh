@@ -410,7 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
     if (lane == 0) prefetch_tiles(0, kRing);
     __syncwarp();
     pdl_wait();
-    if (lane == 0) pdl_launch_dependents();  // past the dependency wait; this kernel writes no cache row
     uint32_t it = 0;
     mq_walk(p, nothing, [&](int, const MqUnit& un, int kind, int t0, int n) {
       if (lane == 0 && it == kRing) prefetch_tiles(kRing, 0xffffffffu);
@@ -455,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
   } else if (warp == kMmaWarp) {
     // ---------------- MMAs (one thread issues) ----------------
     pdl_wait();
+    if (lane == 0) pdl_launch_dependents();  // past the dependency wait; this kernel writes no cache row
     const uint32_t id_qk = umma_idesc_f16(kCols, kSub, false);
     const uint32_t id_pv = umma_idesc_f16(kCols, kD, true);
     uint32_t q = 0, nu = 0;

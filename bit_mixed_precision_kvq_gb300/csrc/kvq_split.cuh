@@ -42,9 +42,15 @@ namespace kvq {
 // allow 168 registers per thread.
 constexpr int kConsumerWarps = 11;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 6;                     // 6 x 32 KB = 192 KB in flight per CTA
-constexpr int kTileBf16 = 64;                  // positions per bf16 tile: 64 * 512 B = 32 KB
-constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 16 KB into a bf16 stage
+constexpr int kStages = 5;                     // 5 x 40 KB = 200 KB in flight per CTA
+constexpr int kTileBf16 = 80;                  // positions per bf16 tile: 80 * 512 B = 40 KB
+constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 20 KB into a bf16 stage
+// Cluster mode: text tiles of at most 16 rows (a text prefix, the step's
+// row) go to a small stage of their own, so that a CTA's whole piece can be
+// resident at once (16 CTAs of a bf16 head's unit hold ~200 KB each).
+constexpr int kTextStageRows = 16;
+constexpr int kTextVOff = kTextStageRows * 2 * kD;     // V rows start 4 KB into the text stage
+constexpr int kTextStageBytes = 2 * kTextVOff;
 constexpr uint32_t kPrefetchBytes = 32 * 1024;  // L2 prefetch before the dependency wait
 constexpr int kNoLimit = 1 << 30;              // kblock: no multi-query column limit
 constexpr int kMaxClusterCtas = 16;            // cluster mode: CTAs per cluster (at most)
@@ -54,19 +60,23 @@ constexpr uint32_t kRecvBytes = (kD + 2) * 4;
 
 struct SplitSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
-  // Global mode: merge of the consumer warps' rows -- warps 3r .. 3r + 2
-  // fold their scaled o rows into the three buffers in round r (a fixed
-  // order, so results are reproducible bit for bit).
-  float mbuf[3][kNH][kD + 4];                  // padded rows: fewer bank conflicts
+  alignas(128) uint8_t tstage[kTextStageBytes];  // cluster mode: short text tiles
+  union {
+    // Global mode: merge of the consumer warps' rows -- warps 3r .. 3r + 2
+    // fold their scaled o rows into the three buffers in round r (a fixed
+    // order, so results are reproducible bit for bit).
+    float mbuf[3][kNH][kD + 4];  // padded rows: fewer bank conflicts
+    // Cluster mode: CTA rank j receives column j's partial of every rank r
+    // here (o row, then M and L), stored by rank r.
+    float recv[kMaxClusterCtas][kD + 4];
+  };
   float merge_ml[kConsumerWarps][kNH][2];
   float merge_sc[kConsumerWarps][kNH];         // exp2(m_warp - M) per (warp, column)
   float merge_ML[kNH][2];                      // the CTA's (M, L) per column
   float qsum[kConsumerWarps][kNH][4];
-  // Cluster mode: CTA rank j receives column j's partial of every rank r
-  // here (o row, then M and L), stored by rank r.
-  alignas(16) float recv[kMaxClusterCtas][kD + 4];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t full_t, empty_t;  // the text stage
   uint64_t recv_bar;  // cluster mode: the other ranks' partials landed (transaction bytes)
   int abort;
   int role;   // fused step: combine role of this CTA for the current unit
@@ -117,7 +127,7 @@ __device__ __forceinline__ uint32_t round16(uint32_t x) { return (x + 15u) & ~15
 // the launch itself writes.
 template <bool kStep, bool kGen, typename F>
 __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui, int Tu, int kind,
-                                             int t0, int n, F&& f) {
+                                             int t0, int n, F&& f, uint32_t voff = kBf16VOff) {
   if (kGen && kind == kTileKonly) {
     // bf16 K rows (protected K segment) + packed V rows and their scale/zero
     const int64_t krow = prot_k_row(p, ui.b, kClsKonly, ui.slot) * p.Tv + (t0 - p.vs);
@@ -148,13 +158,13 @@ __device__ __forceinline__ void tile_sources(const Params& p, const UnitInfo& ui
       const int64_t nrow = (static_cast<int64_t>(ui.b) * p.Hkv + ui.h) * kD;
       if (head) {
         f(0u, ks + row * (2 * kD), head);
-        f(static_cast<uint32_t>(kBf16VOff), vs + vrow_p * (2 * kD), head);
+        f(voff, vs + vrow_p * (2 * kD), head);
       }
       f(head, reinterpret_cast<const uint8_t*>(p.k_new + nrow), static_cast<uint32_t>(2 * kD));
-      f(kBf16VOff + head, reinterpret_cast<const uint8_t*>(p.v_new + nrow), static_cast<uint32_t>(2 * kD));
+      f(voff + head, reinterpret_cast<const uint8_t*>(p.v_new + nrow), static_cast<uint32_t>(2 * kD));
     } else {
       f(0u, ks + row * (2 * kD), bytes);
-      f(static_cast<uint32_t>(kBf16VOff), vs + vrow_p * (2 * kD), bytes);
+      f(voff, vs + vrow_p * (2 * kD), bytes);
     }
   } else {
     const int64_t row = (static_cast<int64_t>(ui.b) * p.n_packed + ui.slot) * p.Tv_pad + (t0 - p.vs);
@@ -201,21 +211,48 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
   }
 }
 
-// Issue the bulk copies of one tile into ring position it.
+// Where a tile is staged: the text stage (cluster mode, text tiles of at
+// most kTextStageRows rows) or the ring.  Producer and consumers count the
+// tiles of each in walk order: TileSeq::r ring tiles, TileSeq::t text-stage
+// tiles so far.
+__device__ __forceinline__ bool in_text_stage(const Params& p, int kind, int n) {
+  return p.plan.cs > 1 && kind == kTileText && n <= kTextStageRows;
+}
+struct TileSeq {
+  uint32_t r = 0, t = 0;
+};
+
+// Issue the bulk copies of one tile into its stage (waiting, bounded, for the
+// stage's previous tile to be released) and advance the sequence.
 template <bool kStep, bool kGen>
 __device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const UnitInfo& ui, int Tu, int kind,
-                                           int t0, int n, uint32_t it) {
-  const int st = it % kStages;
-  const uint32_t round = it / kStages;
-  if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
-    report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
-  uint8_t* dst = sm.stage[st];
+                                           int t0, int n, TileSeq& seq) {
+  uint8_t* dst;
+  uint64_t* full;
+  uint32_t voff = kBf16VOff;
+  if (in_text_stage(p, kind, n)) {
+    if (seq.t > 0 && !mbar_wait(&sm.empty_t, (seq.t - 1) & 1, p.tile_polls))
+      report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
+    dst = sm.tstage;
+    full = &sm.full_t;
+    voff = kTextVOff;
+    ++seq.t;
+  } else {
+    const int st = seq.r % kStages;
+    const uint32_t round = seq.r / kStages;
+    if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
+      report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
+    dst = sm.stage[st];
+    full = &sm.full[st];
+    ++seq.r;
+  }
   uint32_t total = 0;
-  tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; });
-  mbar_arrive_expect_tx(&sm.full[st], total);
+  tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t, const uint8_t*, uint32_t bytes) { total += bytes; },
+                            voff);
+  mbar_arrive_expect_tx(full, total);
   tile_sources<kStep, kGen>(p, ui, Tu, kind, t0, n, [&](uint32_t off, const uint8_t* src, uint32_t bytes) {
-    bulk_g2s(dst + off, src, bytes, &sm.full[st]);
-  });
+    bulk_g2s(dst + off, src, bytes, full);
+  }, voff);
 }
 
 // Before griddepcontrol.wait, with preload set in a uniform call: copy the
@@ -231,21 +268,23 @@ template <bool kStep, bool kGen>
 __device__ __forceinline__ uint32_t producer_preload(const Params& p, SplitSmem& sm, int c) {
   if (!p.preload || p.seq_len != nullptr) return 0;
   uint32_t it = 0;
+  TileSeq seq;
   bool stop = false;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    if (stop || it >= static_cast<uint32_t>(kStages) || (kStep && kind == kTileText && t0 + n == Tu)) {
+    const bool full = in_text_stage(p, kind, n) ? seq.t >= 1 : seq.r >= static_cast<uint32_t>(kStages);
+    if (stop || full || (kStep && kind == kTileText && t0 + n == Tu)) {
       stop = true;
       return;
     }
-    issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, it);
+    issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, seq);
     ++it;
   });
   return it;
 }
 
-// Before griddepcontrol.wait, first of all: the query rows of the chunk's
-// units into L2 -- the consumers need them before any tile (single-query
-// units read nh consecutive rows of D bf16).
+// Before griddepcontrol.wait (after the early tile copies are issued): the
+// query rows of the chunk's units into L2 -- the consumers need them before
+// any tile (single-query units read nh consecutive rows of D bf16).
 template <bool kGen>
 __device__ __forceinline__ void prefetch_q(const Params& p, int c) {
   const Cut a = p.cuts[c];
@@ -264,13 +303,13 @@ __device__ __forceinline__ void prefetch_q(const Params& p, int c) {
   }
 }
 
-// Before griddepcontrol.wait: pull the CTA's next cache rows (after the
-// `skip` tiles already copied) into L2 -- a stage's worth, or in cluster mode
-// the whole chunk (cluster mode launches fewer CTAs than SMs, so the next
-// layer's CTAs find free SMs early and have time for it).  More only delays
-// the first tile and q behind the other SMs' prefetches when the previous
-// kernel does not overlap.  L2 is coherent with every SM's stores, so a line
-// that the previous kernel writes later is simply updated there.
+// Pull the CTA's next cache rows (after the `skip` tiles already copied)
+// into L2 -- a stage's worth, or in cluster mode the rest of the chunk --
+// so that the copies issued later hit L2: before griddepcontrol.wait when
+// nothing was copied early (L2 is coherent with every SM's stores, so a line
+// that the previous kernel writes later is simply updated there), else right
+// after it, off the path of the early copies.  More only delays the first
+// tile and q behind the other SMs' prefetches.
 template <bool kGen>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c, uint32_t skip) {
   uint32_t budget = p.plan.cs > 1 ? 0xffffffffu : kPrefetchBytes;
@@ -287,7 +326,7 @@ __device__ __forceinline__ void producer_prefetch(const Params& p, int c, uint32
 
 // The fused step's own K/V row (position Tu - 1, from k_new / v_new) into
 // the cache's text segment, for the units (column chunk 0) whose last
-// position this CTA holds.  Whole producer warp, after the dependency wait:
+// position this CTA holds.  The whole producer warp, after the dependency wait:
 // lanes 0-15 the K row, 16-31 the V row, 16 bytes each; then a fence, so the
 // row is visible before this CTA lets the next kernel launch.
 template <bool kGen>
@@ -295,6 +334,7 @@ __device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane
   const Cut a = p.cuts[c];
   const Cut e = p.cuts[c + 1];
   const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
+  bool wrote = false;
   for (int u = a.u; u <= u_last; ++u) {
     const UnitInfo ui = unit_info<kGen>(p, u);
     if (ui.hc != 0) continue;
@@ -309,8 +349,9 @@ __device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane
     uint8_t* dst = const_cast<uint8_t*>(p.seg[half ? KVQ_SEG_TEXT_V : KVQ_SEG_TEXT_K]) +
                    (bh * p.T_text + tr) * (2 * kD) + 16 * q;
     *reinterpret_cast<uint4*>(dst) = w;
+    wrote = true;
   }
-  __threadfence();
+  if (wrote) __threadfence();
 }
 
 // After the dependency wait: the CTA's tiles from ring position `skip` on
@@ -318,8 +359,15 @@ __device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane
 template <bool kStep, bool kGen>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c, uint32_t skip) {
   uint32_t it = 0;
+  TileSeq seq;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    if (it >= skip) issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, it);
+    if (it >= skip) {
+      issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, seq);
+    } else if (in_text_stage(p, kind, n)) {
+      ++seq.t;
+    } else {
+      ++seq.r;
+    }
     ++it;
   });
 }
@@ -1027,6 +1075,7 @@ __device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem&
     }
   }
   named_bar(1, kConsumerWarps * 32);
+  cluster_wait();  // every rank's receive barrier is initialised (arrived at kernel start)
   const int rank = static_cast<int>(cluster_ctarank()), cs = p.plan.cs;
   if (ctid < nh * 32) {  // column j, slots d .. d + 3
     const int j = ctid >> 5, d = (ctid & 31) * 4;
@@ -1100,7 +1149,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
   const int u_last = chunk_last_unit(p.cuts, c, p.plan.U);
   constexpr int ppg = G / 32;
   const float sl2 = p.scale_log2;
-  uint32_t it = 0;    // tiles seen (stage ring position)
+  uint32_t it = 0;    // tiles seen
+  TileSeq seq;        // ... of them in the ring and in the text stage
   uint32_t gblk = 0;  // 32-position blocks dealt so far (round-robin over warps)
   for (int u = a.u; u <= u_last; ++u) {
     const UnitInfo ui = unit_info<kGen>(p, u);
@@ -1179,17 +1229,23 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     acc.zo[0] = acc.zo[1] = acc.zo[2] = acc.zo[3] = 0.f;
     bool packed_acc = false;  // packed accumulation (see Acc); packed units only
 
-    // Wait for a tile.
-    auto begin_tile = [&](int, int, int) -> const uint8_t* {
-      const int st = it % kStages;
-      const uint32_t round = it / kStages;
-      if (!mbar_wait(&sm.full[st], round & 1, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
-      return sm.stage[st];
+    // Wait for a tile; voff: where its bf16 V rows start in the stage.
+    uint32_t voff = kBf16VOff;
+    bool in_text = false;
+    auto begin_tile = [&](int kind, int, int n) -> const uint8_t* {
+      in_text = in_text_stage(p, kind, n);
+      uint64_t* full = in_text ? &sm.full_t : &sm.full[seq.r % kStages];
+      const uint32_t parity = in_text ? (seq.t & 1) : ((seq.r / kStages) & 1);
+      if (!mbar_wait(full, parity, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
+      voff = in_text ? kTextVOff : kBf16VOff;
+      return in_text ? sm.tstage : sm.stage[seq.r % kStages];
     };
     // Release the tile's stage once this warp is done with it.
     auto end_tile = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[it % kStages]);
+      if (lane == 0) mbar_arrive(in_text ? &sm.empty_t : &sm.empty[seq.r % kStages]);
+      if (in_text) ++seq.t;
+      else ++seq.r;
       ++it;
     };
     // This warp's blocks (bs rows each) of a tile of n rows: first, first + 11, ...
@@ -1205,7 +1261,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
         int first;
         const int nb = deal(n, 32, first);
         for (int kb = first; kb < nb; kb += kConsumerWarps)
-          kblock<2, kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n,
+          kblock<2, kKBf16, kVBf16Lane, 16, 16, G>(base, nullptr, base + voff, nullptr, kb * 32, n,
                                                   kGen && kind == kTileText ? endA - t0 : kNoLimit,
                                                   kGen && kind == kTileText ? endB - t0 : kNoLimit, sl2, qb,
                                                   zb, gid, tig, lane, acc);
@@ -1248,7 +1304,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
             }
           }
           for (int kb = first; kb < nb; kb += kConsumerWarps)
-            kblock<2, kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + kBf16VOff, nullptr, kb * 32, n,
+            kblock<2, kKBf16, kVBf16D, 16, 16, G>(base, nullptr, base + voff, nullptr, kb * 32, n,
                                                  kGen ? endA - t0 : kNoLimit, kGen ? endB - t0 : kNoLimit, sl2,
                                                  qb, zb, gid, tig, lane, acc);
         }
@@ -1420,6 +1476,8 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
+    mbar_init(&sm.full_t, 1);
+    mbar_init(&sm.empty_t, kConsumerWarps);
     mbar_init(&sm.recv_bar, 1);
     sm.abort = 0;
     fence_barrier_init();
@@ -1427,26 +1485,31 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
   __syncthreads();
   if (p.plan.cs > 1) {
     // Cluster mode: each CTA expects the other ranks' partials of its column
-    // as transaction bytes; the cluster barrier makes every CTA's receive
-    // barrier initialised before any rank stores into it.
+    // as transaction bytes.  The cluster barrier, arrived at here and waited
+    // for before the first store into another CTA (consumers) or before the
+    // dependency wait (producer), makes every CTA's receive barrier
+    // initialised before any rank stores into it.
     if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.recv_bar, (p.plan.cs - 1) * kRecvBytes);
-    cluster_sync();
+    cluster_arrive();
   }
   if (warp == kConsumerWarps) {
     uint32_t pre = 0;
     if (lane == 0) {
-      prefetch_q<kGen>(p, blockIdx.x);
       pre = producer_preload<kStep, kGen>(p, sm, blockIdx.x);
-      producer_prefetch<kGen>(p, blockIdx.x, pre);
+      prefetch_q<kGen>(p, blockIdx.x);
+      if (pre == 0) producer_prefetch<kGen>(p, blockIdx.x, 0);
     }
     __syncwarp();
-    pdl_wait();  // the previous kernel in the stream may have written the cache, q, k_new, v_new
+    if (p.plan.cs > 1) cluster_wait();
+    pdl_wait();  // the previous kernel in the stream may have written the cache, k_new, v_new
     if constexpr (kStep) write_step_rows<kGen>(p, blockIdx.x, lane);
     __syncwarp();
     if (lane == 0) {
-      // The next kernel may launch (and read cache rows) from here on: this
-      // CTA is past its dependency wait and its cache writes are fenced.
+      // The next kernel in the stream may launch (and read cache rows) from
+      // here on: this CTA is past its dependency wait and its cache writes
+      // are fenced.
       pdl_launch_dependents();
+      if (pre > 0) producer_prefetch<kGen>(p, blockIdx.x, pre);
       producer_loop<kStep, kGen>(p, sm, blockIdx.x, pre);
     }
     return;
