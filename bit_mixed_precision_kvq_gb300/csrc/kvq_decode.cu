@@ -491,6 +491,19 @@ kvq_status launch_mq_umma(const kvq_layout* L, kvq::Params* p, void* stream) {
   return launch_split(fn, p, stream, false, kMqSmemBytes, kvq::mq::kThreads);
 }
 
+// Which multi-query path is faster, from measured crossovers (GB300, both
+// paths timed on the same calls; L2 flushed): the split kernel re-reads a KV
+// head's cache once per 8 columns but runs at a high rate per CTA; the
+// tcgen05 kernel reads it once per 128 columns at a lower rate per CTA.  The
+// tcgen05 kernel wins only when the split passes fill the GPU several times
+// over: at least 32 (sequence, KV head) pairs and either >= 128 columns per
+// KV head, or >= 32 columns with a short history (T <= 2048).
+bool use_mq_umma(const kvq_layout* L, int32_t n_q, int32_t T) {
+  const int64_t cols = static_cast<int64_t>(L->g) * n_q;
+  if (cols <= kvq::kNH || static_cast<int64_t>(L->d.B) * L->d.H_kv < 32) return false;
+  return cols >= 128 || (cols >= 32 && T <= 2048);
+}
+
 extern "C" size_t kvq_decode_mq_workspace_bytes(const kvq_layout* L, int32_t n_q) {
   if (kvq_check_layout(L) != KVQ_OK || n_q < 1 || n_q > KVQ_MAX_QUERY_TOKENS) return 0;
   return static_cast<size_t>(kvq::ws_total_bytes(decode_units(L, n_q)));
@@ -508,8 +521,8 @@ extern "C" kvq_status kvq_decode_attention_mq(const kvq_layout* L, const void* c
   const kvq_status st = decode_params(L, cache, q_bf16, T, softmax_scale, out_bf16, lse, workspace,
                                       ws_bytes, p, n_q);
   if (st != KVQ_OK) return st;
-  if (L->g * n_q > kvq::kNH) return launch_mq_umma(L, p, stream);  // one pass for every column
-  return launch_decode(L, p, stream);
+  if (use_mq_umma(L, n_q, T)) return launch_mq_umma(L, p, stream);  // one pass for up to 128 columns
+  return launch_decode(L, p, stream);  // one split pass per 8 columns
 }
 
 extern "C" kvq_status kvq_decode_step(const kvq_layout* L, void* cache, const void* q_bf16,

@@ -11,23 +11,23 @@
 // all of them.  Per 32-position sub-tile:
 //   S[c][t]  = q_c . k_t      M = 128 columns, N = 32 positions, K = d
 //   O[c][d] += P[c][t] v_t    M = 128 columns, N = 128 d, K = 32 positions
-// Operands: q (and the per-group q sums) sit in TMEM as the A operand of QK;
-// K sub-tiles are written to shared memory as fp16 tiles -- packed codes as
-// the exact subnormals c * 2^(p - 24) of the split kernel's storage order,
-// one accumulator per 32-element block P of d (its codes share the bit
-// offset p, and G >= 32 keeps P inside one quantisation group), plus one for
-// the zero-point term (A = q group sums as an fp16 hi + lo pair, B = z) --
-// or bf16 rows converted to fp16 (exact); the softmax applies
-// s * 2^(24 - p) per (position, P).  V sub-tiles are dequantised to fp16
+// Operands: q (and the per-group q sums) sit in shared memory as the A
+// operand of QK; K sub-tiles are written to shared memory as fp16 tiles --
+// packed codes moved to bit 0 of their half-word, i.e. the exact subnormals
+// c * 2^-24, in the split kernel's permuted d order, one accumulator per
+// quantisation group g, plus one for the zero-point term (A = q group sums
+// as an fp16 hi + lo pair, B = z) -- or bf16 rows converted to fp16
+// (exact); the softmax applies s_g * 2^24 per (position, group).  V sub-tiles are dequantised to fp16
 // (code * s + z, one rounding) or converted from bf16, so O accumulates true
 // values for every tile kind.  P is written to TMEM (fp16) as the A operand
-// of PV.  The online softmax keeps a running maximum per column (one TMEM
+// of PV.  S has two TMEM buffers, so the QK of the next sub-tile runs while
+// the softmax reads this one.  The online softmax keeps a running maximum per column (one TMEM
 // lane = one thread) and rescales O only when a column's maximum grows by
 // more than 2^8 (P stays <= 256 in fp16).
 //
 // CTA = 12 warps: warps 0-3 softmax (TMEM lanes 32w .. 32w + 31 = columns),
 // warps 4-9 build the operand tiles, warp 10 stages cache tiles by bulk
-// copies (TMA) into a 4 x 32 KB ring, warp 11 allocates TMEM and one of its
+// copies (TMA) into a 3-stage ring, warp 11 allocates TMEM and one of its
 // threads issues the MMAs.  A cluster of cs CTAs takes a unit at a time (unit
 // u goes to cluster u mod clusters), splits its positions at equal cost and
 // merges the cs partial rows through distributed shared memory; cs = 1 CTAs
@@ -51,7 +51,7 @@ namespace mq {
 
 constexpr int kCols = 128;         // columns per unit (MMA M)
 constexpr int kSub = 32;           // positions per sub-tile (QK N, PV K)
-constexpr int kRing = 4;           // staged-tile ring (4 x 32 KB)
+constexpr int kRing = 3;           // staged-tile ring (3 stages)
 constexpr int kOps = 3;            // operand-tile buffers (sub-tiles built ahead of the MMAs)
 constexpr int kThreads = 384;
 constexpr int kDequantWarps = 6;
@@ -64,13 +64,14 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (log2 units)
 constexpr int kMergePitch = kD + 4;
 static_assert(kCols * kMergePitch * 4 <= kRing * kStageBytes, "merge rows must fit the ring");
 
-// TMEM columns
-constexpr uint32_t kTmS = 0;      // acc_P, P = 0..3, 32 columns each (bf16 tiles use acc_0)
-constexpr uint32_t kTmZ = 128;    // zero-point term, 32
-constexpr uint32_t kTmO = 160;    // O, 128
-constexpr uint32_t kTmP = 288;    // P buffers, 2 x 16
-constexpr uint32_t kTmQ = 320;    // q (fp16, 64 columns = 128 d)
-constexpr uint32_t kTmQs = 384;   // q group sums (hi, lo), 8
+// TMEM columns: two S buffers (QK of the next sub-tile runs while the
+// softmax reads this one), O, two P buffers.
+constexpr uint32_t kTmS = 0;      // S buffer b at kTmS + b * kTmSStride: acc_g, g < D / G <= 4, 32 columns
+                                  // each (bf16 tiles use acc_0), then the zero-point term, 32
+constexpr uint32_t kTmSStride = 160;
+constexpr uint32_t kTmZ = 128;    // zero-point term, inside an S buffer
+constexpr uint32_t kTmO = 320;    // O, 128
+constexpr uint32_t kTmP = 448;    // P buffers, 2 x 16
 constexpr uint32_t kTmCols = 512;
 
 enum SubKind { kSubPackedK = 0, kSubBf16K = 1 };
@@ -80,13 +81,15 @@ struct Smem {
   alignas(1024) uint8_t kt[kOps][kSub * 256];        // K operand: 32 pos x 128 fp16, K-major
   alignas(1024) uint8_t vt[kOps][kSub * 256];        // V operand: 32 pos x 128 fp16, MN-major
   alignas(128) uint8_t zt[kOps][kSub * 32];          // Z operand: 32 pos x 16 fp16, K-major
-  alignas(16) float fac[kOps][4][kSub];              // s * 2^(24 - p) * scale_log2 per (P, position)
+  alignas(16) float fac[kOps][4][kSub];              // s_g * 2^24 * scale_log2 per (group g, position)
+  alignas(1024) uint8_t qt[kCols * kD * 2];         // q: 128 columns x 128 fp16, K-major (A of QK)
+  alignas(128) uint8_t qst[kCols * 16 * 2];         // q group sums (hi, lo): 128 x 16 fp16, K-major
   alignas(16) float ml[kCols][2];                    // cluster merge: the CTA's (m, l) per column
   float wm[kCols], wl[kCols];                        // cluster merge: (m, l), then weights, per (column, rank)
   float mML[kCols][2];                               // cluster merge: (M, L) per combined column
   uint64_t full[kRing], empty[kRing];
   uint64_t op_full[kOps], pv_done[kOps], p_full[2];
-  uint64_t s_full, s_free, q_ready;
+  uint64_t s_full[2], s_free[2], q_ready;
   uint32_t tmem_base;
   int abort;
 };
@@ -213,6 +216,12 @@ __device__ __forceinline__ void build_sub(const Params& p, Smem& sm, int kind, c
         uint32_t f[4][4];
         if (pos < n) {
           k_packed_regs<KB>(kc + (r0 + pos) * KROW, t, f);
+          // every code to bit 0 of its half-word (c * 2^-24), so that the
+          // blocks of one quantisation group share one accumulator
+#pragma unroll
+          for (int P = 0; P < 4; ++P)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[P][i] >>= kKShift<KB>(P);
         } else {
 #pragma unroll
           for (int P = 0; P < 4; ++P) f[P][0] = f[P][1] = f[P][2] = f[P][3] = 0u;
@@ -241,7 +250,7 @@ __device__ __forceinline__ void build_sub(const Params& p, Smem& sm, int kind, c
         sts128(zt + (pos >> 3) * 128 + (pos & 7) * 16, zw[0], zw[1], zw[2], zw[3]);
         sts128(zt + 512 + (pos >> 3) * 128 + (pos & 7) * 16, zw[4], zw[5], zw[6], zw[7]);
 #pragma unroll
-        for (int P = 0; P < 4; ++P) sm.fac[buf][P][pos] = s[(32 * P) / G] * kKFactor<KB>(P) * p.scale_log2;
+        for (int g = 0; g < NG; ++g) sm.fac[buf][g][pos] = s[g] * 16777216.f * p.scale_log2;
       }
     }
   } else {  // bf16 K rows (text, protected, K-only, or 16-bit "packed" K): 16 chunks of 8 d per row
@@ -376,8 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
       mbar_init(&sm.pv_done[b], 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&sm.p_full[b], 4);
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.s_free[b], 4);
+    }
     mbar_init(&sm.q_ready, 4);
     sm.abort = 0;
     fence_barrier_init();
@@ -483,24 +494,28 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
         if (lane == 0) {
           const int buf = q % kOps;
           wait_bar(p, sm, &sm.op_full[buf], (q / kOps) & 1);
-          if (q > 0) wait_bar(p, sm, &sm.s_free, (q - 1) & 1);
+          if (q >= 2) wait_bar(p, sm, &sm.s_free[q & 1], ((q - 2) >> 1) & 1);
           tc_fence_after();
           const uint32_t kb = smem_u32(sm.kt[buf]);
+          const uint32_t qa = smem_u32(sm.qt);  // K step ks of q: chunks 2 ks, 2 ks + 1
+          const uint32_t sb = tm + kTmS + (q & 1) * kTmSStride;
           if (KB < 16 && kind == kTilePacked) {
+            // one accumulator per quantisation group g: K steps 2P, 2P + 1 of
+            // the 32-element blocks P of g
 #pragma unroll
-            for (int P = 0; P < 4; ++P)
-#pragma unroll
-              for (int s = 0; s < 2; ++s) {
-                const int ks = 2 * P + s;
-                umma_ts(tm + kTmS + 32 * P, tm + kTmQ + 8 * ks, umma_sdesc(kb + ks * 1024, 512, 128), id_qk, s > 0);
-              }
-            umma_ts(tm + kTmZ, tm + kTmQs, umma_sdesc(smem_u32(sm.zt[buf]), 512, 128), id_qk, false);
+            for (int ks = 0; ks < 8; ++ks) {
+              const int g = (16 * ks) / G;
+              umma_ss(sb + 32 * g, umma_sdesc(qa + ks * 4096, 2048, 128), umma_sdesc(kb + ks * 1024, 512, 128),
+                      id_qk, (16 * ks) % G != 0);
+            }
+            umma_ss(sb + kTmZ, umma_sdesc(smem_u32(sm.qst), 2048, 128), umma_sdesc(smem_u32(sm.zt[buf]), 512, 128),
+                    id_qk, false);
           } else {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-              umma_ts(tm + kTmS, tm + kTmQ + 8 * ks, umma_sdesc(kb + ks * 1024, 512, 128), id_qk, ks > 0);
+              umma_ss(sb, umma_sdesc(qa + ks * 4096, 2048, 128), umma_sdesc(kb + ks * 1024, 512, 128), id_qk, ks > 0);
           }
-          umma_commit(&sm.s_full);
+          umma_commit(&sm.s_full[q & 1]);
           if (pending) issue_pv(q - 1);
         }
         pending = true;
@@ -531,9 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
       const int cg = un.hc * kCols + c;  // column among the KV head's g * n_q
       end_c = active ? p.plan.T - (p.n_q - 1 - cg % p.n_q) : 0;
       if (pe <= ps) return;
-      // q of this column into TMEM: fp16 in the permuted order kappa (column
-      // 16P + 4t + i holds d = 32P + 8t + i and d + 4), and its group sums
-      // as an fp16 hi + lo pair (K index g and NG + g)
+      // q of this column as row c of the QK A tile (K-major core matrices:
+      // element kappa at (kappa / 8) * 2048 + (c / 8) * 128 + (c % 8) * 16 +
+      // (kappa % 8) * 2), fp16 in the permuted order kappa = 32P + 8t + 2i + e
+      // for d = 32P + 8t + i + 4e; its group sums as an fp16 hi + lo pair
+      // (K index g and NG + g) as row c of the zero-point A tile
       uint32_t qv[32];
       float qs[NG];
 #pragma unroll
@@ -558,7 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
             qs[(32 * P) / G] += sum;
           }
         }
-        tmem_st32(tm + lb + kTmQ + 32 * half, qv);
+#pragma unroll
+        for (int P2 = 0; P2 < 2; ++P2)
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            sts128(sm.qt + (4 * (2 * half + P2) + t) * 2048 + (c >> 3) * 128 + (c & 7) * 16, qv[16 * P2 + 4 * t],
+                   qv[16 * P2 + 4 * t + 1], qv[16 * P2 + 4 * t + 2], qv[16 * P2 + 4 * t + 3]);
       }
       uint32_t zq[16];
 #pragma unroll
@@ -570,9 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
         zq[g >> 1] |= static_cast<uint32_t>(__half_as_ushort(hi)) << (16 * (g & 1));
         zq[(NG + g) >> 1] |= static_cast<uint32_t>(__half_as_ushort(lo)) << (16 * ((NG + g) & 1));
       }
-      tmem_st16(tm + lb + kTmQs, zq);
-      tmem_st_wait();
-      tc_fence_before();
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        sts128(sm.qst + k * 2048 + (c >> 3) * 128 + (c & 7) * 16, zq[4 * k], zq[4 * k + 1], zq[4 * k + 2],
+               zq[4 * k + 3]);
+      fence_async_smem();  // the tensor cores read the tiles
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_ready);
     }, [&](int, const MqUnit&, int kind, int t0, int n) {
@@ -580,50 +604,51 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
         const int buf = q & 1, ob = q % kOps;
         const int nval = min(kSub, n - r0);
         const int t0s = t0 + r0;
-        wait_bar(p, sm, &sm.s_full, q & 1);
+        wait_bar(p, sm, &sm.s_full[q & 1], (q >> 1) & 1);
         tc_fence_after();
+        const uint32_t sb = kTmS + (q & 1) * kTmSStride;
         float S[kSub];
         uint32_t a[32];
         if (KB < 16 && kind == kTilePacked) {
-          // two halves of 16 positions: the five accumulators' loads in flight together
+          // two halves of 16 positions: the accumulators' loads in flight together
+          constexpr int NG = kD / G;
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            uint32_t az[16], a0[16], a1[16], a2[16], a3[16];
-            tmem_ld16(tm + lb + kTmZ + 16 * hf, az);
-            tmem_ld16(tm + lb + kTmS + 16 * hf, a0);
-            tmem_ld16(tm + lb + kTmS + 32 + 16 * hf, a1);
-            tmem_ld16(tm + lb + kTmS + 64 + 16 * hf, a2);
-            tmem_ld16(tm + lb + kTmS + 96 + 16 * hf, a3);
+            uint32_t az[16], ag[NG][16];
+            tmem_ld16(tm + lb + sb + kTmZ + 16 * hf, az);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) tmem_ld16(tm + lb + sb + 32 * g + 16 * hf, ag[g]);
             tmem_ld_wait();
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 f0 = reinterpret_cast<const float4*>(sm.fac[ob][0])[4 * hf + i4];
-              const float4 f1 = reinterpret_cast<const float4*>(sm.fac[ob][1])[4 * hf + i4];
-              const float4 f2 = reinterpret_cast<const float4*>(sm.fac[ob][2])[4 * hf + i4];
-              const float4 f3 = reinterpret_cast<const float4*>(sm.fac[ob][3])[4 * hf + i4];
-              const float fa[4][4] = {{f0.x, f0.y, f0.z, f0.w}, {f1.x, f1.y, f1.z, f1.w},
-                                      {f2.x, f2.y, f2.z, f2.w}, {f3.x, f3.y, f3.z, f3.w}};
+              float fa[NG][4];
+#pragma unroll
+              for (int g = 0; g < NG; ++g) {
+                const float4 f = reinterpret_cast<const float4*>(sm.fac[ob][g])[4 * hf + i4];
+                fa[g][0] = f.x;
+                fa[g][1] = f.y;
+                fa[g][2] = f.z;
+                fa[g][3] = f.w;
+              }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = 4 * i4 + e;
                 float x = sl2 * __uint_as_float(az[i]);
-                x = fmaf(fa[0][e], __uint_as_float(a0[i]), x);
-                x = fmaf(fa[1][e], __uint_as_float(a1[i]), x);
-                x = fmaf(fa[2][e], __uint_as_float(a2[i]), x);
-                x = fmaf(fa[3][e], __uint_as_float(a3[i]), x);
+#pragma unroll
+                for (int g = 0; g < NG; ++g) x = fmaf(fa[g][e], __uint_as_float(ag[g][i]), x);
                 S[16 * hf + i] = x;
               }
             }
           }
         } else {
-          tmem_ld32(tm + lb + kTmS, a);
+          tmem_ld32(tm + lb + sb, a);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < kSub; ++i) S[i] = sl2 * __uint_as_float(a[i]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_free);
+        if (lane == 0) mbar_arrive(&sm.s_free[q & 1]);
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kSub; ++i) {
@@ -633,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
         const bool need = mx > m_use + kRescaleLog2 || (m_use == -INFINITY && mx > -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mx : m_use;
-          const float cr = (need && m_use != -INFINITY) ? exp2f(m_use - m_new) : 1.f;
+          const float cr = (need && m_use != -INFINITY) ? ex2(m_use - m_new) : 1.f;
           if (have_o) {  // every earlier PV must have landed before O is rescaled
             wait_bar(p, sm, &sm.pv_done[(q - 1) % kOps], ((q - 1) / kOps) & 1);
             tc_fence_after();
@@ -654,8 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_umma_kernel(const __grid_const
         float ls = 0.f;
 #pragma unroll
         for (int j = 0; j < kSub / 2; ++j) {
-          const float p0 = S[2 * j] == -INFINITY ? 0.f : exp2f(S[2 * j] - m_use);
-          const float p1 = S[2 * j + 1] == -INFINITY ? 0.f : exp2f(S[2 * j + 1] - m_use);
+          const float p0 = S[2 * j] == -INFINITY ? 0.f : ex2(S[2 * j] - m_use);
+          const float p1 = S[2 * j + 1] == -INFINITY ? 0.f : ex2(S[2 * j + 1] - m_use);
           ls += p0 + p1;
           pp[j] = pack_f16x2(p0, p1);
         }

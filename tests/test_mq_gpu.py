@@ -2,9 +2,11 @@
 CPU oracle: token i of sequence b is an ordinary decode query over positions
 [0, T - n_q + 1 + i), so the oracle runs once per token.  Bar as for the
 single-query decode (4e-3 * max|V_hat|); n_q = 1 gives the same bits as
-kvq_decode_attention.  Calls with more than eight (query head, token)
-columns per KV head run on the tensor-core (tcgen05) kernel, the others on
-the split-KV kernel; the cases cover both."""
+kvq_decode_attention.  Calls run on the split-KV kernel (one pass per 8
+(query head, token) columns of a KV head) unless there are at least 32
+(sequence, KV head) pairs and >= 128 columns per KV head, or >= 32 columns
+with T <= 2048 -- then on the tensor-core (tcgen05) kernel (one pass per 128
+columns); the cases cover both."""
 import math
 
 import pytest
@@ -43,6 +45,10 @@ CASES = [
     (Case(1, 4, 4, 400, 16, 300, 2, 4, 32, [0]), 64, 400),                # g = 1, 64 tokens: 8 units
     (Case(2, 16, 2, 2500, 30, 2400, 4, 2, 64, [], konly=[1]), 6, 2450),   # long history, K-only head
     (Case(16, 16, 16, 130, 10, 120, 4, 2, 32, [3]), 8, 130),              # 256 units: stream-cut plan
+    # tensor-core kernel: 64 (b, KV head) pairs, g = 4, 8 tokens = 32 columns, short history
+    (Case(8, 32, 8, 600, 10, 560, 2, 2, 32, [3]), 8, 600),
+    # tensor-core kernel: 32 pairs, 32 tokens = 128 columns, T > 2048, K-only head
+    (Case(4, 32, 8, 2300, 16, 2200, 4, 2, 64, [1], konly=[5]), 32, 2300),
 ]
 
 
