@@ -17,10 +17,11 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libkvq.so")
 SOURCES = ["kvq_layout.cpp", "kvq_append.cu", "kvq_decode.cu", "kvq_split_k2.cu", "kvq_split_k4.cu",
-           "kvq_split_k8.cu", "kvq_split_k16.cu", "kvq_decode_noalloc.cu",
+           "kvq_split_k8.cu", "kvq_split_k16.cu", "kvq_split_cl_k2.cu", "kvq_split_cl_k4.cu",
+           "kvq_split_cl_k8.cu", "kvq_split_cl_k16.cu", "kvq_decode_noalloc.cu",
            "kvq_probe.cu", "kvq_mq_umma_k2.cu", "kvq_mq_umma_k4.cu", "kvq_mq_umma_k8.cu",
            "kvq_mq_umma_k16.cu"]
-HEADERS = ["kvq_internal.h", "kvq_device.cuh", "kvq_ptx.cuh", "kvq_split.cuh", "kvq_umma.cuh",
+HEADERS = ["kvq_internal.h", "kvq_device.cuh", "kvq_ptx.cuh", "kvq_split.cuh", "kvq_split_inst.cuh", "kvq_umma.cuh",
            "kvq_mq_umma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

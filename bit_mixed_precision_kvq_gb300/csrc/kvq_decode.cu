@@ -32,6 +32,10 @@ const void* split_kernel_k2(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k4(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k8(int vb, int G, bool step, int halves, bool general);
 const void* split_kernel_k16(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_cl_k2(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_cl_k4(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_cl_k8(int vb, int G, bool step, int halves, bool general);
+const void* split_kernel_cl_k16(int vb, int G, bool step, int halves, bool general);
 const void* mq_umma_kernel_k2(int vb, int G);
 const void* mq_umma_kernel_k4(int vb, int G);
 const void* mq_umma_kernel_k8(int vb, int G);
@@ -106,12 +110,12 @@ bool tile_geometry_ok(const kvq::Params* p) {
 }
 
 // general: the variant for layouts with K-only heads and multi-query calls.
-const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool general) {
+const void* split_kernel_for(int kb, int vb, int G, bool step, int halves, bool general, bool cluster) {
   switch (kb) {
-    case 2: return kvq::split_kernel_k2(vb, G, step, halves, general);
-    case 4: return kvq::split_kernel_k4(vb, G, step, halves, general);
-    case 8: return kvq::split_kernel_k8(vb, G, step, halves, general);
-    case 16: return kvq::split_kernel_k16(vb, G, step, halves, general);
+    case 2: return (cluster ? kvq::split_kernel_cl_k2 : kvq::split_kernel_k2)(vb, G, step, halves, general);
+    case 4: return (cluster ? kvq::split_kernel_cl_k4 : kvq::split_kernel_k4)(vb, G, step, halves, general);
+    case 8: return (cluster ? kvq::split_kernel_cl_k8 : kvq::split_kernel_k8)(vb, G, step, halves, general);
+    case 16: return (cluster ? kvq::split_kernel_cl_k16 : kvq::split_kernel_k16)(vb, G, step, halves, general);
   }
   return nullptr;
 }
@@ -293,25 +297,24 @@ kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool coope
 // plan to cluster mode where that pays; *fn gets the kernel.
 kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const void** fn) {
   const bool general = L->n_konly > 0 || p->n_q > 1;
-  *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general);
-  if (!*fn) return KVQ_ERR_UNSUPPORTED;
+  // the cluster-mode kernel of the same shape: how many of its clusters fit
+  const void* fn_cl = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, true);
+  if (!fn_cl) return KVQ_ERR_UNSUPPORTED;
   int max_clusters = 0;
-  kvq_status st = prepare_split(*fn, kSplitSmemBytes, &max_clusters);
+  kvq_status st = prepare_split(fn_cl, kSplitSmemBytes, &max_clusters);
   if (st != KVQ_OK) return st;
   if (!use_cluster_mode(p->plan, max_clusters)) {
-    // Global mode copies early only when a CTA's share fits one ring: with
-    // more, its early copies would compete for memory with the tail of a
-    // previous kernel as heavy as this one, for no gain.
-    if (p->plan.total / std::max(p->plan.C, 1) > static_cast<int64_t>(kvq::kStages) * kvq::kStageBytes)
-      p->preload = 0;
-    return KVQ_OK;
+    p->preload = 0;  // early copies are a cluster-mode feature (a CTA's whole piece fits its ring)
+    *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, false);
+    if (!*fn) return KVQ_ERR_UNSUPPORTED;
+    return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
   }
   p->plan.cs = kClusterCtas;
   kvq_plan_cuts(&p->plan, p->cuts);
   p->pk_halves = packed_halves(p->plan, L, p->n_q);
   packed_tile_geometry(p);
   if (!tile_geometry_ok(p)) return KVQ_ERR_UNSUPPORTED;
-  *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general);
+  *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, true);
   if (!*fn) return KVQ_ERR_UNSUPPORTED;
   return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
 }

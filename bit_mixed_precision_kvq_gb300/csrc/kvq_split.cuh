@@ -215,8 +215,9 @@ __device__ __forceinline__ void walk_chunk(const Params& p, int c, F&& f) {
 // most kTextStageRows rows) or the ring.  Producer and consumers count the
 // tiles of each in walk order: TileSeq::r ring tiles, TileSeq::t text-stage
 // tiles so far.
-__device__ __forceinline__ bool in_text_stage(const Params& p, int kind, int n) {
-  return p.plan.cs > 1 && kind == kTileText && n <= kTextStageRows;
+template <bool kCl>
+__device__ __forceinline__ bool in_text_stage(int kind, int n) {
+  return kCl && kind == kTileText && n <= kTextStageRows;
 }
 struct TileSeq {
   uint32_t r = 0, t = 0;
@@ -224,13 +225,13 @@ struct TileSeq {
 
 // Issue the bulk copies of one tile into its stage (waiting, bounded, for the
 // stage's previous tile to be released) and advance the sequence.
-template <bool kStep, bool kGen>
+template <bool kStep, bool kGen, bool kCl>
 __device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const UnitInfo& ui, int Tu, int kind,
                                            int t0, int n, TileSeq& seq) {
   uint8_t* dst;
   uint64_t* full;
   uint32_t voff = kBf16VOff;
-  if (in_text_stage(p, kind, n)) {
+  if (in_text_stage<kCl>(kind, n)) {
     if (seq.t > 0 && !mbar_wait(&sm.empty_t, (seq.t - 1) & 1, p.tile_polls))
       report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
     dst = sm.tstage;
@@ -264,19 +265,19 @@ __device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const
 // runs, every earlier cache write of the stream's library kernels is in L2);
 // the caller enables it only where no other kernel writes the cache just
 // before.  Returns the number of tiles issued.
-template <bool kStep, bool kGen>
+template <bool kStep, bool kGen, bool kCl>
 __device__ __forceinline__ uint32_t producer_preload(const Params& p, SplitSmem& sm, int c) {
-  if (!p.preload || p.seq_len != nullptr) return 0;
+  if (!kCl || !p.preload || p.seq_len != nullptr) return 0;
   uint32_t it = 0;
   TileSeq seq;
   bool stop = false;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    const bool full = in_text_stage(p, kind, n) ? seq.t >= 1 : seq.r >= static_cast<uint32_t>(kStages);
+    const bool full = in_text_stage<kCl>(kind, n) ? seq.t >= 1 : seq.r >= static_cast<uint32_t>(kStages);
     if (stop || full || (kStep && kind == kTileText && t0 + n == Tu)) {
       stop = true;
       return;
     }
-    issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, seq);
+    issue_tile<kStep, kGen, kCl>(p, sm, ui, Tu, kind, t0, n, seq);
     ++it;
   });
   return it;
@@ -310,9 +311,9 @@ __device__ __forceinline__ void prefetch_q(const Params& p, int c) {
 // that the previous kernel writes later is simply updated there), else right
 // after it, off the path of the early copies.  More only delays the first
 // tile and q behind the other SMs' prefetches.
-template <bool kGen>
+template <bool kGen, bool kCl>
 __device__ __forceinline__ void producer_prefetch(const Params& p, int c, uint32_t skip) {
-  uint32_t budget = p.plan.cs > 1 ? 0xffffffffu : kPrefetchBytes;
+  uint32_t budget = kCl ? 0xffffffffu : kPrefetchBytes;
   uint32_t k = 0;
   walk_chunk<kGen, false, false>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     if (k++ < skip || budget == 0) return;
@@ -356,14 +357,14 @@ __device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane
 
 // After the dependency wait: the CTA's tiles from ring position `skip` on
 // (the first `skip` were issued by producer_preload).
-template <bool kStep, bool kGen>
+template <bool kStep, bool kGen, bool kCl>
 __device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c, uint32_t skip) {
   uint32_t it = 0;
   TileSeq seq;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
     if (it >= skip) {
-      issue_tile<kStep, kGen>(p, sm, ui, Tu, kind, t0, n, seq);
-    } else if (in_text_stage(p, kind, n)) {
+      issue_tile<kStep, kGen, kCl>(p, sm, ui, Tu, kind, t0, n, seq);
+    } else if (in_text_stage<kCl>(kind, n)) {
       ++seq.t;
     } else {
       ++seq.r;
@@ -1140,7 +1141,7 @@ __device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem&
   if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
 }
 
-template <int KB, int VB, int G, bool kStep, int NHP, bool kGen>
+template <int KB, int VB, int G, bool kStep, int NHP, bool kGen, bool kCl>
 __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
@@ -1233,7 +1234,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     uint32_t voff = kBf16VOff;
     bool in_text = false;
     auto begin_tile = [&](int kind, int, int n) -> const uint8_t* {
-      in_text = in_text_stage(p, kind, n);
+      in_text = in_text_stage<kCl>(kind, n);
       uint64_t* full = in_text ? &sm.full_t : &sm.full[seq.r % kStages];
       const uint32_t parity = in_text ? (seq.t & 1) : ((seq.r / kStages) & 1);
       if (!mbar_wait(full, parity, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
@@ -1330,132 +1331,132 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     // The fused step finishes a unit held by this CTA alone right here;
     // otherwise the partial goes to slot u + c (global mode) or, in cluster
     // mode, to this CTA's shared memory for the cluster's combine.
-    const bool cluster = p.plan.cs > 1;
+    constexpr bool cluster = kCl;
     int cf = c, cl = c;
     if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
     const bool sole = kStep && !cluster && cf == cl;
     named_bar(1, kConsumerWarps * 32);
-    if (cluster) {
+    if constexpr (kCl) {
       cluster_push_combine(p, sm, acc, ui.prot, nh, out_row(static_cast<int>(cluster_ctarank()) < nh
                                                                     ? static_cast<int>(cluster_ctarank()) : 0),
                            warp, lane);
-      continue;  // one unit per CTA in cluster mode
-    }
-    // Per column: the CTA's running max M and sum L, and each warp's weight.
-    if (ctid < kNH) {
-      const int j = ctid;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float m = sm.merge_ml[w][j][0];
-        const float sc = (M == -INFINITY) ? 0.f : exp2f(m - M);
-        sm.merge_sc[w][j] = sc;
-        L = fmaf(sm.merge_ml[w][j][1], sc, L);
-      }
-      if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
-      sm.merge_ML[j][0] = M;
-      sm.merge_ML[j][1] = L;
-    }
-    named_bar(1, kConsumerWarps * 32);
-    // The warps' scaled o rows into the three buffers, three warps a round.
-    // Output rows: protected units d = 16 gid + mt (+ 8); packed units
-    // d = 16 mt + gid (+ 8) (two compile-time patterns).
-    auto put_rows = [&](float (*buf)[kD + 4], bool add, int dbase, int dstep) {
-      const float s0 = sm.merge_sc[warp][2 * tig], s1 = sm.merge_sc[warp][2 * tig + 1];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int d0 = dbase + dstep * mt, d1 = d0 + 8;
-        float* r0 = &buf[2 * tig][0];
-        float* r1 = &buf[2 * tig + 1][0];
-        if (add) {
-          r0[d0] += acc.o[mt][0] * s0;
-          r1[d0] += acc.o[mt][1] * s1;
-          r0[d1] += acc.o[mt][2] * s0;
-          r1[d1] += acc.o[mt][3] * s1;
-        } else {
-          r0[d0] = acc.o[mt][0] * s0;
-          r1[d0] = acc.o[mt][1] * s1;
-          r0[d1] = acc.o[mt][2] * s0;
-          r1[d1] = acc.o[mt][3] * s1;
+    } else {
+      // Per column: the CTA's running max M and sum L, and each warp's weight.
+      if (ctid < kNH) {
+        const int j = ctid;
+        float M = -INFINITY;
+  #pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+        float L = 0.f;
+  #pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float m = sm.merge_ml[w][j][0];
+          const float sc = (M == -INFINITY) ? 0.f : exp2f(m - M);
+          sm.merge_sc[w][j] = sc;
+          L = fmaf(sm.merge_ml[w][j][1], sc, L);
         }
-      }
-    };
-#pragma unroll 1
-    for (int round = 0; round < (kConsumerWarps + 2) / 3; ++round) {
-      if (warp / 3 == round) {
-        if (ui.prot) put_rows(sm.mbuf[warp % 3], round > 0, 16 * gid, 1);
-        else put_rows(sm.mbuf[warp % 3], round > 0, gid, 16);
+        if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
+        sm.merge_ML[j][0] = M;
+        sm.merge_ML[j][1] = L;
       }
       named_bar(1, kConsumerWarps * 32);
-    }
-    const int64_t slot = static_cast<int64_t>(u) + c;
-    for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
-      const int j = idx / kD, d = idx - j * kD;
-      const float O = (sm.mbuf[0][j][d] + sm.mbuf[1][j][d]) + sm.mbuf[2][j][d];
-      const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
-      if (sole) {
-        const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
-        const int64_t orow = out_row(j);
-        p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
-        if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
-      } else {
-        p.ws_o[(slot * kNH + j) * kD + d] = O;
-        if (d == 0) {
-          p.ws_ml[(slot * kNH + j) * 2] = M;
-          p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
-        }
-      }
-    }
-    named_bar(1, kConsumerWarps * 32);
-    if constexpr (kStep) {
-      if (!sole) {
-        // Publish the partial.  The last min(n, nh) arrivals at the unit's
-        // counter (n = its chunks) combine its rows, arrival n - nh + r
-        // taking rows r, r + min(n, nh), ...; the very last one resets the
-        // counter to zero (for the next call), which also releases the
-        // others, who wait (bounded) for that.  An arrival that finds the
-        // counter at n or more (it was not zero when the call started)
-        // reports it and writes NaN rows.
-        if (ctid == 0) {
-          __threadfence();
-          const uint32_t n = static_cast<uint32_t>(cl - cf + 1);
-          const uint32_t nc = min(n, static_cast<uint32_t>(nh));
-          const uint32_t k = atomicAdd(&p.cnt[u], 1u);
-          int role = -1;
-          if (k >= n) {
-            report_failure(p, sm, KVQ_STATUS_COUNTER);
-            role = -2;
-          } else if (k == n - 1) {
-            __threadfence();
-            atomicExch(&p.cnt[u], 0u);
-            role = static_cast<int>(nc) - 1;
-          } else if (k >= n - nc) {
-            role = static_cast<int>(k - (n - nc));
-            if (!wait_unit_released(&p.cnt[u], p.peer_polls)) report_failure(p, sm, KVQ_STATUS_PEER_WAIT);
+      // The warps' scaled o rows into the three buffers, three warps a round.
+      // Output rows: protected units d = 16 gid + mt (+ 8); packed units
+      // d = 16 mt + gid (+ 8) (two compile-time patterns).
+      auto put_rows = [&](float (*buf)[kD + 4], bool add, int dbase, int dstep) {
+        const float s0 = sm.merge_sc[warp][2 * tig], s1 = sm.merge_sc[warp][2 * tig + 1];
+  #pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int d0 = dbase + dstep * mt, d1 = d0 + 8;
+          float* r0 = &buf[2 * tig][0];
+          float* r1 = &buf[2 * tig + 1][0];
+          if (add) {
+            r0[d0] += acc.o[mt][0] * s0;
+            r1[d0] += acc.o[mt][1] * s1;
+            r0[d1] += acc.o[mt][2] * s0;
+            r1[d1] += acc.o[mt][3] * s1;
+          } else {
+            r0[d0] = acc.o[mt][0] * s0;
+            r1[d0] = acc.o[mt][1] * s1;
+            r0[d1] = acc.o[mt][2] * s0;
+            r1[d1] = acc.o[mt][3] * s1;
           }
-          __threadfence();
-          sm.role = role;
-          sm.ncomb = static_cast<int>(nc);
+        }
+      };
+  #pragma unroll 1
+      for (int round = 0; round < (kConsumerWarps + 2) / 3; ++round) {
+        if (warp / 3 == round) {
+          if (ui.prot) put_rows(sm.mbuf[warp % 3], round > 0, 16 * gid, 1);
+          else put_rows(sm.mbuf[warp % 3], round > 0, gid, 16);
         }
         named_bar(1, kConsumerWarps * 32);
-        const int role = sm.role, nc = sm.ncomb;
-        if (role == -2) {  // corrupt counter: every row of the unit becomes NaN
-          for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
-            const int j = idx / kD, d = idx - j * kD;
-            const int64_t orow = out_row(j);
-            p.out[orow * kD + d] = 0x7fffu;  // bf16 NaN
-            if (d == 0 && p.lse) p.lse[orow] = __int_as_float(0x7fffffff);
+      }
+      const int64_t slot = static_cast<int64_t>(u) + c;
+      for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
+        const int j = idx / kD, d = idx - j * kD;
+        const float O = (sm.mbuf[0][j][d] + sm.mbuf[1][j][d]) + sm.mbuf[2][j][d];
+        const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
+        if (sole) {
+          const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
+          const int64_t orow = out_row(j);
+          p.out[orow * kD + d] = f32_to_bf16_bits(O * inv);
+          if (d == 0 && p.lse) p.lse[orow] = (M != M) ? M : 0.69314718055994531f * (M + log2f(L));
+        } else {
+          p.ws_o[(slot * kNH + j) * kD + d] = O;
+          if (d == 0) {
+            p.ws_ml[(slot * kNH + j) * 2] = M;
+            p.ws_ml[(slot * kNH + j) * 2 + 1] = L;
           }
-        } else if (role >= 0) {
-          const bool bad = sm.abort != 0;
-          float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
-          float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.mbuf[0][0][0]);
-          for (int j = role; j < nh; j += nc)
-            combine_row<kConsumerWarps>(p, u, j, cf, cl, out_row(j), warp, lane, sm_ml, sm_o, bad,
-                                        []() { named_bar(1, kConsumerWarps * 32); });
+        }
+      }
+      named_bar(1, kConsumerWarps * 32);
+      if constexpr (kStep) {
+        if (!sole) {
+          // Publish the partial.  The last min(n, nh) arrivals at the unit's
+          // counter (n = its chunks) combine its rows, arrival n - nh + r
+          // taking rows r, r + min(n, nh), ...; the very last one resets the
+          // counter to zero (for the next call), which also releases the
+          // others, who wait (bounded) for that.  An arrival that finds the
+          // counter at n or more (it was not zero when the call started)
+          // reports it and writes NaN rows.
+          if (ctid == 0) {
+            __threadfence();
+            const uint32_t n = static_cast<uint32_t>(cl - cf + 1);
+            const uint32_t nc = min(n, static_cast<uint32_t>(nh));
+            const uint32_t k = atomicAdd(&p.cnt[u], 1u);
+            int role = -1;
+            if (k >= n) {
+              report_failure(p, sm, KVQ_STATUS_COUNTER);
+              role = -2;
+            } else if (k == n - 1) {
+              __threadfence();
+              atomicExch(&p.cnt[u], 0u);
+              role = static_cast<int>(nc) - 1;
+            } else if (k >= n - nc) {
+              role = static_cast<int>(k - (n - nc));
+              if (!wait_unit_released(&p.cnt[u], p.peer_polls)) report_failure(p, sm, KVQ_STATUS_PEER_WAIT);
+            }
+            __threadfence();
+            sm.role = role;
+            sm.ncomb = static_cast<int>(nc);
+          }
+          named_bar(1, kConsumerWarps * 32);
+          const int role = sm.role, nc = sm.ncomb;
+          if (role == -2) {  // corrupt counter: every row of the unit becomes NaN
+            for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
+              const int j = idx / kD, d = idx - j * kD;
+              const int64_t orow = out_row(j);
+              p.out[orow * kD + d] = 0x7fffu;  // bf16 NaN
+              if (d == 0 && p.lse) p.lse[orow] = __int_as_float(0x7fffffff);
+            }
+          } else if (role >= 0) {
+            const bool bad = sm.abort != 0;
+            float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
+            float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.mbuf[0][0][0]);
+            for (int j = role; j < nh; j += nc)
+              combine_row<kConsumerWarps>(p, u, j, cf, cl, out_row(j), warp, lane, sm_ml, sm_o, bad,
+                                          []() { named_bar(1, kConsumerWarps * 32); });
+          }
         }
       }
     }
@@ -1465,7 +1466,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
 // NHP: 16-row MMA halves per packed block (2 or 4; the launch's pk_halves).
 // kGen: the general variant -- K-only protected heads (a third unit class)
 // and multi-query columns; the other variants run neither.
-template <int KB, int VB, int G, bool kStep, int NHP, bool kGen>
+template <int KB, int VB, int G, bool kStep, int NHP, bool kGen, bool kCl>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -1483,7 +1484,7 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
     fence_barrier_init();
   }
   __syncthreads();
-  if (p.plan.cs > 1) {
+  if constexpr (kCl) {
     // Cluster mode: each CTA expects the other ranks' partials of its column
     // as transaction bytes.  The cluster barrier, arrived at here and waited
     // for before the first store into another CTA (consumers) or before the
@@ -1495,12 +1496,12 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
   if (warp == kConsumerWarps) {
     uint32_t pre = 0;
     if (lane == 0) {
-      pre = producer_preload<kStep, kGen>(p, sm, blockIdx.x);
+      pre = producer_preload<kStep, kGen, kCl>(p, sm, blockIdx.x);
       prefetch_q<kGen>(p, blockIdx.x);
-      if (pre == 0) producer_prefetch<kGen>(p, blockIdx.x, 0);
+      if (pre == 0) producer_prefetch<kGen, kCl>(p, blockIdx.x, 0);
     }
     __syncwarp();
-    if (p.plan.cs > 1) cluster_wait();
+    if constexpr (kCl) cluster_wait();
     pdl_wait();  // the previous kernel in the stream may have written the cache, k_new, v_new
     if constexpr (kStep) write_step_rows<kGen>(p, blockIdx.x, lane);
     __syncwarp();
@@ -1509,12 +1510,12 @@ __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params
       // here on: this CTA is past its dependency wait and its cache writes
       // are fenced.
       pdl_launch_dependents();
-      if (pre > 0) producer_prefetch<kGen>(p, blockIdx.x, pre);
-      producer_loop<kStep, kGen>(p, sm, blockIdx.x, pre);
+      if (pre > 0) producer_prefetch<kGen, kCl>(p, blockIdx.x, pre);
+      producer_loop<kStep, kGen, kCl>(p, sm, blockIdx.x, pre);
     }
     return;
   }
-  consumer_loop<KB, VB, G, kStep, NHP, kGen>(p, sm, blockIdx.x, warp, lane);
+  consumer_loop<KB, VB, G, kStep, NHP, kGen, kCl>(p, sm, blockIdx.x, warp, lane);
 }
 
 }  // namespace kvq

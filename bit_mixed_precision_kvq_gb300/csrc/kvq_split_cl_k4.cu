@@ -1,0 +1,9 @@
+// Cluster-mode instantiations of the split-KV kernel for K bit-width 4
+// (the same variants as the global-mode ones).
+#include "kvq_split_inst.cuh"
+
+namespace kvq {
+const void* split_kernel_cl_k4(int vb, int G, bool step, int halves, bool general) {
+  return split_inst::dispatch<4, true>(vb, G, step, halves, general);
+}
+}  // namespace kvq

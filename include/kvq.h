@@ -398,11 +398,13 @@ void kvq_set_wait_limits(uint32_t tile_polls, uint32_t peer_polls);
  * kvq_set_cache_preload -- for decode calls made later from the calling host
  * thread: with enable != 0, the uniform single-query calls
  * (kvq_decode_attention, kvq_decode_attention_static_ws,
- * kvq_decode_attention_mq with n_q = 1, kvq_decode_step) copy each CTA's
- * first cache tiles into shared memory before the previous kernel in the
- * stream has finished (programmatic dependent launch), so a chain of
- * layers overlaps one layer's cache reads with the previous layer's work.
- * Only cache rows are read early; q, k_new and v_new after the wait.
+ * kvq_decode_attention_mq with n_q = 1, kvq_decode_step) that run in
+ * cluster mode (see kvq_decode_step: every unit's share of a CTA fits its
+ * shared-memory ring) copy each CTA's first cache tiles into shared memory
+ * before the previous kernel in the stream has finished (programmatic
+ * dependent launch), so a chain of layers overlaps one layer's cache reads
+ * with the previous layer's work.  Only cache rows are read early; q, k_new
+ * and v_new after the wait.
  *
  * Requirement: every kernel that writes the cache before the call in its
  * stream is a call of this library, or the host synchronises with it (or
