@@ -241,8 +241,10 @@ kvq_status decode_params(const kvq_layout* L, const void* cache, const void* q_b
 
 // One CTA per SM: the stage ring, merge buffers and barriers must fit the
 // 227 KiB a CTA may use.
-constexpr size_t kSplitSmemBytes = sizeof(kvq::SplitSmem);
-static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one CTA's limit");
+constexpr size_t kSplitSmemCl = sizeof(kvq::SplitSmem<true>);   // cluster mode
+constexpr size_t kSplitSmemGl = sizeof(kvq::SplitSmem<false>);  // global mode
+static_assert(kSplitSmemCl <= 232448 && kSplitSmemGl <= 232448, "split kernel shared memory exceeds one CTA's limit");
+size_t split_smem(const kvq::Params* p) { return p->plan.cs > 1 ? kSplitSmemCl : kSplitSmemGl; }
 
 
 // Launch the split kernel: one CTA per chunk, programmatic serialisation
@@ -251,8 +253,8 @@ static_assert(kSplitSmemBytes <= 232448, "split kernel shared memory exceeds one
 // requested (the global-mode fused step, whose combining CTAs may wait for
 // other CTAs of their unit).  Programmatic serialisation is dropped if the
 // runtime refuses it.
-kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool cooperative,
-                        size_t smem = kSplitSmemBytes, int threads = kvq::kSplitThreads) {
+kvq_status launch_split(const void* fn, kvq::Params* p, void* stream, bool cooperative, size_t smem,
+                        int threads = kvq::kSplitThreads) {
   static std::atomic<int> pdl_ok{1};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p->plan.C);
@@ -301,13 +303,13 @@ kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const vo
   const void* fn_cl = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, true);
   if (!fn_cl) return KVQ_ERR_UNSUPPORTED;
   int max_clusters = 0;
-  kvq_status st = prepare_split(fn_cl, kSplitSmemBytes, &max_clusters);
+  kvq_status st = prepare_split(fn_cl, kSplitSmemCl, &max_clusters);
   if (st != KVQ_OK) return st;
   if (!use_cluster_mode(p->plan, max_clusters)) {
     p->preload = 0;  // early copies are a cluster-mode feature (a CTA's whole piece fits its ring)
     *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, false);
     if (!*fn) return KVQ_ERR_UNSUPPORTED;
-    return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
+    return prepare_split(*fn, kSplitSmemGl, &max_clusters);
   }
   p->plan.cs = kClusterCtas;
   kvq_plan_cuts(&p->plan, p->cuts);
@@ -316,7 +318,7 @@ kvq_status choose_split(const kvq_layout* L, kvq::Params* p, bool step, const vo
   if (!tile_geometry_ok(p)) return KVQ_ERR_UNSUPPORTED;
   *fn = split_kernel_for(L->d.k_bits, L->d.v_bits, L->d.group_size, step, p->pk_halves, general, true);
   if (!*fn) return KVQ_ERR_UNSUPPORTED;
-  return prepare_split(*fn, kSplitSmemBytes, &max_clusters);
+  return prepare_split(*fn, kSplitSmemCl, &max_clusters);
 }
 
 // The split kernel and, in global mode, the combine of one decode call (p
@@ -325,7 +327,7 @@ kvq_status launch_decode(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* split = nullptr;
   kvq_status st = choose_split(L, p, false, &split);
   if (st != KVQ_OK) return st;
-  st = launch_split(split, p, stream, false);
+  st = launch_split(split, p, stream, false, split_smem(p));
   if (st != KVQ_OK || p->plan.cs > 1) return st;
   const bool wide = kvq::plan_max_unit_chunks(p->plan, p->cuts) > 16;
   const void* comb = wide ? reinterpret_cast<const void*>(&kvq::combine_kernel<16>)
@@ -351,7 +353,7 @@ kvq_status launch_step(const kvq_layout* L, kvq::Params* p, void* stream) {
   const void* fn = nullptr;
   const kvq_status st = choose_split(L, p, true, &fn);  // the fused step is single-query
   if (st != KVQ_OK) return st;
-  return launch_split(fn, p, stream, true);
+  return launch_split(fn, p, stream, true, split_smem(p));
 }
 
 // The parameter block of a call is built on the calling host thread and

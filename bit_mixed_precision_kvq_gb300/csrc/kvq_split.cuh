@@ -42,7 +42,8 @@ namespace kvq {
 // allow 168 registers per thread.
 constexpr int kConsumerWarps = 11;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 5;                     // 5 x 40 KB = 200 KB in flight per CTA
+constexpr int kStagesCl = 5;                   // cluster mode: 5 x 40 KB = 200 KB in flight per CTA
+constexpr int kStagesGl = 4;                   // global mode: 4 x 40 KB (its warp merge needs 46 KB)
 constexpr int kTileBf16 = 80;                  // positions per bf16 tile: 80 * 512 B = 40 KB
 constexpr int kBf16VOff = kTileBf16 * 2 * kD;  // V rows start 20 KB into a bf16 stage
 // Cluster mode: text tiles of at most 16 rows (a text prefix, the step's
@@ -58,26 +59,41 @@ constexpr int kMaxClusterCtas = 16;            // cluster mode: CTAs per cluster
 // Cluster mode: one rank's partial of a column (o row, then M and L).
 constexpr uint32_t kRecvBytes = (kD + 2) * 4;
 
-struct SplitSmem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];
-  alignas(128) uint8_t tstage[kTextStageBytes];  // cluster mode: short text tiles
-  union {
-    // Global mode: merge of the consumer warps' rows -- warps 3r .. 3r + 2
-    // fold their scaled o rows into the three buffers in round r (a fixed
-    // order, so results are reproducible bit for bit).
-    float mbuf[3][kNH][kD + 4];  // padded rows: fewer bank conflicts
-    // Cluster mode: CTA rank j receives column j's partial of every rank r
-    // here (o row, then M and L), stored by rank r.
-    float recv[kMaxClusterCtas][kD + 4];
-  };
+// Shared memory of the split kernel, per combine mode.
+template <bool kCl>
+struct SplitSmem;
+
+template <>
+struct SplitSmem<true> {  // cluster mode
+  static constexpr int kRing = kStagesCl;
+  alignas(128) uint8_t stage[kRing][kStageBytes];
+  alignas(128) uint8_t tstage[kTextStageBytes];  // short text tiles
+  // CTA rank j receives column j's partial of every rank r here (o row,
+  // then M and L), stored by rank r.
+  alignas(16) float recv[kMaxClusterCtas][kD + 4];
   float merge_ml[kConsumerWarps][kNH][2];
-  float merge_sc[kConsumerWarps][kNH];         // exp2(m_warp - M) per (warp, column)
-  float merge_ML[kNH][2];                      // the CTA's (M, L) per column
   float qsum[kConsumerWarps][kNH][4];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kRing];
+  uint64_t empty[kRing];
   uint64_t full_t, empty_t;  // the text stage
-  uint64_t recv_bar;  // cluster mode: the other ranks' partials landed (transaction bytes)
+  uint64_t recv_bar;         // the other ranks' partials landed (transaction bytes)
+  int abort;
+  int role, ncomb;           // (global mode only)
+};
+
+template <>
+struct SplitSmem<false> {  // global mode
+  static constexpr int kRing = kStagesGl;
+  alignas(128) uint8_t stage[kRing][kStageBytes];
+  alignas(128) uint8_t tstage[16];  // (no text stage in global mode)
+  // the consumer warps' o rows at a unit's end, merged after one barrier
+  alignas(16) float merge_o[kConsumerWarps][kNH][kD + 4];  // padded rows: fewer bank conflicts
+  float merge_ml[kConsumerWarps][kNH][2];
+  float qsum[kConsumerWarps][kNH][4];
+  uint64_t full[kRing];
+  uint64_t empty[kRing];
+  uint64_t full_t, empty_t;  // (unused)
+  uint64_t recv_bar;         // (unused)
   int abort;
   int role;   // fused step: combine role of this CTA for the current unit
   int ncomb;  // fused step: CTAs combining the current unit
@@ -85,7 +101,8 @@ struct SplitSmem {
 
 // A bounded wait gave up (or a counter was found corrupt): mark the call's
 // status word and this CTA's outputs.
-__device__ __forceinline__ void report_failure(const Params& p, SplitSmem& sm, uint32_t bit) {
+template <typename Sm>
+__device__ __forceinline__ void report_failure(const Params& p, Sm& sm, uint32_t bit) {
   sm.abort = 1;
   if (p.status) atomicOr(p.status, bit);
 }
@@ -226,7 +243,7 @@ struct TileSeq {
 // Issue the bulk copies of one tile into its stage (waiting, bounded, for the
 // stage's previous tile to be released) and advance the sequence.
 template <bool kStep, bool kGen, bool kCl>
-__device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const UnitInfo& ui, int Tu, int kind,
+__device__ __forceinline__ void issue_tile(const Params& p, SplitSmem<kCl>& sm, const UnitInfo& ui, int Tu, int kind,
                                            int t0, int n, TileSeq& seq) {
   uint8_t* dst;
   uint64_t* full;
@@ -239,8 +256,9 @@ __device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const
     voff = kTextVOff;
     ++seq.t;
   } else {
-    const int st = seq.r % kStages;
-    const uint32_t round = seq.r / kStages;
+    constexpr int kRing = SplitSmem<kCl>::kRing;
+    const int st = seq.r % kRing;
+    const uint32_t round = seq.r / kRing;
     if (round > 0 && !mbar_wait(&sm.empty[st], (round - 1) & 1, p.tile_polls))
       report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
     dst = sm.stage[st];
@@ -266,13 +284,13 @@ __device__ __forceinline__ void issue_tile(const Params& p, SplitSmem& sm, const
 // the caller enables it only where no other kernel writes the cache just
 // before.  Returns the number of tiles issued.
 template <bool kStep, bool kGen, bool kCl>
-__device__ __forceinline__ uint32_t producer_preload(const Params& p, SplitSmem& sm, int c) {
+__device__ __forceinline__ uint32_t producer_preload(const Params& p, SplitSmem<kCl>& sm, int c) {
   if (!kCl || !p.preload || p.seq_len != nullptr) return 0;
   uint32_t it = 0;
   TileSeq seq;
   bool stop = false;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
-    const bool full = in_text_stage<kCl>(kind, n) ? seq.t >= 1 : seq.r >= static_cast<uint32_t>(kStages);
+    const bool full = in_text_stage<kCl>(kind, n) ? seq.t >= 1 : seq.r >= static_cast<uint32_t>(SplitSmem<kCl>::kRing);
     if (stop || full || (kStep && kind == kTileText && t0 + n == Tu)) {
       stop = true;
       return;
@@ -358,7 +376,7 @@ __device__ __forceinline__ void write_step_rows(const Params& p, int c, int lane
 // After the dependency wait: the CTA's tiles from ring position `skip` on
 // (the first `skip` were issued by producer_preload).
 template <bool kStep, bool kGen, bool kCl>
-__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem& sm, int c, uint32_t skip) {
+__device__ __forceinline__ void producer_loop(const Params& p, SplitSmem<kCl>& sm, int c, uint32_t skip) {
   uint32_t it = 0;
   TileSeq seq;
   walk_chunk<kGen, kStep, true>(p, c, [&](const UnitInfo& ui, int Tu, int kind, int t0, int n) {
@@ -1044,7 +1062,7 @@ __device__ __forceinline__ bool wait_unit_released(const uint32_t* cnt, uint32_t
 // the staged-tile ring, idle now (one unit per CTA).  CTA rank j < nh then
 // waits (bounded) for the other ranks' slots and writes column j's output
 // row, orow; a CTA that receives nothing is done once its stores are issued.
-__device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem& sm, const Acc& acc, bool prot,
+__device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem<true>& sm, const Acc& acc, bool prot,
                                                      int nh, int64_t orow, int warp, int lane) {
   constexpr int kPitch = kD + 4;  // padded rows: the fragment stores spread over the banks
   const int gid = lane >> 2, tig = lane & 3;
@@ -1142,7 +1160,8 @@ __device__ __forceinline__ void cluster_push_combine(const Params& p, SplitSmem&
 }
 
 template <int KB, int VB, int G, bool kStep, int NHP, bool kGen, bool kCl>
-__device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, int c, int warp, int lane) {
+__device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem<kCl>& sm, int c, int warp, int lane) {
+  constexpr int kRing = SplitSmem<kCl>::kRing;
   const int gid = lane >> 2, tig = lane & 3;
   const int ctid = warp * 32 + lane;  // 0 .. 32*kConsumerWarps-1
   const Cut a = p.cuts[c];
@@ -1235,16 +1254,16 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     bool in_text = false;
     auto begin_tile = [&](int kind, int, int n) -> const uint8_t* {
       in_text = in_text_stage<kCl>(kind, n);
-      uint64_t* full = in_text ? &sm.full_t : &sm.full[seq.r % kStages];
-      const uint32_t parity = in_text ? (seq.t & 1) : ((seq.r / kStages) & 1);
+      uint64_t* full = in_text ? &sm.full_t : &sm.full[seq.r % kRing];
+      const uint32_t parity = in_text ? (seq.t & 1) : ((seq.r / kRing) & 1);
       if (!mbar_wait(full, parity, p.tile_polls)) report_failure(p, sm, KVQ_STATUS_TILE_WAIT);
       voff = in_text ? kTextVOff : kBf16VOff;
-      return in_text ? sm.tstage : sm.stage[seq.r % kStages];
+      return in_text ? sm.tstage : sm.stage[seq.r % kRing];
     };
     // Release the tile's stage once this warp is done with it.
     auto end_tile = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(in_text ? &sm.empty_t : &sm.empty[seq.r % kStages]);
+      if (lane == 0) mbar_arrive(in_text ? &sm.empty_t : &sm.empty[seq.r % kRing]);
       if (in_text) ++seq.t;
       else ++seq.r;
       ++it;
@@ -1335,67 +1354,45 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
     int cf = c, cl = c;
     if constexpr (kStep) plan_unit_chunks(p.plan, p.cuts, u, &cf, &cl);
     const bool sole = kStep && !cluster && cf == cl;
-    named_bar(1, kConsumerWarps * 32);
     if constexpr (kCl) {
+      named_bar(1, kConsumerWarps * 32);  // every tile consumed, merge_ml published
       cluster_push_combine(p, sm, acc, ui.prot, nh, out_row(static_cast<int>(cluster_ctarank()) < nh
                                                                     ? static_cast<int>(cluster_ctarank()) : 0),
                            warp, lane);
     } else {
-      // Per column: the CTA's running max M and sum L, and each warp's weight.
-      if (ctid < kNH) {
-        const int j = ctid;
-        float M = -INFINITY;
-  #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
-        float L = 0.f;
-  #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float m = sm.merge_ml[w][j][0];
-          const float sc = (M == -INFINITY) ? 0.f : exp2f(m - M);
-          sm.merge_sc[w][j] = sc;
-          L = fmaf(sm.merge_ml[w][j][1], sc, L);
-        }
-        if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
-        sm.merge_ML[j][0] = M;
-        sm.merge_ML[j][1] = L;
-      }
-      named_bar(1, kConsumerWarps * 32);
-      // The warps' scaled o rows into the three buffers, three warps a round.
-      // Output rows: protected units d = 16 gid + mt (+ 8); packed units
-      // d = 16 mt + gid (+ 8) (two compile-time patterns).
-      auto put_rows = [&](float (*buf)[kD + 4], bool add, int dbase, int dstep) {
-        const float s0 = sm.merge_sc[warp][2 * tig], s1 = sm.merge_sc[warp][2 * tig + 1];
-  #pragma unroll
+      // Every warp's o rows as they are (output rows: protected units
+      // d = 16 gid + mt (+ 8), packed units d = 16 mt + gid (+ 8)); after one
+      // barrier each thread forms (column j, element d) from all warps in
+      // warp order (reproducible bit for bit).
+      auto store_rows = [&](int dbase, int dstep) {
+#pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const int d0 = dbase + dstep * mt, d1 = d0 + 8;
-          float* r0 = &buf[2 * tig][0];
-          float* r1 = &buf[2 * tig + 1][0];
-          if (add) {
-            r0[d0] += acc.o[mt][0] * s0;
-            r1[d0] += acc.o[mt][1] * s1;
-            r0[d1] += acc.o[mt][2] * s0;
-            r1[d1] += acc.o[mt][3] * s1;
-          } else {
-            r0[d0] = acc.o[mt][0] * s0;
-            r1[d0] = acc.o[mt][1] * s1;
-            r0[d1] = acc.o[mt][2] * s0;
-            r1[d1] = acc.o[mt][3] * s1;
-          }
+          sm.merge_o[warp][2 * tig][d0] = acc.o[mt][0];
+          sm.merge_o[warp][2 * tig + 1][d0] = acc.o[mt][1];
+          sm.merge_o[warp][2 * tig][d1] = acc.o[mt][2];
+          sm.merge_o[warp][2 * tig + 1][d1] = acc.o[mt][3];
         }
       };
-  #pragma unroll 1
-      for (int round = 0; round < (kConsumerWarps + 2) / 3; ++round) {
-        if (warp / 3 == round) {
-          if (ui.prot) put_rows(sm.mbuf[warp % 3], round > 0, 16 * gid, 1);
-          else put_rows(sm.mbuf[warp % 3], round > 0, gid, 16);
-        }
-        named_bar(1, kConsumerWarps * 32);
-      }
+      if (ui.prot) store_rows(16 * gid, 1);
+      else store_rows(gid, 16);
+      named_bar(1, kConsumerWarps * 32);
       const int64_t slot = static_cast<int64_t>(u) + c;
       for (int idx = ctid; idx < nh * kD; idx += kConsumerWarps * 32) {
         const int j = idx / kD, d = idx - j * kD;
-        const float O = (sm.mbuf[0][j][d] + sm.mbuf[1][j][d]) + sm.mbuf[2][j][d];
-        const float M = sm.merge_ML[j][0], L = sm.merge_ML[j][1];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_ml[w][j][0]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float sc = exp2f(sm.merge_ml[w][j][0] - M);
+            L = fmaf(sm.merge_ml[w][j][1], sc, L);
+            O = fmaf(sm.merge_o[w][j][d], sc, O);
+          }
+        }
+        if (sm.abort) M = __int_as_float(0x7fffffff);  // NaN marks a failed wait
         if (sole) {
           const float inv = (M != M) ? M : (L > 0.f ? 1.0f / L : 0.f);  // L = 0: inactive sequence
           const int64_t orow = out_row(j);
@@ -1452,7 +1449,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
           } else if (role >= 0) {
             const bool bad = sm.abort != 0;
             float (*sm_ml)[2] = reinterpret_cast<float (*)[2]>(&sm.merge_ml[0][0][0]);
-            float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.mbuf[0][0][0]);
+            float4 (*sm_o)[32] = reinterpret_cast<float4 (*)[32]>(&sm.merge_o[0][0][0]);
             for (int j = role; j < nh; j += nc)
               combine_row<kConsumerWarps>(p, u, j, cf, cl, out_row(j), warp, lane, sm_ml, sm_o, bad,
                                           []() { named_bar(1, kConsumerWarps * 32); });
@@ -1469,11 +1466,11 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem& sm, in
 template <int KB, int VB, int G, bool kStep, int NHP, bool kGen, bool kCl>
 __global__ void __maxnreg__(168) split_mma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
+  SplitSmem<kCl>& sm = *reinterpret_cast<SplitSmem<kCl>*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < SplitSmem<kCl>::kRing; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
