@@ -1172,6 +1172,26 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem<kCl>& s
   uint32_t it = 0;    // tiles seen
   TileSeq seq;        // ... of them in the ring and in the text stage
   uint32_t gblk = 0;  // 32-position blocks dealt so far (round-robin over warps)
+  // q of unit uu for lane (gid, tig): elements 32P + 8 tig .. + 7 of head
+  // column gid, P = 0..3 (zero past the unit's columns), through L2 (the
+  // previous kernel may have written q).  In global mode with 32-position
+  // blocks (short units, several per CTA) the next unit's loads are issued
+  // before this unit's warp merge, so they land during it; the other
+  // kernels load q at the unit's start.
+  constexpr bool kPrefQ = !kCl && NHP == 2;
+  uint4 qraw[4];
+  auto load_q = [&](int uu, uint4 (&r)[4]) {
+    const UnitInfo un = unit_info<kGen>(p, uu);
+    const int c0n = un.hc * kNH;
+    const int nhn = kGen ? min(kNH, p.g * p.n_q - c0n) : min(kNH, p.g - c0n);
+    int64_t row;
+    if constexpr (kGen) row = col_row(p, un.b, un.h, c0n + (gid < nhn ? gid : 0));
+    else row = static_cast<int64_t>(un.b) * p.Hq + un.h * p.g + c0n + gid;
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+      r[P] = gid < nhn ? __ldcg(reinterpret_cast<const uint4*>(p.q + row * kD + 32 * P + 8 * tig))
+                       : make_uint4(0u, 0u, 0u, 0u);
+  };
   for (int u = a.u; u <= u_last; ++u) {
     const UnitInfo ui = unit_info<kGen>(p, u);
     // The unit's columns: query heads h*g + hc*kNH + j; in the general
@@ -1183,7 +1203,10 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem<kCl>& s
       if constexpr (kGen) return col_row(p, ui.b, ui.h, c0 + j);
       else return static_cast<int64_t>(ui.b) * p.Hq + hq0 + j;
     };
-    if (u == a.u) pdl_wait();  // q (and the cache) may come from the previous kernel
+    if (u == a.u) {
+      pdl_wait();  // q (and the cache) may come from the previous kernel
+      if constexpr (kPrefQ) load_q(u, qraw);
+    }
     const int Tu = seq_end<kStep>(p, ui.b);
     const int pe = min((u == e.u) ? e.p : p.plan.T, Tu);
     const int ps = min((u == a.u) ? a.p : 0, pe);
@@ -1198,9 +1221,11 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem<kCl>& s
 #pragma unroll
     for (int P = 0; P < 4; ++P) {
       uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (gid < nh)
-        raw = __ldcg(reinterpret_cast<const uint4*>(
-            p.q + out_row(gid) * kD + 32 * P + 8 * tig));  // L2 path: written by the previous kernel
+      if constexpr (kPrefQ) {
+        raw = qraw[P];
+      } else if (gid < nh) {
+        raw = __ldcg(reinterpret_cast<const uint4*>(p.q + out_row(gid) * kD + 32 * P + 8 * tig));
+      }
       const float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
                           bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
       qb[2 * P][0] = pack_f16x2(x[0], x[4]);
@@ -1334,6 +1359,9 @@ __device__ __forceinline__ void consumer_loop(const Params& p, SplitSmem<kCl>& s
 
     if constexpr (VB < 16) {
       if (packed_acc) acc_to_true<VB, G>(acc, tig);
+    }
+    if constexpr (kPrefQ) {
+      if (u < u_last) load_q(u + 1, qraw);
     }
     // ---- merge the warps' states and write the partial of (u, c) ----
 #pragma unroll
