@@ -287,3 +287,38 @@ def test_mq_argument_checks(lib):
     st = lib.kvq_decode_attention_mq(ctypes.byref(L0), FAKE, FAKE, 4, 12, 0.1, FAKE, None, FAKE,
                                      kvq.decode_mq_workspace_bytes(L0, 4) - 1, None)
     assert st == 3  # past the position check, stopped by the workspace size
+
+
+def test_concurrent_argument_checks_from_two_threads(lib):
+    """Decode entry points keep no process-wide state: calls from several
+    host threads run at once (ctypes releases the GIL) and each gets its own
+    status, with no lock between them."""
+    import threading
+    L = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+    ws = L.workspace_bytes
+    errors = []
+
+    def worker(kind, n):
+        try:
+            for i in range(n):
+                if kind == 0:  # T out of range -> KVQ_ERR_INVALID_ARG
+                    with pytest.raises(kvq.KvqError) as e:
+                        kvq.decode_attention(L, FAKE, FAKE, 257, FAKE, 0.1, 0, FAKE, ws, stream=0)
+                    assert e.value.status == 1
+                elif kind == 1:  # workspace too small -> KVQ_ERR_CAPACITY
+                    with pytest.raises(kvq.KvqError) as e:
+                        kvq.decode_step(L, FAKE, FAKE, FAKE, FAKE, 220, FAKE, 0.1, 0, FAKE, ws - 1, stream=0)
+                    assert e.value.status == 3
+                else:  # layouts built concurrently agree with one built alone
+                    L2 = kvq.cache_layout(2, 8, 4, 128, 256, 10, 200, 4, 4, 32, [1])
+                    assert L2.workspace_bytes == ws and L2.total_bytes == L.total_bytes
+        except BaseException as exc:  # noqa: BLE001 -- reported below
+            errors.append((kind, repr(exc)))
+
+    threads = [threading.Thread(target=worker, args=(k, 2000)) for k in (0, 1, 2, 0, 1)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors[:3]
